@@ -1,0 +1,62 @@
+// common.cuh -- device helpers shared by the TwELL kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "twell.h"
+
+namespace twell {
+
+using bf16 = __nv_bfloat16;
+
+// ---- element conversions ---------------------------------------------------
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+
+template <class T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// bf16 pair packed in a 32-bit word -> two floats (exact widening).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> bf16 pair (round to nearest even), low half = a.
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// Bit pattern of the storage value of v (for assembling vector stores).
+__device__ __forceinline__ uint32_t store_bits(float v, float *) { return __float_as_uint(v); }
+__device__ __forceinline__ uint32_t store_bits(float v, bf16 *) {
+  bf16 b = __float2bfloat16_rn(v);
+  return (uint32_t)(*reinterpret_cast<uint16_t *>(&b));
+}
+
+// 16-byte read-only load that does not allocate in L1 (streamed weight rows).
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---- device status word ------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t *st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ---- control block in the workspace -----------------------------------------
+// Written by the overflow-compaction kernel, read by everything after it.
+struct Ctl {
+  int32_t n_rows;   // rows on the dense path (overflow rows, or T in dense mode)
+  int32_t dense;    // 1: every row runs densely (n_ovf > dense_switch * T)
+  int32_t n_ovf;    // true number of overflow rows
+  int32_t pad[13];
+};
+
+}  // namespace twell

@@ -1,0 +1,104 @@
+// kernels.h -- host-side launchers of the TwELL kernels (internal to libtwell).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "twell.h"
+
+namespace twell {
+
+struct Ctl;
+
+// Workspace carve-up shared by all entry points.
+struct Workspace {
+  Ctl *ctl;           // control block
+  int32_t *rows;      // [T] rows of the dense path (hybrid: overflow rows)
+  int32_t *pos;       // [T] overflow position of each row, -1 if none
+  void *h;            // [T][F] dtype: h rows of the dense path
+  void *xg;           // [T][D] dtype: gathered x rows of the dense path
+  // backward scratch
+  float *dz;          // [F/C][T][K] fp32: dz at the slots
+  float *du;          // [F/C][T][K] fp32: du at the slots
+  float *hs;          // [F/C][T][K] fp32: h at the slots
+  int32_t *col_ptr;   // [F+1] neuron-major (transposed) pointers
+  int32_t *col_cnt;   // [F]   per-neuron counts / cursors
+  int32_t *col_tok;   // [T*(F/C)*K] token of each transposed entry
+  int32_t *col_slot;  // [T*(F/C)*K] slot of each transposed entry
+  void *dzr;          // [T][F] dtype: dz rows of the dense path
+  void *dur;          // [T][F] dtype: du rows of the dense path
+  void *dyg;          // [T][D] dtype: gathered dy rows of the dense path
+  size_t bytes;       // total bytes needed
+};
+
+// Lay out (or size, when base == nullptr) the workspace.
+Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train);
+
+struct FwdArgs {
+  int T, D, F, C, K, dtype, gated, train;
+  const void *x, *Wg, *Wu, *Wd;
+  const float *bg, *rb;
+  twell_t tw;
+  void *y;
+  Workspace ws;
+  float dense_switch;
+};
+
+struct BwdArgs {
+  int T, D, F, C, K, dtype, gated;
+  const void *x, *Wg, *Wu, *Wd, *dy;
+  twell_t tw;
+  float lambda;
+  void *dx;
+  float *dWg, *dbg, *dWu, *dWd;
+  Workspace ws;
+};
+
+// pack.cu
+cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
+cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
+                                    cudaStream_t s);
+cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s);
+cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
+                               int dtype, cudaStream_t s);
+
+// simt_gemm.cu (fp32 path)
+cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_simt_dense_gu(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_simt_dense_down(const FwdArgs &a, cudaStream_t s);
+
+// tc_gemm.cu (bf16 tensor-core path)
+bool tc_available();
+cudaError_t launch_tc_gate_pack(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s);
+
+// Kernel identities for the optional per-launch timing (twell_profile_*).
+enum KernelId {
+  KID_START = -1,
+  KID_GATE_PACK = 0,
+  KID_OVERFLOW_COMPACT = 1,
+  KID_UPDOWN = 2,
+  KID_GATHER_ROWS = 3,
+  KID_DENSE_GU = 4,
+  KID_DENSE_DOWN = 5,
+  KID_PACK_DENSE = 6,
+  KID_COPY_FB = 7,
+  KID_BWD_SLOTS = 8,
+  KID_BWD_DX = 9,
+  KID_BWD_TRANSPOSE = 10,
+  KID_BWD_DW = 11,
+  KID_BWD_DENSE = 12,
+  KID_COUNT = 13
+};
+// Record a timing event after a launch of kernel `id` (no-op unless enabled).
+void prof_mark(int id, cudaStream_t s);
+
+// updown.cu
+cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);
+
+// backward.cu
+cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s);
+
+}  // namespace twell

@@ -1,0 +1,675 @@
+// tc_gemm.cu -- tcgen05 (5th-generation tensor core) GEMM engine for the bf16
+// path, with the epilogues of the TwELL FFN:
+//   EPI_PACK : z = x Wg^T + bg + rb -> ReLU -> TwELL slots + nnz     (gate)
+//   EPI_GU   : dual B (Wg, Wu): g = ReLU(z) rounded to bf16, u, h = g*u
+//              -> h rows (+ g_fb / u_fb rows of overflow rows)       (dense rows)
+//   EPI_DOWN : y[tok] = h Wd, Wd read MN-major straight from [F][D]   (dense rows)
+//   EPI_F32  : plain fp32 C = A B^T or A B (test hook)
+//
+// "Sparser, Faster, Lighter Transformer Language Models", technical summary
+// section 2.A: TwELL is materialised in the epilogue of an optimised dense
+// matmul, with no synchronisation between CTAs; each CTA owns whole tiles.
+//
+// Structure (one CTA per SM, persistent over output tiles, 192 threads):
+//   warp 0      TMA producer: A and B tiles (128B-swizzled) into a ring of
+//               shared-memory stages, completion counted on mbarriers.
+//   warp 1      allocates TMEM; one elected lane issues tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 in, fp32 accumulate in TMEM) and
+//               commits each stage back to the producer and each finished
+//               accumulator to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld 32x32b (thread = accumulator row),
+//               fused element-wise work and stores.  Two TMEM accumulators
+//               alternate so the epilogue of tile i overlaps the MMAs of i+1.
+// Every mbarrier wait is bounded by a 2-second global-timer limit; on expiry
+// the CTA records TWELL_ERR_TIMEOUT in the status word, drains, frees its TMEM
+// and returns.
+#include <cuda.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_test.h"
+
+namespace twell {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, NTHREADS = 192;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3 };
+
+// ---------------------------------------------------------------- PTX ----
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait.  Returns false (and raises the CTA-wide abort flag and the
+// device status) when the limit expires or another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      set_status(status, TWELL_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a 128B-swizzled operand tile.
+//  [0,14) start>>4  [16,30) LBO>>4  [32,46) SBO>>4  [46,48) version 1
+//  [61,64) layout 2 = SWIZZLE_128B
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D=f32, A=B=bf16, A K-major, B K- or
+// MN-major, N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.  The
+// wait is inside the same asm statement, so no use of the outputs can be
+// scheduled before the load has completed.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar() {  // named barrier of the 4 epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// --------------------------------------------------------------- params --
+struct TcParams {
+  int M_host;              // rows when m_dev == nullptr
+  const int32_t *m_dev;    // device row count (dense path: ctl->n_rows)
+  const Ctl *ctl;          // dense-path control (EPI_GU / EPI_DOWN), else null
+  int N, Kdim;             // output columns, contraction length
+  int Tn, F, D, C, Kslots, cap, gated, train;
+  const float *bg, *rb;
+  const int32_t *rows, *pos;
+  uint8_t *idx, *nnz;
+  bf16 *val;
+  bf16 *h, *g_fb, *u_fb, *y;
+  float *out;              // EPI_F32
+  int32_t *status;
+};
+
+template <int BN, int NB, bool B_MN, int EPI>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+  static constexpr int TMEM_COLS_USED = 2 * NB * BN;
+  static constexpr int TMEM_COLS = TMEM_COLS_USED <= 32 ? 32 : TMEM_COLS_USED <= 64 ? 64
+                                   : TMEM_COLS_USED <= 128 ? 128 : TMEM_COLS_USED <= 256 ? 256
+                                                                                         : 512;
+  static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 : 0;  // idx + bf16 val, K<=32
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
+  static_assert(STAGES >= 2, "too few stages");
+  static_assert(TMEM_COLS_USED <= 512, "TMEM overflow");
+};
+
+}  // namespace
+
+template <int BN, int NB, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
+               const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+               TcParams p) {
+  using CF = Cfg<BN, NB, B_MN, EPI>;
+  constexpr int S = CF::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *stages = smem;
+  // full[S] empty[S] tfull[2] tempty[2] mma_done
+  uint64_t *bars = (uint64_t *)(smem + S * CF::STAGE_BYTES);
+  uint32_t *tmem_slot = (uint32_t *)(bars + 2 * S + 5);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  float *s_bias = (float *)(smem + S * CF::STAGE_BYTES + 256);
+  uint8_t *s_slots = (uint8_t *)(s_bias + BN);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
+
+  // rows and tiles (dense-path row count read from the device)
+  int M = p.m_dev ? *p.m_dev : p.M_host;
+  const bool dense_all = p.ctl ? p.ctl->dense != 0 : false;
+  const int m_blocks = (M + BM - 1) / BM;
+  const int n_blocks = (p.N + BN - 1) / BN;
+  const int num_tiles = m_blocks * n_blocks;
+  const int KT = (p.Kdim + BK - 1) / BK;
+  if ((int)blockIdx.x >= num_tiles) return;  // uniform for the CTA
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(CF::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      const CUtensorMap *amap = (p.ctl && dense_all) ? &mapA2 : &mapA;
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mb = tile / n_blocks, nb = tile % n_blocks;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sbase = smem_u32(stages + stage * CF::STAGE_BYTES);
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, CF::STAGE_BYTES);
+          tma_load_2d(sbase, amap, kt * BK, mb * BM, fb);
+#pragma unroll
+          for (int op = 0; op < NB; ++op) {
+            const CUtensorMap *bm = op == 0 ? &mapB0 : &mapB1;
+            const uint32_t bbase = sbase + CF::A_BYTES + op * CF::B_BYTES;
+            if (B_MN) {
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(bbase + i * (64 * BK * 2), bm, nb * BN + 64 * i, kt * BK, fb);
+            } else {
+              tma_load_2d(bbase, bm, kt * BK, nb * BN, fb);
+            }
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain after an abort: wait (bounded) until the last load issued into
+      // each stage has landed, so no copy is in flight when the CTA exits.
+      if (!ok) {
+        for (int s = 0; s < S && s < issued; ++s) {
+          const long last = s + (long)S * ((issued - 1 - s) / S);
+          const uint32_t par = (uint32_t)((last / S) & 1);
+          const uint64_t t0 = global_timer();
+          while (!mbar_try(full0 + 8 * s, par) && global_timer() - t0 < WAIT_LIMIT_NS / 4) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t IDESC = make_idesc(BM, BN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t use = (uint32_t)(lt >> 1);
+        if (!mbar_wait(tempty0 + 8 * buf, (use & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t dacc = tmem_base + (uint32_t)(buf * NB * BN);
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sbase = smem_u32(stages + stage * CF::STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(sbase + kk * 32, 16, 1024);
+#pragma unroll
+            for (int op = 0; op < NB; ++op) {
+              const uint32_t bbase = sbase + CF::A_BYTES + op * CF::B_BYTES;
+              // K-major: 128 B rows, 8-row groups 1024 B apart, K step = +32 B.
+              // MN-major: 64-element MN groups 8 KB apart (LBO), 8-row K groups
+              // 1024 B apart (SBO), K step of 16 rows = +2048 B.
+              const uint64_t bd = B_MN ? sw128_desc(bbase + kk * 2048, 64 * BK * 2, 1024)
+                                       : sw128_desc(bbase + kk * 32, 16, 1024);
+              mma_bf16(dacc + op * BN, ad, bd, IDESC, (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * buf);
+      }
+      // All MMAs issued by this thread are complete before TMEM is freed.
+      mma_commit(mma_done);
+      const uint64_t t0 = global_timer();
+      while (!mbar_try(mma_done, 0) && global_timer() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;          // accumulator row of this thread
+    const int et = threadIdx.x - 64;        // 0..127 among epilogue threads
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      const int mb = tile / n_blocks, nb = tile % n_blocks;
+      const int buf = lt & 1;
+      const uint32_t use = (uint32_t)(lt >> 1);
+      const int n0 = nb * BN;
+      const int m = mb * BM + row;
+      const bool row_ok = m < M;
+      // per-tile column constants
+      if (EPI == EPI_PACK || EPI == EPI_GU) {
+        epi_bar();
+        for (int c = et; c < BN; c += 128) s_bias[c] = (n0 + c < p.N) ? p.bg[n0 + c] : 0.f;
+        epi_bar();
+      }
+      const bool ok = mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NB * BN);
+
+      if (EPI == EPI_PACK) {
+        const float rbv = (p.rb && row_ok) ? p.rb[m] : 0.f;
+        const int K = p.Kslots;
+        uint8_t *my_idx = s_slots + row * 32;
+        bf16 *my_val = (bf16 *)(s_slots + 128 * 32) + row * 32;
+        for (int jt = 0; jt < BN / p.C; ++jt) {
+          const int j = (n0 + jt * p.C) / p.C;      // global TwELL tile index
+          const bool tile_ok = n0 + jt * p.C < p.N;
+          for (int k = 0; k < K; ++k) {
+            my_idx[k] = 0xFF;
+            my_val[k] = __float2bfloat16_rn(0.f);
+          }
+          int cnt = 0;
+          for (int c0 = 0; c0 < p.C; c0 += 32) {
+            float v[32];
+            tmem_ld32(tacc + jt * p.C + c0, v);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float z = (v[i] + s_bias[jt * p.C + c0 + i]) + rbv;
+              if (z > 0.f) {
+                if (cnt < K) {
+                  my_idx[cnt] = (uint8_t)(c0 + i);
+                  my_val[cnt] = __float2bfloat16_rn(z);
+                }
+                ++cnt;
+              }
+            }
+          }
+          if (row_ok && tile_ok) {
+            const size_t s0 = ((size_t)j * p.Tn + m) * (size_t)K;
+            uint8_t *gi = p.idx + s0;
+            bf16 *gv = p.val + s0;
+            if (K % 16 == 0) {
+              for (int k = 0; k < K; k += 16) *(uint4 *)(gi + k) = *(const uint4 *)(my_idx + k);
+            } else if (K == 8) {
+              *(uint2 *)gi = *(const uint2 *)my_idx;
+            } else if (K == 4) {
+              *(uint32_t *)gi = *(const uint32_t *)my_idx;
+            } else {
+              for (int k = 0; k < K; ++k) gi[k] = my_idx[k];
+            }
+            if (K % 8 == 0) {
+              for (int k = 0; k < K; k += 8) *(uint4 *)(gv + k) = *(const uint4 *)(my_val + k);
+            } else {
+              for (int k = 0; k < K; ++k) gv[k] = my_val[k];
+            }
+            p.nnz[(size_t)j * p.Tn + m] = (uint8_t)cnt;
+          }
+        }
+      } else if (EPI == EPI_GU) {
+        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
+        const float rbv = (p.rb && row_ok) ? p.rb[tok] : 0.f;
+        const int ps = row_ok ? (dense_all ? p.pos[tok] : m) : -1;
+        const bool fb_ok = ps >= 0 && ps < p.cap;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float zg[32], zu[32];
+          tmem_ld32(tacc + c0, zg);
+          if (NB == 2) tmem_ld32(tacc + BN + c0, zu);
+          if (!row_ok || n0 + c0 >= p.N) continue;
+          uint32_t hw[16], gw[16], uw[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float g2[2], u2[2], h2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float z = (zg[i + e] + s_bias[c0 + i + e]) + rbv;
+              g2[e] = z > 0.f ? __bfloat162float(__float2bfloat16_rn(z)) : 0.f;
+              u2[e] = NB == 2 ? zu[i + e] : 1.f;
+              h2[e] = p.gated ? g2[e] * u2[e] : g2[e];
+            }
+            hw[i / 2] = pack_bf2(h2[0], h2[1]);
+            gw[i / 2] = pack_bf2(g2[0], g2[1]);
+            uw[i / 2] = pack_bf2(u2[0], u2[1]);
+          }
+          uint4 *hd = (uint4 *)(p.h + (size_t)m * p.F + n0 + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+          if (fb_ok) {
+            uint4 *gd = (uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              gd[v4] = make_uint4(gw[4 * v4], gw[4 * v4 + 1], gw[4 * v4 + 2], gw[4 * v4 + 3]);
+            if (p.train && p.gated) {
+              uint4 *ud = (uint4 *)(p.u_fb + (size_t)ps * p.F + n0 + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                ud[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+            }
+          }
+        }
+      } else if (EPI == EPI_DOWN) {
+        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(tacc + c0, v);
+          if (!row_ok || n0 + c0 >= p.N) continue;
+          if (n0 + c0 + 32 > p.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (n0 + c0 + i < p.N) p.y[(size_t)tok * p.D + n0 + c0 + i] = __float2bfloat16_rn(v[i]);
+            continue;
+          }
+          uint4 *yd = (uint4 *)(p.y + (size_t)tok * p.D + n0 + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            yd[v4] = make_uint4(pack_bf2(v[8 * v4], v[8 * v4 + 1]), pack_bf2(v[8 * v4 + 2], v[8 * v4 + 3]),
+                                pack_bf2(v[8 * v4 + 4], v[8 * v4 + 5]),
+                                pack_bf2(v[8 * v4 + 6], v[8 * v4 + 7]));
+        }
+      } else {  // EPI_F32
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(tacc + c0, v);
+          if (!row_ok) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n0 + c0 + i < p.N) p.out[(size_t)m * p.N + n0 + c0 + i] = v[i];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(CF::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host --
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeFn)f;
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box {bc, br},
+// 128-byte swizzle (bc * 2 == 128).
+bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t bc,
+              uint32_t br) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {bc, br};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  });
+  return n;
+}
+
+template <int BN, int NB, bool B_MN, int EPI>
+cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a2, const CUtensorMap &b0,
+                      const CUtensorMap &b1, const TcParams &p, int max_tiles, cudaStream_t s) {
+  using CF = Cfg<BN, NB, B_MN, EPI>;
+  auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  int grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<grid, NTHREADS, CF::SMEM, s>>>(a, a2, b0, b1, p);
+  return cudaGetLastError();
+}
+
+TcParams base_params(const FwdArgs &a) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.Tn = a.T; p.F = a.F; p.D = a.D; p.C = a.C; p.Kslots = a.K; p.cap = a.tw.ovf_cap;
+  p.gated = a.gated; p.train = a.train; p.bg = a.bg; p.rb = a.rb; p.rows = a.ws.rows;
+  p.pos = a.ws.pos; p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val;
+  p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;
+  p.status = a.tw.status;
+  return p;
+}
+
+}  // namespace
+
+bool tc_available() {
+  static int ok = -1;
+  if (ok < 0) {
+    int dev = 0, major = 0, minor = 0;
+    ok = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess)
+      ok = (major == 10 && minor == 3 && encode_fn() != nullptr) ? 1 : 0;
+  }
+  return ok == 1;
+}
+
+cudaError_t launch_tc_gate_pack(const FwdArgs &a, cudaStream_t s) {
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, a.x, a.D, a.T, 64, BM) || !make_map(&mw, a.Wg, a.D, a.F, 64, 128))
+    return cudaErrorInvalidValue;
+  TcParams p = base_params(a);
+  p.M_host = a.T;
+  p.N = a.F;
+  p.Kdim = a.D;
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 127) / 128);
+  return launch_tc<128, 1, false, EPI_PACK>(mx, mx, mw, mw, p, tiles, s);
+}
+
+cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
+  CUtensorMap mxg, mx, mg, mu;
+  if (!make_map(&mxg, a.ws.xg, a.D, a.T, 64, BM) || !make_map(&mx, a.x, a.D, a.T, 64, BM) ||
+      !make_map(&mg, a.Wg, a.D, a.F, 64, 128) ||
+      !make_map(&mu, a.gated ? a.Wu : a.Wg, a.D, a.F, 64, 128))
+    return cudaErrorInvalidValue;
+  TcParams p = base_params(a);
+  p.m_dev = &a.ws.ctl->n_rows;
+  p.ctl = a.ws.ctl;
+  p.N = a.F;
+  p.Kdim = a.D;
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 127) / 128);
+  if (a.gated) return launch_tc<128, 2, false, EPI_GU>(mxg, mx, mg, mu, p, tiles, s);
+  return launch_tc<128, 1, false, EPI_GU>(mxg, mx, mg, mg, p, tiles, s);
+}
+
+// Down projection of the dense-path rows: A = h rows (dense-path order),
+// B = W_down read MN-major from its neuron-major [F][D] storage.
+cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
+  CUtensorMap mh, md;
+  if (!make_map(&mh, a.ws.h, a.F, a.T, 64, BM) || !make_map(&md, a.Wd, a.D, a.F, 64, 64))
+    return cudaErrorInvalidValue;
+  TcParams p = base_params(a);
+  p.m_dev = &a.ws.ctl->n_rows;
+  p.ctl = a.ws.ctl;
+  p.N = a.D;
+  p.Kdim = a.F;
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.D + 127) / 128);
+  return launch_tc<128, 1, true, EPI_DOWN>(mh, mh, md, md, p, tiles, s);
+}
+
+// Test hook: fp32 C[M][N] = A[M][K] B^T (B [N][K], b_mn = 0) or A B (B [K][N],
+// b_mn = 1); bf16 operands.
+cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N, int K, int b_mn,
+                         int32_t *status, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, K, M, 64, BM)) return cudaErrorInvalidValue;
+  if (b_mn ? !make_map(&mb, B, N, K, 64, 64) : !make_map(&mb, B, K, N, 64, 128))
+    return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.M_host = M;
+  p.N = N;
+  p.Kdim = K;
+  p.out = Cout;
+  p.status = status;
+  const int tiles = ((M + BM - 1) / BM) * ((N + 127) / 128);
+  if (b_mn) return launch_tc<128, 1, true, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
+  return launch_tc<128, 1, false, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
+}
+
+}  // namespace twell
+
+extern "C" int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K,
+                                  int b_mn, int32_t *status, void *stream) {
+  if (!twell::tc_available()) return TWELL_ERR_UNSUPPORTED;
+  if (!A || !B || !C || M < 1 || N < 1 || K < 8 || (K % 8) || (b_mn && (N % 8))) return TWELL_ERR_ARG;
+  cudaError_t e = twell::tc_test_gemm(A, B, C, M, N, K, b_mn, status, (cudaStream_t)stream);
+  return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}

@@ -1,0 +1,344 @@
+// twell_abi.cu -- the C ABI of libtwell.so: argument checks, workspace
+// carve-up and the launch sequence of each entry point (see include/twell.h).
+//
+// Forward launch sequence ("Sparser, Faster, Lighter Transformer Language
+// Models", technical summary sections 2.A-2.B):
+//   1. gate matmul + ReLU + TwELL pack epilogue         (TwELL, nnz)
+//   2. overflow compaction                               (hybrid: overflow rows,
+//                                                         hybrid / all-dense mode)
+//   3. fused sparse up + down projection                 (non-overflow rows)
+//   4. dense gate+up and down over the dense-path rows   (overflow rows, or all
+//                                                         rows in all-dense mode)
+// The hybrid/all-dense decision is taken on the device (step 2) and read by
+// steps 3-4 from the workspace, so the host never waits for the GPU.
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace twell {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---- optional per-launch timing ---------------------------------------------
+namespace {
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> id;
+  size_t used = 0;
+};
+Profiler &profiler() {
+  static Profiler p;
+  return p;
+}
+}  // namespace
+
+void prof_mark(int kid, cudaStream_t s) {
+  Profiler &p = profiler();
+  if (!p.on) return;
+  std::lock_guard<std::mutex> g(p.mu);
+  if (p.used == p.ev.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return;
+    p.ev.push_back(e);
+    p.id.push_back(0);
+  }
+  p.id[p.used] = kid;
+  cudaEventRecord(p.ev[p.used], s);
+  ++p.used;
+}
+
+static const char *kKernelNames[KID_COUNT] = {
+    "gate_gemm_relu_twell", "overflow_compact", "twell_updown_fused", "gather_rows",
+    "dense_rows_gate_up",   "dense_rows_down",  "pack_dense",         "copy_fb_rows",
+    "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
+    "bwd_dense_rows"};
+
+Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
+  Workspace w;
+  memset(&w, 0, sizeof(w));
+  const size_t es = dtype == TWELL_BF16 ? 2 : 4;
+  const size_t nt = (size_t)F / (size_t)C;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void * {
+    const size_t o = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return base ? (void *)((char *)base + o) : nullptr;
+  };
+  w.ctl = (Ctl *)take(sizeof(Ctl));
+  w.rows = (int32_t *)take(sizeof(int32_t) * (size_t)T);
+  w.pos = (int32_t *)take(sizeof(int32_t) * (size_t)T);
+  w.h = take(es * (size_t)T * F);
+  w.xg = take(es * (size_t)T * D);
+  if (train) {
+    const size_t slots = nt * (size_t)T * (size_t)K;
+    w.dz = (float *)take(4 * slots);
+    w.du = (float *)take(4 * slots);
+    w.hs = (float *)take(4 * slots);
+    w.col_ptr = (int32_t *)take(4 * ((size_t)F + 1));
+    w.col_cnt = (int32_t *)take(4 * (size_t)F);
+    w.col_tok = (int32_t *)take(4 * slots);
+    w.col_slot = (int32_t *)take(4 * slots);
+    w.dzr = take(es * (size_t)T * F);
+    w.dur = take(es * (size_t)T * F);
+    w.dyg = take(es * (size_t)T * D);
+  }
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace twell
+
+using namespace twell;
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool pow2_k(int K) { return K == 1 || K == 2 || K == 4 || K == 8 || K == 16 || K == 32; }
+
+twell_status check_shape(int T, int D, int F, int C, int K, int dtype) {
+  if (dtype != TWELL_F32 && dtype != TWELL_BF16) return TWELL_ERR_DTYPE;
+  if (T < 1 || F < 1 || D < 8) return TWELL_ERR_ARG;
+  if (C != 32 && C != 64 && C != 128) return TWELL_ERR_ARG;
+  if (F % C != 0 || !pow2_k(K) || K > C) return TWELL_ERR_ARG;
+  const size_t es = dtype == TWELL_BF16 ? 2 : 4;
+  if ((D * es) % 16 != 0 || (F * es) % 16 != 0) return TWELL_ERR_ALIGN;
+  if (D * es / 16 > 1024) return TWELL_ERR_ARG;  // d_model <= 8192 (bf16) / 4096 (fp32)
+  if ((double)T * (double)(F / C) * (double)K >= 2147483647.0) return TWELL_ERR_ARG;
+  if ((double)T * (double)F >= 9.0e15) return TWELL_ERR_ARG;
+  return TWELL_OK;
+}
+
+twell_status check_tw(const twell_t *tw, int train) {
+  if (!tw) return TWELL_ERR_ARG;
+  twell_status s = check_shape(tw->T, 16, tw->F, tw->C, tw->K, tw->dtype);
+  if (s != TWELL_OK) return s;
+  if (!tw->idx || !tw->val || !tw->nnz || !tw->n_ovf || !tw->status) return TWELL_ERR_ARG;
+  if (tw->ovf_cap < 0) return TWELL_ERR_ARG;
+  if (tw->ovf_cap > 0 && (!tw->ovf_rows || !tw->g_fb)) return TWELL_ERR_ARG;
+  if (!aligned16(tw->idx) || !aligned16(tw->val) || !aligned16(tw->nnz)) return TWELL_ERR_ALIGN;
+  if (tw->ovf_cap > 0 && !aligned16(tw->g_fb)) return TWELL_ERR_ALIGN;
+  if (train) {
+    if (!tw->u_val || (tw->ovf_cap > 0 && !tw->u_fb)) return TWELL_ERR_ARG;
+    if (!aligned16(tw->u_val) || (tw->ovf_cap > 0 && !aligned16(tw->u_fb))) return TWELL_ERR_ALIGN;
+  }
+  return TWELL_OK;
+}
+
+twell_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TWELL_OK;
+  if (e == cudaErrorNotSupported) return TWELL_ERR_UNSUPPORTED;
+  return TWELL_ERR_CUDA;
+}
+
+twell_status check_ws(void *ws, size_t ws_bytes, const Workspace &need) {
+  if (!ws) return TWELL_ERR_WORKSPACE;
+  if (((uintptr_t)ws & 255u) != 0) return TWELL_ERR_WORKSPACE;
+  if (ws_bytes < need.bytes) return TWELL_ERR_WORKSPACE;
+  return TWELL_OK;
+}
+
+float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_switch : 0.5f; }
+
+bool use_tc(int dtype) { return dtype == TWELL_BF16 && tc_available(); }
+
+// Steps 1-2 of the forward (shared by twell_pack and twell_ffn_forward).
+cudaError_t run_gate_and_split(FwdArgs &a, cudaStream_t s) {
+  prof_mark(KID_START, s);
+  cudaError_t e = use_tc(a.dtype) ? launch_tc_gate_pack(a, s) : launch_simt_gate_pack(a, s);
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_GATE_PACK, s);
+  e = launch_overflow_compact(a.tw, &a.ws, a.dense_switch, s);
+  prof_mark(KID_OVERFLOW_COMPACT, s);
+  return e;
+}
+
+// Step 4: dense gate+up (+ down when write_y) over the dense-path rows.
+cudaError_t run_dense_rows(FwdArgs &a, bool write_y, cudaStream_t s) {
+  cudaError_t e;
+  if (use_tc(a.dtype)) {
+    e = launch_gather_rows(a.x, a.ws.xg, a.ws, a.T, a.D, a.dtype, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_GATHER_ROWS, s);
+    e = launch_tc_dense_gu(a, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_DENSE_GU, s);
+    if (!write_y) return e;
+    e = launch_tc_dense_down(a, s);
+    prof_mark(KID_DENSE_DOWN, s);
+    return e;
+  }
+  e = launch_simt_dense_gu(a, s);
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_DENSE_GU, s);
+  if (!write_y) return e;
+  e = launch_simt_dense_down(a, s);
+  prof_mark(KID_DENSE_DOWN, s);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *twell_version(void) { return "twell-gb300 0.1 (sm_103a)"; }
+
+size_t twell_workspace_size(int T, int D, int F, int C, int K, int dtype, int train) {
+  if (check_shape(T, D, F, C, K, dtype) != TWELL_OK) return 0;
+  return carve_workspace(nullptr, T, D, F, C, K, dtype, train).bytes;
+}
+
+twell_status twell_pack_dense(const void *H, twell_t *tw, void *stream) {
+  twell_status st = check_tw(tw, 0);
+  if (st != TWELL_OK) return st;
+  if (!H) return TWELL_ERR_ARG;
+  if (!aligned16(H)) return TWELL_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  prof_mark(KID_START, s);
+  cudaError_t e = launch_pack_dense(H, *tw, s);
+  prof_mark(KID_PACK_DENSE, s);
+  if (e == cudaSuccess) e = launch_overflow_compact(*tw, nullptr, 1.0f, s);
+  prof_mark(KID_OVERFLOW_COMPACT, s);
+  if (e == cudaSuccess) e = launch_copy_fb_rows(H, *tw, s);
+  prof_mark(KID_COPY_FB, s);
+  return cuda_status(e);
+}
+
+twell_status twell_pack(const void *x, const void *Wg, const float *bg, const float *row_bias,
+                        int D, twell_t *tw, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+  twell_status st = check_tw(tw, 0);
+  if (st != TWELL_OK) return st;
+  st = check_shape(tw->T, D, tw->F, tw->C, tw->K, tw->dtype);
+  if (st != TWELL_OK) return st;
+  if (!x || !Wg || !bg) return TWELL_ERR_ARG;
+  if (!aligned16(x) || !aligned16(Wg)) return TWELL_ERR_ALIGN;
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 0);
+  st = check_ws(workspace, workspace_bytes, need);
+  if (st != TWELL_OK) return st;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
+  a.gated = 0; a.train = 0; a.x = x; a.Wg = Wg; a.bg = bg; a.rb = row_bias; a.tw = *tw;
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 0);
+  a.dense_switch = 2.0f;  // the pack never switches to all-dense mode
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = run_gate_and_split(a, s);
+  if (e == cudaSuccess) e = run_dense_rows(a, false, s);  // fills g_fb of the overflow rows
+  return cuda_status(e);
+}
+
+twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
+                               const float *row_bias, const void *Wu, const void *Wd, int D,
+                               int train, twell_t *tw, void *y, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+  const int gated = Wu != nullptr;
+  twell_status st = check_tw(tw, train && gated);
+  if (st != TWELL_OK) return st;
+  st = check_shape(tw->T, D, tw->F, tw->C, tw->K, tw->dtype);
+  if (st != TWELL_OK) return st;
+  if (!x || !Wg || !bg || !Wd || !y) return TWELL_ERR_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wd) || !aligned16(y) ||
+      (Wu && !aligned16(Wu)))
+    return TWELL_ERR_ALIGN;
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, train);
+  st = check_ws(workspace, workspace_bytes, need);
+  if (st != TWELL_OK) return st;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
+  a.gated = gated; a.train = train ? 1 : 0;
+  a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.bg = bg; a.rb = row_bias; a.tw = *tw; a.y = y;
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, train);
+  a.dense_switch = switch_of(tw);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = run_gate_and_split(a, s);
+  if (e == cudaSuccess) {
+    e = launch_updown_fused(a, s);
+    prof_mark(KID_UPDOWN, s);
+  }
+  if (e == cudaSuccess) e = run_dense_rows(a, true, s);
+  return cuda_status(e);
+}
+
+twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, const void *Wd,
+                                const twell_t *tw, const void *dy, float lambda, int D,
+                                void *dx, float *dWg, float *dbg, float *dWu, float *dWd,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+  const int gated = Wu != nullptr;
+  twell_status st = check_tw(tw, gated);
+  if (st != TWELL_OK) return st;
+  st = check_shape(tw->T, D, tw->F, tw->C, tw->K, tw->dtype);
+  if (st != TWELL_OK) return st;
+  if (!x || !Wg || !Wd || !dy || !dx || !dWg || !dbg || !dWd || (gated && !dWu))
+    return TWELL_ERR_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wd) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16(dWg) || !aligned16(dWd) || (gated && (!aligned16(Wu) || !aligned16(dWu))))
+    return TWELL_ERR_ALIGN;
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 1);
+  st = check_ws(workspace, workspace_bytes, need);
+  if (st != TWELL_OK) return st;
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
+  a.gated = gated; a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.dy = dy; a.tw = *tw;
+  a.lambda = lambda; a.dx = dx; a.dWg = dWg; a.dbg = dbg; a.dWu = dWu; a.dWd = dWd;
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
+  return cuda_status(launch_backward(a, (cudaStream_t)stream));
+}
+
+int twell_profile_begin(void) {
+  Profiler &p = profiler();
+  std::lock_guard<std::mutex> g(p.mu);
+  p.used = 0;
+  p.on = true;
+  return TWELL_OK;
+}
+
+int twell_profile_end(int capacity, int *kernel_ids, float *ms, int *count) {
+  Profiler &p = profiler();
+  std::lock_guard<std::mutex> g(p.mu);
+  p.on = false;
+  int n = 0;
+  for (size_t i = 1; i < p.used; ++i) {
+    if (p.id[i] < 0) continue;  // an entry point's start marker
+    if (cudaEventSynchronize(p.ev[i]) != cudaSuccess) return TWELL_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, p.ev[i - 1], p.ev[i]) != cudaSuccess) return TWELL_ERR_CUDA;
+    if (n < capacity) {
+      if (kernel_ids) kernel_ids[n] = p.id[i];
+      if (ms) ms[n] = t;
+    }
+    ++n;
+  }
+  if (count) *count = n;
+  p.used = 0;
+  return n <= capacity ? TWELL_OK : TWELL_ERR_CAPACITY;
+}
+
+const char *twell_kernel_name(int kernel_id) {
+  return (kernel_id >= 0 && kernel_id < KID_COUNT) ? kKernelNames[kernel_id] : "unknown";
+}
+
+twell_status twell_get_status(const twell_t *tw, void *stream, int32_t *n_ovf) {
+  if (!tw || !tw->status) return TWELL_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t host[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(&host[0], tw->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && n_ovf && tw->n_ovf)
+    e = cudaMemcpyAsync(&host[1], tw->n_ovf, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(tw->status, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return TWELL_ERR_CUDA;
+  if (n_ovf) *n_ovf = host[1];
+  return (twell_status)host[0];
+}
+
+}  // extern "C"
