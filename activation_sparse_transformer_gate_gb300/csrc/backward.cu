@@ -1,9 +1,412 @@
-// backward.cu -- sparse backward of the TwELL FFN (not built yet).
+// backward.cu -- sparse backward of the TwELL FFN with the L1 term.
+//
+// "Sparser, Faster, Lighter Transformer Language Models", technical summary
+// section 2.B (training): hybrid x dense and dense x hybrid matmuls and a sparse
+// transpose for the weight gradients; L1 regularisation of the ReLU FFN
+// activations.  With h = g*u (plain FFN: h = g, u = 1):
+//   dh = dy . Wd[n] + lambda sign(h),  dz = [z > 0] dh u,  du = dh g
+//   dx = sum_n dz Wg[n] + du Wu[n]
+//   dWg[n] = sum_t dz x_t, dbg[n] = sum_t dz, dWu[n] = sum_t du x_t,
+//   dWd[n] = sum_t h dy_t
+// Launch sequence (all on the caller's stream):
+//   1. hybrid split of the saved TwELL (overflow rows, in this workspace)
+//   2. one CTA per token: dh at its active pairs from gathered W_down rows,
+//      dz / du / h at those pairs, and its dx row from gathered W_gate / W_up
+//      rows (hybrid x dense).  Pairs come from the TwELL slots, or from the
+//      dense backup row of an overflow row.
+//   3. one CTA per tile: deterministic transpose of the slots into
+//      neuron-major lists ordered by token (sparse transpose)
+//   4. one CTA per neuron: dWg, dWu, dWd rows and dbg from gathered x / dy rows
+//      of its list, then the overflow rows' contributions (dense x hybrid)
 #include "common.cuh"
+#include "gather.cuh"
 #include "kernels.h"
 
 namespace twell {
 
-cudaError_t launch_backward(const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+struct BParams {
+  const void *x, *Wg, *Wu, *Wd, *dy;
+  const uint8_t *idx, *nnz;
+  const void *val, *u_val, *g_fb, *u_fb;
+  int Tn, D, F, C, K, gated, cap;
+  float lambda;
+  const Ctl *ctl;
+  const int32_t *rows, *pos;
+  float *dz, *du, *hs;       // slot arrays [F/C][T][K]
+  float *dzr, *dur, *hr;     // overflow rows [n_ovf][F]
+  int32_t *col_start, *col_cnt, *col_tok, *col_slot;
+  void *dx;
+  float *dWg, *dbg, *dWu, *dWd;
+  int32_t *status;
+};
+
+__device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// 2. Per-token sparse backward.  A non-overflow row takes its pairs from the
+// TwELL slots (u from u_val) and writes dz / du / h at the slots; an overflow
+// row takes its pairs from its dense backup row (g_fb, u_fb) and writes them
+// into the overflow-row arrays.  Both accumulate their dx row.
+template <class T, int VPT>
+__global__ void __launch_bounds__(512) bwd_token_kernel(BParams p) {
+  constexpr int EV = Vec<T>::EV;
+  __shared__ int s_n[LIST_CAP];
+  __shared__ float s_g[LIST_CAP];
+  __shared__ float s_u[LIST_CAP];
+  __shared__ int s_slot[LIST_CAP];
+  __shared__ int s_wsum[32];
+  __shared__ float s_red[PB][33];
+  __shared__ float s_tot[PB];
+  __shared__ int s_total;
+
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nt = p.F / p.C;
+  const int NV = p.D / EV;
+  const int ps = p.pos[t];
+  const bool ovf = ps >= 0;
+  if (ovf && ps >= p.cap) return;  // no dense backup row (capacity error raised)
+
+  const uint4 *dyrow = (const uint4 *)p.dy + (size_t)t * NV;
+  float dyr[VPT][EV], dxr[VPT][EV];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int vi = tid + v * blockDim.x;
+    uint4 r = vi < NV ? dyrow[vi] : make_uint4(0, 0, 0, 0);
+    Vec<T>::unpack(r, dyr[v]);
+#pragma unroll
+    for (int e = 0; e < EV; ++e) dxr[v][e] = 0.f;
+  }
+  const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu, *Wd4 = (const uint4 *)p.Wd;
+  const T *uval = (const T *)p.u_val;
+  const T *ufb = (const T *)p.u_fb;
+  PairSource<T> src;
+  src.idx = p.idx; src.nnz = p.nnz; src.val = (const T *)p.val; src.Tn = p.Tn; src.C = p.C;
+  src.K = p.K; src.t = t;
+  src.dense = ovf ? (const T *)p.g_fb + (size_t)ps * p.F : nullptr;
+  src.dense_tile = p.C;
+  src.dense_all = true;
+  src.neg_slots = ovf;
+
+  int group = LIST_CAP / (ovf ? p.C : p.K);
+  if (group > (int)blockDim.x) group = blockDim.x;
+  for (int g0 = 0; g0 < nt; g0 += group) {
+    const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
+    for (int i = tid; i < P; i += blockDim.x) {  // u of every pair, once
+      const int sl = s_slot[i];
+      s_u[i] = !p.gated ? 1.f : (sl >= 0 ? to_f(uval[sl]) : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
+    }
+    __syncthreads();
+    for (int b0 = 0; b0 < P; b0 += PB) {
+      const int nb = P - b0 < PB ? P - b0 : PB;
+      float pd[PB];
+      {
+        uint4 wd[PB][VPT];
+#pragma unroll
+        for (int b = 0; b < PB; ++b) {
+          const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
+#pragma unroll
+          for (int v = 0; v < VPT; ++v) {
+            const int vi = tid + v * blockDim.x;
+            wd[b][v] = (b < nb && vi < NV) ? ldg_stream(Wd4 + rb + vi) : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(dyr, wd[b]);
+      }
+      uint4 wg[PB][VPT], wu[PB][VPT];
+#pragma unroll
+      for (int b = 0; b < PB; ++b) {
+        const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int vi = tid + v * blockDim.x;
+          const bool ok = b < nb && vi < NV;
+          wg[b][v] = ok ? ldg_stream(Wg4 + rb + vi) : make_uint4(0, 0, 0, 0);
+          wu[b][v] = (ok && p.gated) ? ldg_stream(Wu4 + rb + vi) : make_uint4(0, 0, 0, 0);
+        }
+      }
+      float dot[PB];
+      block_reduce8(pd, dot, s_red, s_tot);
+      float dzb[PB], dub[PB];
+#pragma unroll
+      for (int b = 0; b < PB; ++b) {
+        const float g = b < nb ? s_g[b0 + b] : 0.f;
+        const float u = b < nb ? s_u[b0 + b] : 0.f;
+        const float h = p.gated ? g * u : g;
+        const float dh = dot[b] + p.lambda * sgnf(h);
+        const bool act = b < nb && g > 0.f;
+        dzb[b] = act ? (p.gated ? dh * u : dh) : 0.f;
+        dub[b] = act ? dh * g : 0.f;
+        if (tid == b && b < nb) {
+          const int sl = s_slot[b0 + b];
+          if (sl >= 0) {
+            p.dz[sl] = dzb[b];
+            p.du[sl] = dub[b];
+            p.hs[sl] = h;
+          } else {
+            const size_t o = (size_t)ps * p.F + (-1 - sl);
+            p.dzr[o] = dzb[b];
+            p.dur[o] = dub[b];
+            p.hr[o] = h;
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < PB; ++b) {
+        if (b >= nb) break;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          float fg[EV], fu[EV];
+          Vec<T>::unpack(wg[b][v], fg);
+          Vec<T>::unpack(wu[b][v], fu);
+#pragma unroll
+          for (int e = 0; e < EV; ++e) {
+            dxr[v][e] = fmaf(dzb[b], fg[e], dxr[v][e]);
+            if (p.gated) dxr[v][e] = fmaf(dub[b], fu[e], dxr[v][e]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  uint4 *dxrow = (uint4 *)p.dx + (size_t)t * NV;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int vi = tid + v * blockDim.x;
+    if (vi < NV) dxrow[vi] = Vec<T>::pack(dxr[v]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. Sparse transpose of one tile's slots into neuron-major lists.  The list of
+// neuron j*C + c occupies col_tok/col_slot[col_start .. + col_cnt) inside the
+// tile's region [j*T*K, (j+1)*T*K), ordered by token: tokens are visited 1024
+// at a time, and a token's rank among the tokens of its chunk that use column c
+// comes from per-warp lane masks (popc below the lane) plus per-warp offsets.
+// Overflow rows are not listed (their pairs live in the overflow-row arrays).
+template <int C>
+__global__ void __launch_bounds__(1024) twell_transpose_kernel(BParams p) {
+  __shared__ uint32_t occ[32][C];
+  __shared__ int woff[32][C];
+  __shared__ int cnt[C], run[C];
+  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int K = p.K, Tn = p.Tn;
+  const size_t region = (size_t)j * Tn * K;
+  for (int c = tid; c < C; c += blockDim.x) cnt[c] = 0;
+  __syncthreads();
+  for (int base = 0; base < Tn; base += blockDim.x) {
+    const int t = base + tid;
+    if (t < Tn && p.pos[t] < 0) {
+      const int n = p.nnz[(size_t)j * Tn + t];
+      const size_t s0 = ((size_t)j * Tn + t) * K;
+      for (int k = 0; k < n && k < K; ++k) {
+        const int c = p.idx[s0 + k];
+        if (c < C) atomicAdd(&cnt[c], 1);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int r = 0;
+    for (int c = 0; c < C; ++c) {
+      run[c] = r;
+      p.col_start[j * C + c] = (int)(region + r);
+      p.col_cnt[j * C + c] = cnt[c];
+      r += cnt[c];
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = 0; base < Tn; base += blockDim.x) {
+    for (int i = tid; i < 32 * C; i += blockDim.x) (&occ[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = base + tid;
+    const bool act = t < Tn && p.pos[t] < 0;
+    const int n = act ? (int)p.nnz[(size_t)j * Tn + t] : 0;
+    const size_t s0 = ((size_t)j * Tn + (act ? t : 0)) * K;
+    for (int k = 0; k < n && k < K; ++k) {
+      const int c = p.idx[s0 + k];
+      if (c < C) atomicOr(&occ[w][c], 1u << lane);
+    }
+    __syncthreads();
+    for (int c = tid; c < C; c += blockDim.x) {
+      int r = run[c];
+      for (int q = 0; q < 32; ++q) {
+        woff[q][c] = r;
+        r += __popc(occ[q][c]);
+      }
+      run[c] = r;
+    }
+    __syncthreads();
+    for (int k = 0; k < n && k < K; ++k) {
+      const int c = p.idx[s0 + k];
+      if (c >= C) continue;
+      const int e = woff[w][c] + __popc(occ[w][c] & lt);
+      p.col_tok[region + e] = t;
+      p.col_slot[region + e] = (int)(s0 + k);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4. One CTA per neuron: weight-gradient rows from the neuron's list
+// (ascending tokens), then the overflow rows (ascending).  Rows of neurons
+// that are never active are written as zeros.
+template <class T, int VPT>
+__global__ void __launch_bounds__(512) bwd_dw_kernel(BParams p) {
+  constexpr int EV = Vec<T>::EV;
+  const int n = blockIdx.x, tid = threadIdx.x;
+  const int NV = p.D / EV;
+  const uint4 *x4 = (const uint4 *)p.x, *dy4 = (const uint4 *)p.dy;
+  float ag[VPT][EV], au[VPT][EV], ad[VPT][EV];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int e = 0; e < EV; ++e) ag[v][e] = au[v][e] = ad[v][e] = 0.f;
+  float sb = 0.f;
+  const int start = p.col_start[n], cnt = p.col_cnt[n];
+  for (int e0 = 0; e0 < cnt; e0 += PB) {
+    const int nb = cnt - e0 < PB ? cnt - e0 : PB;
+    uint4 xv[PB][VPT], yv[PB][VPT];
+    float fz[PB], fu[PB], fh[PB];
+#pragma unroll
+    for (int b = 0; b < PB; ++b) {
+      const int e = start + e0 + (b < nb ? b : 0);
+      const int t = p.col_tok[e], sl = p.col_slot[e];
+      fz[b] = b < nb ? p.dz[sl] : 0.f;
+      fu[b] = b < nb ? p.du[sl] : 0.f;
+      fh[b] = b < nb ? p.hs[sl] : 0.f;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int vi = tid + v * blockDim.x;
+        const bool ok = b < nb && vi < NV;
+        xv[b][v] = ok ? x4[(size_t)t * NV + vi] : make_uint4(0, 0, 0, 0);
+        yv[b][v] = ok ? dy4[(size_t)t * NV + vi] : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < PB; ++b) {
+      if (b >= nb) break;
+      sb += fz[b];
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        float fx[EV], fy[EV];
+        Vec<T>::unpack(xv[b][v], fx);
+        Vec<T>::unpack(yv[b][v], fy);
+#pragma unroll
+        for (int e = 0; e < EV; ++e) {
+          ag[v][e] = fmaf(fz[b], fx[e], ag[v][e]);
+          au[v][e] = fmaf(fu[b], fx[e], au[v][e]);
+          ad[v][e] = fmaf(fh[b], fy[e], ad[v][e]);
+        }
+      }
+    }
+  }
+  // overflow rows (dense backup)
+  const int n_rows = min(p.ctl->n_ovf, p.cap);
+  const T *gfb = (const T *)p.g_fb;
+  for (int i = 0; i < n_rows; ++i) {
+    if (!(to_f(gfb[(size_t)i * p.F + n]) > 0.f)) continue;
+    const int t = p.rows[i];
+    const float z = p.dzr[(size_t)i * p.F + n], u = p.dur[(size_t)i * p.F + n];
+    const float h = p.hr[(size_t)i * p.F + n];
+    sb += z;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int vi = tid + v * blockDim.x;
+      if (vi >= NV) continue;
+      float fx[EV], fy[EV];
+      Vec<T>::unpack(x4[(size_t)t * NV + vi], fx);
+      Vec<T>::unpack(dy4[(size_t)t * NV + vi], fy);
+#pragma unroll
+      for (int e = 0; e < EV; ++e) {
+        ag[v][e] = fmaf(z, fx[e], ag[v][e]);
+        au[v][e] = fmaf(u, fx[e], au[v][e]);
+        ad[v][e] = fmaf(h, fy[e], ad[v][e]);
+      }
+    }
+  }
+  float4 *og = (float4 *)(p.dWg + (size_t)n * p.D), *od = (float4 *)(p.dWd + (size_t)n * p.D);
+  float4 *ou = p.gated ? (float4 *)(p.dWu + (size_t)n * p.D) : nullptr;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int vi = tid + v * blockDim.x;
+    if (vi >= NV) continue;
+#pragma unroll
+    for (int q = 0; q < EV / 4; ++q) {
+      og[vi * (EV / 4) + q] = make_float4(ag[v][4 * q], ag[v][4 * q + 1], ag[v][4 * q + 2], ag[v][4 * q + 3]);
+      od[vi * (EV / 4) + q] = make_float4(ad[v][4 * q], ad[v][4 * q + 1], ad[v][4 * q + 2], ad[v][4 * q + 3]);
+      if (ou)
+        ou[vi * (EV / 4) + q] = make_float4(au[v][4 * q], au[v][4 * q + 1], au[v][4 * q + 2], au[v][4 * q + 3]);
+    }
+  }
+  if (tid == 0) p.dbg[n] = sb;
+}
+
+// ---------------------------------------------------------------------------
+cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
+  BParams p;
+  p.x = a.x; p.Wg = a.Wg; p.Wu = a.Wu; p.Wd = a.Wd; p.dy = a.dy;
+  p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = a.tw.val; p.u_val = a.tw.u_val;
+  p.g_fb = a.tw.g_fb; p.u_fb = a.tw.u_fb;
+  p.Tn = a.T; p.D = a.D; p.F = a.F; p.C = a.C; p.K = a.K; p.gated = a.gated;
+  p.cap = a.tw.ovf_cap; p.lambda = a.lambda;
+  p.ctl = a.ws.ctl; p.rows = a.ws.rows; p.pos = a.ws.pos;
+  p.dz = a.ws.dz; p.du = a.ws.du; p.hs = a.ws.hs;
+  p.dzr = a.ws.dzr; p.dur = a.ws.dur; p.hr = a.ws.hr;
+  p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_tok = a.ws.col_tok;
+  p.col_slot = a.ws.col_slot;
+  p.dx = a.dx; p.dWg = a.dWg; p.dbg = a.dbg; p.dWu = a.dWu; p.dWd = a.dWd;
+  p.status = a.tw.status;
+
+  // 1. hybrid split of the saved activations into this workspace
+  cudaError_t e = launch_flags_from_nnz(a.tw, a.ws, s);
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_START, s);
+  e = launch_overflow_compact(a.tw, &a.ws, 2.0f, s, /*write_user=*/false);
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_OVERFLOW_COMPACT, s);
+  const bool bf = a.dtype == TWELL_BF16;
+  // 2. per-token slots / overflow rows + dx
+  const int EV = bf ? 8 : 4;
+  const int NV = a.D / EV;
+  const int vpt = NV <= 512 ? 1 : 2;
+  const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
+  if (bf) {
+    if (vpt == 1) bwd_token_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_token_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
+  } else {
+    if (vpt == 1) bwd_token_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_token_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_BWD_SLOTS, s);
+  // 3. transpose
+  const int nt = a.F / a.C;
+  if (a.C == 32) twell_transpose_kernel<32><<<nt, 1024, 0, s>>>(p);
+  else if (a.C == 64) twell_transpose_kernel<64><<<nt, 1024, 0, s>>>(p);
+  else twell_transpose_kernel<128><<<nt, 1024, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_BWD_TRANSPOSE, s);
+  // 4. weight gradients
+  if (bf) {
+    if (vpt == 1) bwd_dw_kernel<bf16, 1><<<a.F, threads, 0, s>>>(p);
+    else bwd_dw_kernel<bf16, 2><<<a.F, threads, 0, s>>>(p);
+  } else {
+    if (vpt == 1) bwd_dw_kernel<float, 1><<<a.F, threads, 0, s>>>(p);
+    else bwd_dw_kernel<float, 2><<<a.F, threads, 0, s>>>(p);
+  }
+  e = cudaGetLastError();
+  prof_mark(KID_BWD_DW, s);
+  return e;
+}
 
 }  // namespace twell

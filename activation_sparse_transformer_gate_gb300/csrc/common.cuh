@@ -52,11 +52,17 @@ __device__ __forceinline__ void set_status(int32_t *st, int code) {
 
 // ---- control block in the workspace -----------------------------------------
 // Written by the overflow-compaction kernel, read by everything after it.
+// Overflow rows go through the tensor-core dense-row GEMMs when there are at
+// least this many of them (one full M tile); fewer go through the gather
+// kernels, which read their overflowing tiles from the wide-tile buffer.
+constexpr int OVF_GEMM_MIN = 128;
+
 struct Ctl {
-  int32_t n_rows;   // rows on the dense path (overflow rows, or T in dense mode)
+  int32_t n_rows;   // rows on the dense GEMM path: T (all-dense), n_ovf (ovf_gemm) or 0
   int32_t dense;    // 1: every row runs densely (n_ovf > dense_switch * T)
   int32_t n_ovf;    // true number of overflow rows
-  int32_t pad[13];
+  int32_t ovf_gemm; // 1: overflow rows run on the dense GEMM path
+  int32_t pad[12];
 };
 
 }  // namespace twell

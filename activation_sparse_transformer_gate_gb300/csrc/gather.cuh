@@ -1,0 +1,191 @@
+// gather.cuh -- helpers of the row-gather kernels (one CTA per token or per
+// neuron, 16-byte vectors of a d_model row per thread).
+#pragma once
+
+#include "common.cuh"
+
+namespace twell {
+
+constexpr int LIST_CAP = 2048;  // (neuron, value) pairs staged per tile group
+constexpr int PB = 8;           // pairs consumed per batch
+
+template <class T> struct Vec;
+template <> struct Vec<bf16> {
+  static constexpr int EV = 8;
+  static __device__ __forceinline__ void unpack(const uint4 &r, float *f) {
+    f[0] = bf_lo(r.x); f[1] = bf_hi(r.x); f[2] = bf_lo(r.y); f[3] = bf_hi(r.y);
+    f[4] = bf_lo(r.z); f[5] = bf_hi(r.z); f[6] = bf_lo(r.w); f[7] = bf_hi(r.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float *f) {
+    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]),
+                      pack_bf2(f[6], f[7]));
+  }
+};
+template <> struct Vec<float> {
+  static constexpr int EV = 4;
+  static __device__ __forceinline__ void unpack(const uint4 &r, float *f) {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float *f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// Dot product of the thread's slice of a row held in registers with one
+// gathered row (16-byte vectors).
+template <class T, int VPT>
+__device__ __forceinline__ float slice_dot(const float (&xr)[VPT][Vec<T>::EV],
+                                           const uint4 (&w)[VPT]) {
+  constexpr int EV = Vec<T>::EV;
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    float f[EV];
+    Vec<T>::unpack(w[v], f);
+#pragma unroll
+    for (int e = 0; e < EV; ++e) s = fmaf(xr[v][e], f[e], s);
+  }
+  return s;
+}
+
+// Reduce 8 per-lane values across the warp with 9 shuffles (a transposing
+// reduction); afterwards lane L holds the warp total of value (L >> 2) & 7.
+__device__ __forceinline__ float warp_reduce8(float (&p)[PB]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 16;
+    const float send = hi ? p[i] : p[i + 4];
+    const float keep = hi ? p[i + 4] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 8;
+    const float send = hi ? p[i] : p[i + 2];
+    const float keep = hi ? p[i + 2] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const bool hi = lane & 4;
+    const float send = hi ? p[0] : p[1];
+    const float keep = hi ? p[1] : p[0];
+    p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+  p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+  return p[0];
+}
+
+// Sum the PB per-thread partial values across the CTA.  Every thread gets
+// the PB totals in out[] (fixed reduction order: deterministic).
+// s_red must hold PB x 33 floats and s_tot PB floats; contains 2 barriers.
+__device__ __forceinline__ void block_reduce8(float (&pd)[PB], float (&out)[PB],
+                                              float (*s_red)[33], float *s_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float wsum = warp_reduce8(pd);
+  if ((lane & 3) == 0) s_red[lane >> 2][w] = wsum;
+  __syncthreads();
+  if (threadIdx.x < PB) {
+    float u = 0.f;
+    for (int q = 0; q < nw; ++q) u += s_red[threadIdx.x][q];
+    s_tot[threadIdx.x] = u;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < PB; ++b) out[b] = s_tot[b];
+}
+
+// Where the active pairs of one (row, tile) come from.  Rows whose tiles all
+// fit their K slots read the TwELL slots; an overflow row reads a dense vector
+// of C ReLU values for each tile (the wide-tile buffer in the forward, the
+// dense backup row in the backward) -- always (dense_all) or only for the
+// tiles whose true count exceeds K.
+template <class T>
+struct PairSource {
+  const uint8_t *idx, *nnz;
+  const T *val;
+  int Tn, C, K;
+  int t;                 // token
+  const T *dense;        // dense vector base (nullptr: slots only)
+  size_t dense_tile;     // element stride between consecutive tiles' vectors
+  bool dense_all;        // every tile from the dense vectors
+  bool neg_slots;        // encode slots as -1 - n (results go to a dense row)
+};
+
+// Compact the pairs of tiles [g0, g0 + group) of one token into the shared
+// list: s_n = neuron, s_g = gate value, s_slot = TwELL slot (or -1 - n).
+// Returns the pair count.  Pairs are in ascending neuron order.  Contains
+// barriers: every thread of the CTA must call it.
+template <class T>
+__device__ __forceinline__ int build_pairs(const PairSource<T> &ps, int g0, int group, int nt,
+                                           int *s_n, float *s_g, int *s_slot, int *s_wsum,
+                                           int *s_total, int32_t *status) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+  const int j = g0 + tid;
+  const bool mine = tid < group && j < nt;
+  const int nz = mine ? (int)ps.nnz[(size_t)j * ps.Tn + ps.t] : 0;
+  const bool from_dense = mine && ps.dense && (ps.dense_all || nz > ps.K);
+  const int cnt = from_dense ? nz : (nz < ps.K ? nz : ps.K);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int v = lane < nw ? s_wsum[lane] : 0;
+    int wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    if (lane < nw) s_wsum[lane] = wi - v;
+    if (lane == 31) *s_total = wi;
+  }
+  __syncthreads();
+  const int off = s_wsum[w] + incl - cnt;
+  if (cnt > 0) {
+    if (from_dense) {
+      const T *dv = ps.dense + (size_t)j * ps.dense_tile;
+      int k = 0;
+      for (int c = 0; c < ps.C && k < cnt; ++c) {
+        const float g = to_f(dv[c]);
+        if (g > 0.f) {
+          const int n = j * ps.C + c;
+          s_n[off + k] = n;
+          s_g[off + k] = g;
+          s_slot[off + k] = -1 - n;
+          ++k;
+        }
+      }
+      for (; k < cnt; ++k) {  // fewer positive values than counted: no-op pairs
+        s_n[off + k] = j * ps.C;
+        s_g[off + k] = 0.f;
+        s_slot[off + k] = -1 - j * ps.C;
+      }
+    } else {
+      const size_t s0 = ((size_t)j * ps.Tn + ps.t) * (size_t)ps.K;
+      for (int k = 0; k < cnt; ++k) {
+        int c = ps.idx[s0 + k];
+        if (c >= ps.C) {
+          set_status(status, TWELL_ERR_INDEX);
+          c = 0;
+        }
+        const int n = j * ps.C + c;
+        s_n[off + k] = n;
+        s_g[off + k] = to_f(ps.val[s0 + k]);
+        s_slot[off + k] = ps.neg_slots ? -1 - n : (int)(s0 + k);
+      }
+    }
+  }
+  __syncthreads();
+  return *s_total;
+}
+
+}  // namespace twell

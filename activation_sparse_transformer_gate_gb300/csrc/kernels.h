@@ -14,10 +14,13 @@ struct Ctl;
 // Workspace carve-up shared by all entry points.
 struct Workspace {
   Ctl *ctl;           // control block
+  uint32_t *ovf_bits; // [ceil(T/32)] overflow-row bitmap (set by the gate epilogue)
   int32_t *rows;      // [T] rows of the dense path (hybrid: overflow rows)
   int32_t *pos;       // [T] overflow position of each row, -1 if none
   void *h;            // [T][F] dtype: h rows of the dense path
   void *xg;           // [T][D] dtype: gathered x rows of the dense path
+  void *wide;         // [F/C][T][C] dtype: full ReLU(z) of overflowing (tile, row)s
+  void *urows;        // [T][F] dtype (training): u rows from the dense path
   // backward scratch
   float *dz;          // [F/C][T][K] fp32: dz at the slots
   float *du;          // [F/C][T][K] fp32: du at the slots
@@ -26,9 +29,9 @@ struct Workspace {
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
   int32_t *col_tok;   // [T*(F/C)*K] token of each transposed entry
   int32_t *col_slot;  // [T*(F/C)*K] slot of each transposed entry
-  void *dzr;          // [T][F] dtype: dz rows of the dense path
-  void *dur;          // [T][F] dtype: du rows of the dense path
-  void *dyg;          // [T][D] dtype: gathered dy rows of the dense path
+  float *dzr;         // [T][F] fp32: dz rows of the overflow rows
+  float *dur;         // [T][F] fp32: du rows of the overflow rows
+  float *hr;          // [T][F] fp32: h rows of the overflow rows
   size_t bytes;       // total bytes needed
 };
 
@@ -57,8 +60,19 @@ struct BwdArgs {
 
 // pack.cu
 cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
+// Hybrid split.  With a workspace: reads the overflow-row bitmap (which must
+// hold the flags of this call), writes the row list / positions / control
+// block and -- when write_user -- the caller's ovf_rows and n_ovf.  Without a
+// workspace: derives the flags from nnz (one CTA) and writes only the caller's
+// list and count.
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
-                                    cudaStream_t s);
+                                    cudaStream_t s, bool write_user = true);
+// Overflow-row bitmap from the nnz counts (clears the bitmap first).
+cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s);
+// Dense backup rows of overflow rows that do not take the dense GEMM path.
+cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s);
+// All-dense training forward: u at the slots of the non-overflow rows.
+cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s);
 cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
                                int dtype, cudaStream_t s);
@@ -90,7 +104,9 @@ enum KernelId {
   KID_BWD_TRANSPOSE = 10,
   KID_BWD_DW = 11,
   KID_BWD_DENSE = 12,
-  KID_COUNT = 13
+  KID_FILL_U = 13,
+  KID_ASSEMBLE_FB = 14,
+  KID_COUNT = 15
 };
 // Record a timing event after a launch of kernel `id` (no-op unless enabled).
 void prof_mark(int id, cudaStream_t s);

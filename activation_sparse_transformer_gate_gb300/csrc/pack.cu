@@ -1,5 +1,6 @@
 // pack.cu -- TwELL packing of a dense activation matrix, the overflow-row
-// compaction that turns TwELL into the hybrid format, and row gathers.
+// compaction that turns TwELL into the hybrid format, and the small row
+// kernels around it.
 //
 // "Sparser, Faster, Lighter Transformer Language Models", technical summary
 // section 2.A: TwELL keeps K (index, value) slots per (row, tile of C
@@ -73,18 +74,24 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s) 
   return cudaGetLastError();
 }
 
-// Hybrid split (one CTA of 1024 threads): a row overflows iff one of its tiles
-// has nnz > K.  Rows are visited in ascending order, 1024 at a time; a
-// ballot/popc block scan gives each overflow row its list position, so the
-// list is ascending and deterministic.  Writes the caller's list (first
-// ovf_cap entries) and count, and -- when a workspace is given -- the full
-// dense-path row list, each row's position, and the control block that picks
-// hybrid or all-dense mode.
+// Mode decisions taken on the device after the overflow rows are counted.
+__device__ __forceinline__ void write_ctl(Ctl *ctl, int n_ovf, int Tn, float dense_switch) {
+  const int dense = (float)n_ovf > dense_switch * (float)Tn ? 1 : 0;
+  const int og = (!dense && n_ovf >= OVF_GEMM_MIN) ? 1 : 0;
+  ctl->n_ovf = n_ovf;
+  ctl->dense = dense;
+  ctl->ovf_gemm = og;
+  ctl->n_rows = dense ? Tn : (og ? n_ovf : 0);
+}
+
+// Hybrid split from nnz (one CTA of 1024 threads, no workspace): a row
+// overflows iff one of its tiles has nnz > K.  Rows are visited in ascending
+// order, 1024 at a time; a ballot/popc block scan gives each overflow row its
+// list position, so the list is ascending and deterministic.
 __global__ void __launch_bounds__(1024)
 overflow_compact_kernel(const uint8_t *__restrict__ nnz, int Tn, int nt, int K, int cap,
                         int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf,
-                        int32_t *status, Ctl *ctl, int32_t *__restrict__ rows,
-                        int32_t *__restrict__ pos, float dense_switch) {
+                        int32_t *status) {
   __shared__ int warp_cnt[32];
   __shared__ int warp_off[32];
   __shared__ int total;
@@ -116,33 +123,118 @@ overflow_compact_kernel(const uint8_t *__restrict__ nnz, int Tn, int nt, int K, 
     }
     __syncthreads();
     const int p = running + warp_off[w] + __popc(b & ((1u << lane) - 1u));
-    if (t < Tn) {
-      if (flag) {
-        if (rows) rows[p] = t;
-        if (p < cap) ovf_rows[p] = t;
-      }
-      if (pos) pos[t] = flag ? p : -1;
-    }
+    if (t < Tn && flag && p < cap) ovf_rows[p] = t;
     running += total;
     __syncthreads();
   }
   if (tid == 0) {
     *n_ovf = running;
     if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
-    if (ctl) {
-      const int dense = (float)running > dense_switch * (float)Tn ? 1 : 0;
-      ctl->n_ovf = running;
-      ctl->dense = dense;
-      ctl->n_rows = dense ? Tn : running;
+  }
+}
+
+// Hybrid split from the overflow-row bitmap (one CTA of 1024 threads).  Each
+// thread owns one 32-row word per round; a block scan of the word popcounts
+// gives each overflow row its ascending list position.
+__global__ void __launch_bounds__(1024)
+overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
+                     int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf, int32_t *status,
+                     Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
+                     float dense_switch) {
+  __shared__ int warp_off[32];
+  __shared__ int word_off[1024];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int words = (Tn + 31) / 32;
+  int running = 0;
+  for (int base = 0; base < words; base += 1024) {
+    const int wi = base + tid;
+    const uint32_t word = wi < words ? bits[wi] : 0u;
+    const int c = __popc(word);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
     }
+    if (lane == 31) warp_off[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      const int v = warp_off[lane];
+      int wi2 = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, wi2, o);
+        if (lane >= o) wi2 += u;
+      }
+      warp_off[lane] = wi2 - v;
+      if (lane == 31) total = wi2;
+    }
+    __syncthreads();
+    const int off = running + warp_off[w] + incl - c;
+    word_off[tid] = off;
+    uint32_t m = word;
+    int k = 0;
+    while (m) {  // list entries in ascending row order
+      const int b = __ffs(m) - 1;
+      m &= m - 1;
+      const int t = wi * 32 + b;
+      rows[off + k] = t;
+      if (ovf_rows && off + k < cap) ovf_rows[off + k] = t;
+      ++k;
+    }
+    __syncthreads();
+    const int r0 = base * 32;  // positions of every row (coalesced)
+    for (int r = tid; r < 1024 * 32; r += 1024) {
+      const int t = r0 + r;
+      if (t >= Tn) break;
+      const uint32_t wd = bits[t >> 5];
+      const int b = t & 31;
+      pos[t] = ((wd >> b) & 1u) ? word_off[r >> 5] + __popc(wd & ((1u << b) - 1u)) : -1;
+    }
+    running += total;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if (n_ovf) *n_ovf = running;
+    if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
+    write_ctl(ctl, running, Tn, dense_switch);
   }
 }
 
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
-                                    cudaStream_t s) {
-  overflow_compact_kernel<<<1, 1024, 0, s>>>(
-      tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap, tw.ovf_rows, tw.n_ovf, tw.status,
-      ws ? ws->ctl : nullptr, ws ? ws->rows : nullptr, ws ? ws->pos : nullptr, dense_switch);
+                                    cudaStream_t s, bool write_user) {
+  if (ws) {
+    overflow_scan_kernel<<<1, 1024, 0, s>>>(ws->ovf_bits, tw.T, tw.ovf_cap,
+                                            write_user ? tw.ovf_rows : nullptr,
+                                            write_user ? tw.n_ovf : nullptr, tw.status, ws->ctl,
+                                            ws->rows, ws->pos, dense_switch);
+    return cudaGetLastError();
+  }
+  overflow_compact_kernel<<<1, 1024, 0, s>>>(tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,
+                                             tw.ovf_rows, tw.n_ovf, tw.status);
+  return cudaGetLastError();
+}
+
+// Overflow-row bitmap from nnz: one thread per (tile, row).
+__global__ void flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, long total, int Tn, int K,
+                                      uint32_t *__restrict__ bits) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    if (nnz[i] > K) {
+      const int t = (int)(i % Tn);
+      atomicOr(&bits[t >> 5], 1u << (t & 31));
+    }
+  }
+}
+
+cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(ws.ovf_bits, 0, 4 * (((size_t)tw.T + 31) / 32), s);
+  if (e != cudaSuccess) return e;
+  const long total = (long)tw.T * (tw.F / tw.C);
+  long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  flags_from_nnz_kernel<<<(unsigned)blocks, 256, 0, s>>>(tw.nnz, total, tw.T, tw.K, ws.ovf_bits);
   return cudaGetLastError();
 }
 
@@ -169,12 +261,12 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
   return cudaGetLastError();
 }
 
-// dst[m] = src[rows[m]] for the dense-path rows (hybrid mode only; in all-dense
-// mode the consumers read src directly).
+// dst[m] = src[rows[m]] for the overflow rows when they take the dense GEMM
+// path (in all-dense mode the GEMMs read src directly).
 __global__ void gather_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                    int row_vecs, const Ctl *__restrict__ ctl,
                                    const int32_t *__restrict__ rows) {
-  if (ctl->dense) return;
+  if (ctl->dense || !ctl->ovf_gemm) return;
   const int n = ctl->n_rows;
   for (int m = blockIdx.x; m < n; m += gridDim.x) {
     const uint4 *a = src + (size_t)rows[m] * row_vecs;
@@ -189,6 +281,90 @@ cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, 
   int blocks = T < 1216 ? T : 1216;
   gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, D * es / 16, ws.ctl,
                                             ws.rows);
+  return cudaGetLastError();
+}
+
+// Dense backup rows of the overflow rows (when they do not take the dense GEMM
+// path): zeros, then the slots of the tiles that fit and the wide tiles of
+// those that overflow.  One CTA per overflow-list position.
+template <class T>
+__global__ void assemble_fb_rows_kernel(const Ctl *__restrict__ ctl,
+                                        const int32_t *__restrict__ rows,
+                                        const uint8_t *__restrict__ idx,
+                                        const uint8_t *__restrict__ nnz, const T *__restrict__ val,
+                                        const T *__restrict__ wide, T *__restrict__ g_fb, int Tn,
+                                        int F, int C, int K, int cap) {
+  if (ctl->dense || ctl->ovf_gemm) return;
+  const int n_fb = min(ctl->n_ovf, cap);
+  for (int i = blockIdx.x; i < n_fb; i += gridDim.x) {
+    const int t = rows[i];
+    T *row = g_fb + (size_t)i * F;
+    for (int n = threadIdx.x; n < F; n += blockDim.x) row[n] = from_f<T>(0.f);
+    __syncthreads();
+    for (int j = threadIdx.x; j < F / C; j += blockDim.x) {
+      const size_t tj = (size_t)j * Tn + t;
+      const int cnt = nnz[tj];
+      if (cnt > K) {
+        for (int c = 0; c < C; ++c) row[(size_t)j * C + c] = wide[tj * C + c];
+      } else {
+        for (int k = 0; k < cnt; ++k) {
+          const int c = idx[tj * K + k];
+          if (c < C) row[(size_t)j * C + c] = val[tj * K + k];
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s) {
+  if (a.tw.ovf_cap <= 0) return cudaSuccess;
+  int blocks = a.tw.ovf_cap < a.T ? a.tw.ovf_cap : a.T;
+  if (blocks > OVF_GEMM_MIN) blocks = OVF_GEMM_MIN;
+  if (a.dtype == TWELL_BF16)
+    assemble_fb_rows_kernel<bf16><<<blocks, 256, 0, s>>>(
+        a.ws.ctl, a.ws.rows, a.tw.idx, a.tw.nnz, (const bf16 *)a.tw.val, (const bf16 *)a.ws.wide,
+        (bf16 *)a.tw.g_fb, a.T, a.F, a.C, a.K, a.tw.ovf_cap);
+  else
+    assemble_fb_rows_kernel<float><<<blocks, 256, 0, s>>>(
+        a.ws.ctl, a.ws.rows, a.tw.idx, a.tw.nnz, (const float *)a.tw.val,
+        (const float *)a.ws.wide, (float *)a.tw.g_fb, a.T, a.F, a.C, a.K, a.tw.ovf_cap);
+  return cudaGetLastError();
+}
+
+// All-dense training forward: u at the slots of the non-overflow rows, read
+// from the u rows the dense gate+up GEMM wrote.  One thread per (tile, row).
+template <class T>
+__global__ void fill_u_slots_kernel(const Ctl *__restrict__ ctl, const int32_t *__restrict__ pos,
+                                    const uint8_t *__restrict__ idx,
+                                    const uint8_t *__restrict__ nnz, const T *__restrict__ urows,
+                                    T *__restrict__ u_val, int Tn, int F, int C, int K) {
+  if (!ctl->dense) return;
+  const long total = (long)Tn * (F / C);
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(i % Tn), j = (int)(i / Tn);
+    if (pos[t] >= 0) continue;  // overflow rows keep u in the dense backup
+    const int n = nnz[i] < K ? nnz[i] : K;
+    for (int k = 0; k < n; ++k) {
+      const int c = idx[i * K + k];
+      if (c < C) u_val[i * K + k] = urows[(size_t)t * F + (size_t)j * C + c];
+    }
+  }
+}
+
+cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s) {
+  const long total = (long)a.T * (a.F / a.C);
+  long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (a.dtype == TWELL_BF16)
+    fill_u_slots_kernel<bf16><<<(unsigned)blocks, 256, 0, s>>>(
+        a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const bf16 *)a.ws.urows, (bf16 *)a.tw.u_val,
+        a.T, a.F, a.C, a.K);
+  else
+    fill_u_slots_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+        a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const float *)a.ws.urows, (float *)a.tw.u_val,
+        a.T, a.F, a.C, a.K);
   return cudaGetLastError();
 }
 

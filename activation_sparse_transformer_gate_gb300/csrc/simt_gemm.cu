@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(NT)
 simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
                       const float *__restrict__ bg, const float *__restrict__ rb, int Tn, int D,
                       int F, int K, uint8_t *__restrict__ idx, T *__restrict__ val,
-                      uint8_t *__restrict__ nnz) {
+                      uint8_t *__restrict__ nnz, uint32_t *__restrict__ ovf_bits,
+                      T *__restrict__ wide) {
   constexpr int TN = BN / 16;
   constexpr int E = BN / 32;
   __shared__ float smem[BM * (BN + 1) > BK * (BM + 4) + BK * (BN + 4) ? BM * (BN + 1)
@@ -123,7 +124,15 @@ simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
         idx[s0 + k] = 0xFF;
         val[s0 + k] = from_f<T>(0.f);
       }
-    if (lane == 0) nnz[(size_t)j * Tn + t] = (uint8_t)cnt;
+    if (lane == 0) {
+      nnz[(size_t)j * Tn + t] = (uint8_t)cnt;
+      if (cnt > K) atomicOr(&ovf_bits[t >> 5], 1u << (t & 31));
+    }
+    if (cnt > K) {  // overflowing (row, tile): keep the full ReLU(z) tile
+      T *wd = wide + ((size_t)j * Tn + t) * BN;
+#pragma unroll
+      for (int e = 0; e < E; ++e) wd[lane + 32 * e] = from_f<T>(v[e] > 0.f ? v[e] : 0.f);
+    }
   }
 }
 
@@ -132,7 +141,7 @@ cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s) {
 #define TW_GP(TT, BNN)                                                                         \
   simt_gate_pack_kernel<TT, BNN><<<grid, NT, 0, s>>>(                                          \
       (const TT *)a.x, (const TT *)a.Wg, a.bg, a.rb, a.T, a.D, a.F, a.K, a.tw.idx,             \
-      (TT *)a.tw.val, a.tw.nnz)
+      (TT *)a.tw.val, a.tw.nnz, a.ws.ovf_bits, (TT *)a.ws.wide)
   if (a.dtype == TWELL_BF16) {
     if (a.C == 32) TW_GP(bf16, 32); else if (a.C == 64) TW_GP(bf16, 64); else TW_GP(bf16, 128);
   } else {
@@ -157,7 +166,7 @@ struct RowsParams {
   int Tn, D, F, cap, gated, train;
   const Ctl *ctl;
   const int32_t *rows, *pos;
-  void *h, *g_fb, *u_fb, *y;
+  void *h, *g_fb, *u_fb, *y, *urows;
 };
 
 template <class T, int MODE>
@@ -243,6 +252,7 @@ __global__ void __launch_bounds__(NT) simt_rows_kernel(RowsParams p) {
         const float u = acc[1][i][q];
         const float hv = p.gated ? g * u : g;
         ((T *)p.h)[(size_t)m * p.F + n] = from_f<T>(hv);
+        if (dense && p.train && p.gated) ((T *)p.urows)[(size_t)m * p.F + n] = from_f<T>(u);
         const int ps = dense ? p.pos[tok] : m;
         if (ps >= 0 && ps < p.cap) {
           ((T *)p.g_fb)[(size_t)ps * p.F + n] = from_f<T>(g);
@@ -260,7 +270,7 @@ static RowsParams rows_params(const FwdArgs &a) {
   p.x = a.x; p.Wg = a.Wg; p.Wu = a.Wu; p.Wd = a.Wd; p.bg = a.bg; p.rb = a.rb;
   p.Tn = a.T; p.D = a.D; p.F = a.F; p.cap = a.tw.ovf_cap; p.gated = a.gated; p.train = a.train;
   p.ctl = a.ws.ctl; p.rows = a.ws.rows; p.pos = a.ws.pos;
-  p.h = a.ws.h; p.g_fb = a.tw.g_fb; p.u_fb = a.tw.u_fb; p.y = a.y;
+  p.h = a.ws.h; p.g_fb = a.tw.g_fb; p.u_fb = a.tw.u_fb; p.y = a.y; p.urows = a.ws.urows;
   return p;
 }
 

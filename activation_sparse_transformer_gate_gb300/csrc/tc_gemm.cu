@@ -168,8 +168,10 @@ struct TcParams {
   const float *bg, *rb;
   const int32_t *rows, *pos;
   uint8_t *idx, *nnz;
+  uint32_t *ovf_bits;
   bf16 *val;
   bf16 *h, *g_fb, *u_fb, *y;
+  bf16 *wide, *urows;
   float *out;              // EPI_F32
   int32_t *status;
 };
@@ -419,6 +421,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
               for (int k = 0; k < K; ++k) gv[k] = my_val[k];
             }
             p.nnz[(size_t)j * p.Tn + m] = (uint8_t)cnt;
+            if (cnt > K) atomicOr(&p.ovf_bits[m >> 5], 1u << (m & 31));
+          }
+          // An overflowing (row, tile) also keeps its full ReLU(z) tile (the
+          // accumulator is read again; the load is warp-collective).
+          const bool wide_row = row_ok && tile_ok && cnt > K;
+          if (__any_sync(0xffffffffu, wide_row)) {
+            for (int c0 = 0; c0 < p.C; c0 += 32) {
+              float v[32];
+              tmem_ld32(tacc + jt * p.C + c0, v);
+              if (!wide_row) continue;
+              uint32_t wv[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float z0 = (v[i] + s_bias[jt * p.C + c0 + i]) + rbv;
+                const float z1 = (v[i + 1] + s_bias[jt * p.C + c0 + i + 1]) + rbv;
+                wv[i / 2] = pack_bf2(z0 > 0.f ? z0 : 0.f, z1 > 0.f ? z1 : 0.f);
+              }
+              uint4 *wd = (uint4 *)(p.wide + ((size_t)j * p.Tn + m) * p.C + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                wd[v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+            }
           }
         }
       } else if (EPI == EPI_GU) {
@@ -450,6 +474,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+          if (dense_all && p.train && p.gated) {  // u at the slots of non-overflow rows
+            uint4 *ur = (uint4 *)(p.urows + (size_t)m * p.F + n0 + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              ur[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+          }
           if (fb_ok) {
             uint4 *gd = (uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
 #pragma unroll
@@ -581,6 +611,9 @@ TcParams base_params(const FwdArgs &a) {
   p.Tn = a.T; p.F = a.F; p.D = a.D; p.C = a.C; p.Kslots = a.K; p.cap = a.tw.ovf_cap;
   p.gated = a.gated; p.train = a.train; p.bg = a.bg; p.rb = a.rb; p.rows = a.ws.rows;
   p.pos = a.ws.pos; p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val;
+  p.ovf_bits = a.ws.ovf_bits;
+  p.wide = (bf16 *)a.ws.wide;
+  p.urows = (bf16 *)a.ws.urows;
   p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;
   p.status = a.tw.status;
   return p;

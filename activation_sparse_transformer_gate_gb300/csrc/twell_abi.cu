@@ -58,7 +58,7 @@ static const char *kKernelNames[KID_COUNT] = {
     "gate_gemm_relu_twell", "overflow_compact", "twell_updown_fused", "gather_rows",
     "dense_rows_gate_up",   "dense_rows_down",  "pack_dense",         "copy_fb_rows",
     "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
-    "bwd_dense_rows"};
+    "bwd_dense_rows",       "fill_u_slots",     "assemble_fb_rows"};
 
 Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
   Workspace w;
@@ -72,11 +72,14 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     return base ? (void *)((char *)base + o) : nullptr;
   };
   w.ctl = (Ctl *)take(sizeof(Ctl));
+  w.ovf_bits = (uint32_t *)take(4 * (((size_t)T + 31) / 32));
   w.rows = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   w.pos = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   w.h = take(es * (size_t)T * F);
   w.xg = take(es * (size_t)T * D);
+  w.wide = take(es * (size_t)T * F);
   if (train) {
+    w.urows = take(es * (size_t)T * F);
     const size_t slots = nt * (size_t)T * (size_t)K;
     w.dz = (float *)take(4 * slots);
     w.du = (float *)take(4 * slots);
@@ -85,9 +88,9 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_tok = (int32_t *)take(4 * slots);
     w.col_slot = (int32_t *)take(4 * slots);
-    w.dzr = take(es * (size_t)T * F);
-    w.dur = take(es * (size_t)T * F);
-    w.dyg = take(es * (size_t)T * D);
+    w.dzr = (float *)take(4 * (size_t)T * F);
+    w.dur = (float *)take(4 * (size_t)T * F);
+    w.hr = (float *)take(4 * (size_t)T * F);
   }
   w.bytes = off;
   return w;
@@ -151,8 +154,10 @@ bool use_tc(int dtype) { return dtype == TWELL_BF16 && tc_available(); }
 
 // Steps 1-2 of the forward (shared by twell_pack and twell_ffn_forward).
 cudaError_t run_gate_and_split(FwdArgs &a, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(a.ws.ovf_bits, 0, 4 * (((size_t)a.T + 31) / 32), s);
+  if (e != cudaSuccess) return e;
   prof_mark(KID_START, s);
-  cudaError_t e = use_tc(a.dtype) ? launch_tc_gate_pack(a, s) : launch_simt_gate_pack(a, s);
+  e = use_tc(a.dtype) ? launch_tc_gate_pack(a, s) : launch_simt_gate_pack(a, s);
   if (e != cudaSuccess) return e;
   prof_mark(KID_GATE_PACK, s);
   e = launch_overflow_compact(a.tw, &a.ws, a.dense_switch, s);
@@ -231,7 +236,11 @@ twell_status twell_pack(const void *x, const void *Wg, const float *bg, const fl
   a.dense_switch = 2.0f;  // the pack never switches to all-dense mode
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = run_gate_and_split(a, s);
-  if (e == cudaSuccess) e = run_dense_rows(a, false, s);  // fills g_fb of the overflow rows
+  if (e == cudaSuccess) {  // dense backup rows: assembled (few rows) or recomputed (many)
+    e = launch_assemble_fb_rows(a, s);
+    prof_mark(KID_ASSEMBLE_FB, s);
+  }
+  if (e == cudaSuccess) e = run_dense_rows(a, false, s);
   return cuda_status(e);
 }
 
@@ -265,6 +274,10 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
     prof_mark(KID_UPDOWN, s);
   }
   if (e == cudaSuccess) e = run_dense_rows(a, true, s);
+  if (e == cudaSuccess && a.train && a.gated) {
+    e = launch_fill_u_slots(a, s);
+    prof_mark(KID_FILL_U, s);
+  }
   return cuda_status(e);
 }
 

@@ -1,0 +1,141 @@
+"""GPU parity of the sparse backward (per-token SDDMM + dx SpMM, sparse
+transpose, dW gathers, overflow rows from the dense backup, L1 term) against
+the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import activation_sparse_transformer_gate_gb300 as tw
+import oracle
+import synth
+from twell_testlib import assert_close_rms, to_np64, torch_dev, z_allowance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    tw._build.build()
+    tw.load()
+
+
+def run_train(a, w, lam, ovf_cap=None):
+    T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
+    dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    d = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
+    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True)
+    ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
+    y = torch.empty((T, D), dtype=tdt, device="cuda")
+    tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 1, bufs.t, y, ws, nws)
+    dx = torch.full((T, D), float("nan"), dtype=tdt, device="cuda")
+    dWg = torch.full((F, D), float("nan"), dtype=torch.float32, device="cuda")
+    dWu = torch.full_like(dWg, float("nan")) if d["Wu"] is not None else None
+    dWd = torch.full_like(dWg, float("nan"))
+    dbg = torch.full((F,), float("nan"), dtype=torch.float32, device="cuda")
+    tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], lam, D, dx, dWg, dbg,
+                          dWu, dWd, ws, nws)
+    code, n_ovf = tw.twell_get_status(bufs.t)
+    return dict(code=code, n_ovf=n_ovf, y=to_np64(y), dx=to_np64(dx), dWg=to_np64(dWg),
+                dbg=to_np64(dbg), dWu=None if dWu is None else to_np64(dWu), dWd=to_np64(dWd))
+
+
+def check_backward(a, w, g, lam, tok_sel=None, neu_sel=None):
+    dt = w.dtype
+    b = oracle.ffn_backward(a["x"], a["Wg"], a["bg"], a["rb"], a["Wu"], a["Wd"], a["dy"], lam, dt,
+                            dt, tok_sel=tok_sel, neu_sel=neu_sel)
+    ts = slice(None) if tok_sel is None else np.asarray(tok_sel)
+    ns = slice(None) if neu_sel is None else np.asarray(neu_sel)
+    al = z_allowance(a, dt, rows=None if tok_sel is None else ts, lam=lam) if dt == "f32" else {}
+    assert_close_rms(g["dx"][ts], b["dx"], dt, "dx", extra=al.get("dx"))
+    for k in ("dWg", "dWd", "dbg") + (("dWu",) if a["Wu"] is not None else ()):
+        ex = al.get(k)
+        assert_close_rms(g[k][ns], b[k], dt, k, out_dtype="f32",
+                         extra=None if ex is None else ex[ns])
+    # neurons that are never active have exactly zero gradient rows
+    dead = np.all(b["dWd"] == 0, axis=1)
+    if dead.any():
+        assert np.all(g["dWg"][ns][dead] == 0) and np.all(g["dWd"][ns][dead] == 0)
+        assert np.all(g["dbg"][ns][dead] == 0)
+    return b
+
+
+def test_bf16_gated_small_with_overflow_rows():
+    w = synth.Workload("bw", 300, 256, 1024, 128, 8, "bf16", True, -2.33, 21, hot_tokens=3,
+                       seq_len=100, hot_bias=1.49, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-4)
+    assert g["code"] == 0 and g["n_ovf"] >= 9
+    check_backward(a, w, g, 1e-4)
+
+
+def test_l1_term_dominant():
+    """lambda comparable to dy . Wd: the L1 gradient matters in every entry."""
+    w = synth.Workload("l1", 160, 256, 512, 64, 8, "bf16", True, -1.8, 22, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 0.5)
+    assert g["code"] == 0
+    check_backward(a, w, g, 0.5)
+
+
+def test_zero_down_weight_closed_form():
+    """W_down = 0: y = 0 and dbg[n] = lambda * sum over active tokens of |u|."""
+    w = synth.Workload("wd0", 128, 256, 512, 128, 8, "bf16", True, -1.5, 23, train=True)
+    a = synth.generate(w)
+    a["Wd"] = np.zeros_like(a["Wd"])
+    g = run_train(a, w, 0.25)
+    assert g["code"] == 0
+    assert np.all(g["y"] == 0)
+    b = check_backward(a, w, g, 0.25)
+    assert np.abs(b["dbg"]).max() > 0
+
+
+def test_config1_fp32_nongated():
+    w = synth.scaled(synth.config1(), train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3)
+    assert g["code"] == 0
+    check_backward(a, w, g, 1e-3)
+
+
+def test_nongated_bf16_with_overflow():
+    w = synth.Workload("ngb", 200, 256, 512, 64, 4, "bf16", False, -1.7, 24, hot_tokens=2,
+                       seq_len=50, hot_bias=1.5, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 0.05)
+    assert g["code"] == 0 and g["n_ovf"] >= 8
+    check_backward(a, w, g, 0.05)
+
+
+def test_many_overflow_rows_dense_gemm_path():
+    """>= 128 overflow rows (but fewer than half): the forward runs them on the
+    tensor-core dense-row GEMMs; the backward gathers them from g_fb / u_fb."""
+    w = synth.Workload("bmany", 600, 256, 1024, 128, 8, "bf16", True, -2.33, 26, hot_tokens=2,
+                       seq_len=7, hot_bias=1.6, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3)
+    assert g["code"] == 0 and 128 <= g["n_ovf"] < 300
+    check_backward(a, w, g, 1e-3)
+
+
+@pytest.mark.parametrize("C,K", [(32, 2), (64, 16), (128, 32)])
+def test_tile_shapes(C, K):
+    w = synth.Workload(f"bt{C}{K}", 96, 128, 512, C, K, "bf16", True, -1.9, 25 + K, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-2)
+    assert g["code"] == 0
+    check_backward(a, w, g, 1e-2)
+
+
+def test_config5_full_size_sampled():
+    w = synth.config5()
+    a = synth.generate(w)
+    g = run_train(a, w, w.lam)
+    assert g["code"] == 0
+    rng = np.random.default_rng(5)
+    ts = np.unique(np.concatenate([np.arange(8), rng.choice(w.T, 24, replace=False)]))
+    ns = np.unique(np.concatenate([np.arange(8), rng.choice(w.F, 24, replace=False)]))
+    check_backward(a, w, g, w.lam, tok_sel=ts, neu_sel=ns)
+    assert np.isfinite(g["dWg"]).all() and np.isfinite(g["dx"]).all()
