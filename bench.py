@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the activation-sparse (TwELL) FFN hot path on one GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the training forward (gate GEMM + ReLU + TwELL pack, hybrid split, fused sparse
+up/down, dense fallback rows, saved activations) and the sparse backward with
+the L1 term, on the gated bf16 FFN with T=4096, d_model=2048, d_ff=8192,
+tile 128, K=8, ~99% sparse (bias -2.33), lambda = 1e-4.  ``--mode fwd`` times
+the inference forward alone.
+
+Prints ONE JSON line (rank 0).  Multi-GPU: every rank runs its own replica of
+the workload (weak scaling, no collective on the data path); the timed region
+is bracketed by a barrier and a device synchronisation, and the time is the
+maximum over ranks.
+
+``--impl reference`` times the CPU oracle instead (a bounded sample of the
+same workload per step) and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import ctypes
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sparse-FFN tokens/s at 99% sparsity vs dense cuBLAS; gather HBM GB/s vs 8 TB/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["train", "fwd"], default="train")
+    ap.add_argument("--workload", default="c2",
+                    help="c2 | c3 | c4:<bias>:<K> (shapes of the pages' setting)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-dense", action="store_true", help="skip the cuBLAS dense FFN")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def workload_of(name: str, train: bool) -> synth.Workload:
+    if name == "c2":
+        w = synth.config5() if train else synth.config2()
+    elif name == "c3":
+        w = synth.config3()
+    elif name.startswith("c4"):
+        _, b, k = name.split(":")
+        w = synth.config4(float(b), int(k))
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    if train and not w.train:
+        w = synth.scaled(w, lam=1e-4, train=True)
+    return w
+
+
+def describe(w: synth.Workload, train: bool) -> str:
+    from scipy.stats import norm
+    zero = 100.0 * norm.cdf(-w.bias) if w.bias < 0 else 100.0 * (1 - norm.cdf(w.bias))
+    kind = f"training step (fwd+bwd, L1 lambda={w.lam})" if train else "inference forward"
+    s = (f"{kind} of the gated ReLU FFN, bf16, T={w.T} d_model={w.D} d_ff={w.F}, TwELL tile {w.C}"
+         f" K={w.K}, gate bias {w.bias} (~{zero:.1f}% zero)")
+    if w.hot_tokens:
+        s += f", first {w.hot_tokens} of every {w.seq_len} tokens at bias {w.bias + w.hot_bias:.2f}"
+    return s
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        busy = [c for c in sm if c >= 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": float(np.median(busy)) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def upload(torch, dev, v):
+    if v is None:
+        return None
+    if v.dtype == np.uint16:
+        return torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(v).to(dev)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import activation_sparse_transformer_gate_gb300 as tw
+    from activation_sparse_transformer_gate_gb300 import _build
+
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    lib = tw.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    train = args.mode == "train"
+    w = workload_of(args.workload, train)
+    a = synth.generate(w)
+    dtype = tw.TWELL_BF16
+    d = {k: upload(torch, dev, a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
+    T, D, F = w.T, w.D, w.F
+    bufs = tw.TwellBuffers(T, F, w.C, w.K, dtype, train=train, device=dev)
+    ws, nws = tw.workspace(T, D, F, w.C, w.K, dtype, train, device=dev)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    dx = dWg = dWu = dWd = dbg = None
+    if train:
+        dx = torch.empty_like(d["x"])
+        dWg = torch.empty((F, D), dtype=torch.float32, device=dev)
+        dWu, dWd = torch.empty_like(dWg), torch.empty_like(dWg)
+        dbg = torch.empty((F,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(x=None, dy=None):
+        xx = d["x"] if x is None else x
+        tw.twell_ffn_forward(xx, d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, int(train),
+                             bufs.t, y, ws, nws, sh)
+        if train:
+            tw.twell_ffn_backward(xx, d["Wg"], d["Wu"], d["Wd"], bufs.t,
+                                  d["dy"] if dy is None else dy, w.lam, D, dx, dWg, dbg, dWu,
+                                  dWd, ws, nws, sh)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
+
+    def timed(fn, steps):
+        """Sum of per-step device times (CUDA events on the launching stream),
+        with the L2 flushed by a large write before every step."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            flush_buf.fill_(1)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    code, n_ovf = tw.twell_get_status(bufs.t, sh)
+    if code != 0:
+        raise SystemExit(f"device status {code} after warm-up")
+    sampler = None if (args.no_clocks or rank != 0) else ClockSampler(local_rank)
+    if sampler:
+        time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    total_ms = timed(step, args.steps)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.stop() if sampler else None
+    code, n_ovf = tw.twell_get_status(bufs.t, sh)
+    if code != 0:
+        raise SystemExit(f"device status {code} after the timed region")
+    ms_step = total_ms / args.steps
+    value = T * world / (ms_step / 1e3)
+    if rank != 0:
+        return None
+
+    # ---- per-kernel times inside the step (events on the launch stream) ----
+    prof_steps = max(5, min(50, args.steps))
+    lib.twell_profile_begin()
+    for _ in range(prof_steps):
+        flush_buf.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    cap = 64 * prof_steps
+    ids = (ctypes.c_int * cap)()
+    ms = (ctypes.c_float * cap)()
+    cnt = ctypes.c_int(0)
+    lib.twell_kernel_name.restype = ctypes.c_char_p
+    lib.twell_profile_end(cap, ids, ms, ctypes.byref(cnt))
+    per = {}
+    for i in range(min(cnt.value, cap)):
+        per.setdefault(lib.twell_kernel_name(ids[i]).decode(), []).append(ms[i])
+    launches_per_step = cnt.value / prof_steps
+    kern = {k: {"launches_per_step": len(v) / prof_steps, "avg_ms": float(np.mean(v)),
+                "ms_per_step": float(np.sum(v)) / prof_steps} for k, v in per.items()}
+
+    nnz = bufs.nnz.cpu().numpy().astype(np.int64)
+    rl = kernel_rooflines(kern, w, nnz, train)
+    dominant = max((k for k in kern if k in rl), key=lambda k: kern[k]["ms_per_step"], default=None)
+    roof = None
+    if dominant:
+        r = rl[dominant]
+        roof = {"kernel": dominant, "bound": r["bound"], "achieved": round(r["achieved"], 2),
+                "peak": r["peak"], "unit": r["unit"], "frac": round(r["frac"], 4),
+                "traffic": traffic_for(dominant, args.workload, train),
+                "peak_source": r["peak_source"]}
+
+    dense = None if args.no_dense else dense_reference(torch, d, w, train, timed, args)
+    e2e = None if args.no_e2e else end_to_end(torch, d, step, y, dx, w, train, timed, args)
+    cpu = None if (args.no_cpu or world > 1) else cpu_baseline(a, w, train, args.cpu_seconds)
+
+    row_ovf = (nnz > w.K).any(axis=0)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; shapes and sparsity of the pages' FFN setting)",
+        "config": {"workload": describe(w, train), "T": T, "d_model": D, "d_ff": F, "tile": w.C,
+                   "K": w.K, "step": "fwd+bwd" if train else "fwd",
+                   "l2": f"flushed before every timed step ({flush_buf.numel() >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clocks,
+        "kernels": {k: {kk: round(vv, 5) for kk, vv in v.items()} for k, v in kern.items()},
+        "kernel_roofline": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
+                                for kk, vv in v.items()} for k, v in rl.items()},
+        "sparsity": {"active_frac": float(nnz.sum() / (T * F)), "n_ovf": int(row_ovf.sum())},
+    }
+    if dense:
+        line["dense_cublas"] = dense
+        line["speedup_vs_dense"] = round(dense["ms_per_step"] / ms_step, 4)
+    return line
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "of measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "of fallback (no MEASURED_PEAKS.json)"}
+
+
+def kernel_rooflines(kern, w, nnz, train):
+    """Achieved rate of each kernel from its algorithmic work per launch:
+    bytes for the gather kernels (rows gathered + rows streamed + TwELL),
+    flops for the gate GEMM.  See the design notes for the per-unit figures."""
+    peaks = load_peaks()
+    D, F, T, K = w.D, w.F, w.T, w.K
+    row_ovf = (nnz > K).any(axis=0)
+    sparse_rows = int((~row_ovf).sum())
+    pairs = int(np.minimum(nnz, K)[:, ~row_ovf].sum())          # pairs of TwELL rows
+    pairs_all = int(nnz.sum())                                    # incl. overflow rows
+    twell = (F // w.C) * T * (3 * K + 1)
+    wrk = {
+        # per pair: W_up + W_down rows; per token: x row in, y row out; TwELL read
+        "twell_updown_fused": ("hbm", pairs_all * 2 * D * 2 + T * D * 2 * 2 + twell),
+        # per pair: W_down + W_gate + W_up rows; per token: dy in, dx out; u + dz/du/h
+        "bwd_slots_sddmm": ("hbm", pairs_all * 3 * D * 2 + T * D * 2 * 2 + pairs_all * 14),
+        # per pair: x + dy rows and the pair's dz/du/h + list entry; 3 fp32 dW rows out
+        "bwd_dw_gather": ("hbm", pairs_all * (2 * D * 2 + 20) + 3 * F * D * 4 + F * 4),
+        "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
+    }
+    out = {}
+    for k, (bound, work) in wrk.items():
+        if k not in kern:
+            continue
+        sec = kern[k]["avg_ms"] / 1e3
+        if bound == "hbm":
+            ach, peak, unit = work / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            ach, peak, unit = work / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        out[k] = dict(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak,
+                      algorithmic=work, peak_source=peaks["source"])
+    out.setdefault("_counts", {"bound": "-", "pairs_twell_rows": pairs, "pairs_all": pairs_all,
+                               "sparse_rows": sparse_rows})
+    return out
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "activation_sparse_transformer_gate_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, workload, train):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (null otherwise)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        e = json.load(open(p)).get(f"{kernel}|{workload}|{'train' if train else 'fwd'}")
+    except ValueError:
+        return None
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def dense_reference(torch, d, w, train, timed, args):
+    """The same FFN with cuBLAS GEMMs through torch (bf16, fp32 accumulate)."""
+    x, Wg, Wu, Wd, rb, dy = d["x"], d["Wg"], d["Wu"], d["Wd"], d["rb"], d["dy"]
+    bgb = d["bg"].to(torch.bfloat16)
+    lam = w.lam
+
+    def step():
+        z = torch.addmm(bgb, x, Wg.t())
+        if rb is not None:
+            z = z + rb.to(torch.bfloat16)[:, None]
+        g = torch.relu(z)
+        u = x @ Wu.t()
+        h = g * u
+        y = h @ Wd
+        if not train:
+            return y
+        dh = dy @ Wd.t() + lam * torch.sign(h)
+        dz = torch.where(z > 0, dh * u, torch.zeros_like(dh))
+        du = dh * g
+        return (dz @ Wg + du @ Wu, dz.t() @ x, du.t() @ x, h.t() @ dy, dz.float().sum(0))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    steps = max(10, min(args.steps, 200))
+    ms = timed(step, steps) / steps
+    return {"ms_per_step": round(ms, 5), "tokens_per_s": round(w.T / (ms / 1e3), 1),
+            "what": "torch bf16 matmul (cuBLAS) dense FFN" + (" fwd+bwd" if train else " fwd"),
+            "steps": steps}
+
+
+def end_to_end(torch, d, step, y, dx, w, train, timed, args):
+    """Pinned host inputs copied in and the step's outputs copied out, every
+    step, around the same C-ABI calls."""
+    hx = d["x"].cpu().pin_memory()
+    hdy = d["dy"].cpu().pin_memory() if train else None
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hdx = torch.empty(dx.shape, dtype=dx.dtype).pin_memory() if train else None
+    gx = torch.empty_like(d["x"])
+    gdy = torch.empty_like(d["dy"]) if train else None
+
+    def e2e_step():
+        gx.copy_(hx, non_blocking=True)
+        if train:
+            gdy.copy_(hdy, non_blocking=True)
+        step(gx, gdy)
+        hy.copy_(y, non_blocking=True)
+        if train:
+            hdx.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    steps = max(10, min(args.steps, 200))
+    ms = timed(e2e_step, steps) / steps
+    h2d = hx.numel() * 2 + (hdy.numel() * 2 if train else 0)
+    d2h = hy.numel() * 2 + (hdx.numel() * 2 if train else 0)
+    return {"value": round(w.T / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5), "steps": steps}
+
+
+def oracle_sample(a, w, train, S, Fs):
+    """The oracle on S tokens and the first Fs neurons of the workload: the
+    FFN cost is linear in both, so tokens/s scales by Fs/F exactly."""
+    import oracle
+    dt = w.dtype
+    x = a["x"][:S]
+    rb = None if a["rb"] is None else a["rb"][:S]
+    Wg, Wu, Wd, bg = a["Wg"][:Fs], a["Wu"][:Fs], a["Wd"][:Fs], a["bg"][:Fs]
+    t0 = time.perf_counter()
+    oracle.ffn_dense(x, Wg, bg, rb, Wu, Wd, dt, dt)
+    if train:
+        oracle.ffn_backward(x, Wg, bg, rb, Wu, Wd, a["dy"][:S], w.lam, dt, dt)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(a, w, train, seconds):
+    import oracle
+    oracle.build()
+    S = 2
+    t = oracle_sample(a, w, train, S, w.F)
+    S = int(max(2, min(w.T, S * seconds / max(t, 1e-3))))
+    t = oracle_sample(a, w, train, S, w.F)
+    return {"value": round(S / t, 3), "unit": "tokens/s", "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": f"first {S} tokens of the workload, all {w.F} neurons, "
+                      f"{'dense fwd+bwd' if train else 'dense fwd'} in fp64 C loops (OpenMP over "
+                      f"tokens/neurons), {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample of
+    the workload (S tokens x Fs neurons), scaled to tokens/s of the full FFN."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    train = args.mode == "train"
+    w = workload_of(args.workload, train)
+    a = synth.generate(w, rows=64)
+    budget = min(10.0, 150.0 / (args.steps + max(args.warmup, 3)))
+    S, Fs = 1, w.F
+    t = oracle_sample(a, w, train, S, Fs)
+    while t > budget and Fs > 64:
+        Fs //= 2
+        t = oracle_sample(a, w, train, S, Fs)
+    while t * 2 < budget and S < 64:
+        S *= 2
+        t = oracle_sample(a, w, train, S, Fs)
+    for _ in range(max(args.warmup, 3)):
+        oracle_sample(a, w, train, S, Fs)
+    tot = sum(oracle_sample(a, w, train, S, Fs) for _ in range(args.steps))
+    ms_step = tot / args.steps * 1e3
+    value = S * Fs / w.F / (ms_step / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": describe(w, train), "T": w.T, "d_model": w.D, "d_ff": w.F,
+                   "tile": w.C, "K": w.K, "step": "fwd+bwd" if train else "fwd"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "kind": "oracle",
+                         "cores": oracle.get_threads(),
+                         "sample": f"per step: {S} token(s) x {Fs} of {w.F} neurons "
+                                   f"(cost linear in both), dense {'fwd+bwd' if train else 'fwd'}"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
