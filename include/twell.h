@@ -76,7 +76,8 @@ typedef enum {
   TWELL_ERR_TIMEOUT = -6,    /* device: a bounded pipeline wait expired      */
   TWELL_ERR_CUDA = -7,       /* a CUDA runtime/driver call failed            */
   TWELL_ERR_WORKSPACE = -8,  /* workspace NULL, misaligned or too small      */
-  TWELL_ERR_UNSUPPORTED = -9 /* valid request this build does not implement  */
+  TWELL_ERR_UNSUPPORTED = -9,/* valid request this build does not implement  */
+  TWELL_ERR_STATIC_LIMIT = -10 /* size above a fixed static-scratch maximum   */
 } twell_status;
 
 typedef enum { TWELL_F32 = 0, TWELL_BF16 = 1 } twell_dtype;
@@ -147,6 +148,25 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
  * not NULL, the overflow-row count), then clear the status word.  Returns the
  * device status (TWELL_OK when no error was recorded) or TWELL_ERR_CUDA. */
 twell_status twell_get_status(const twell_t *tw, void *stream, int32_t *n_ovf);
+
+/* Overflow-row list of an already packed TwELL, for callers that cannot
+ * allocate device memory (the paper has no counterpart: this is a library
+ * convenience).  Such callers -- code running inside an allocator or memory
+ * pool it does not own, plugin hosts that forbid allocation on their hot
+ * path -- cannot provide the workspace the other entry points take.  This
+ * call reads tw->nnz and writes tw->ovf_rows (first min(n, ovf_cap) rows,
+ * ascending), *tw->n_ovf and, when n > ovf_cap, TWELL_ERR_CAPACITY to the
+ * status word; it does not touch g_fb.  Its scratch is a fixed device array
+ * inside the library (about 2 MiB, held on every GPU that loads the library
+ * until the process exits), so it allocates nothing.
+ *   - T > TWELL_STATIC_SPLIT_MAX_T returns TWELL_ERR_STATIC_LIMIT before any
+ *     launch.
+ *   - The first call on each device looks the array's address up (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race.  The
+ *     array keeps the last call's contents; each call clears what it needs. */
+#define TWELL_STATIC_SPLIT_MAX_T 262144
+twell_status twell_hybrid_split_static(twell_t *tw, void *stream);
 
 /* Optional per-launch timing, for benchmarks.  Between twell_profile_begin
  * and twell_profile_end every entry point records a CUDA event on its stream
