@@ -10,10 +10,12 @@
 //   dWd[n] = sum_t h dy_t
 // Launch sequence (all on the caller's stream):
 //   1. hybrid split of the saved TwELL (overflow rows, in this workspace)
-//   2. one CTA per token: dh at its active pairs from gathered W_down rows,
-//      dz / du / h at those pairs, and its dx row from gathered W_gate / W_up
-//      rows (hybrid x dense).  Pairs come from the TwELL slots, or from the
-//      dense backup row of an overflow row.
+//   2. one CTA per token, two passes: dh at its active pairs from gathered
+//      W_down rows, then dz / du / h at those pairs (hybrid x dense SDDMM);
+//      then its dx row from gathered W_gate / W_up rows (dense x hybrid
+//      SpMM).  Pairs come from the TwELL slots, or from the dense backup row
+//      of an overflow row.  Two passes keep each pass's working set (one or
+//      two weight matrices) small enough to stay in L2.
 //   3. one CTA per tile: deterministic transpose of the slots into
 //      neuron-major lists ordered by token (sparse transpose)
 //   4. one CTA per neuron: dWg, dWu, dWd rows and dbg from gathered x / dy rows
@@ -46,13 +48,28 @@ __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f
 
 }  // namespace
 
+// Pair list of one token for the backward: slots for a non-overflow row, the
+// dense backup row (g_fb) for an overflow row (slot encoded as -1 - n).
+template <class T>
+__device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int ps) {
+  PairSource<T> src;
+  src.idx = p.idx; src.nnz = p.nnz; src.val = (const T *)p.val; src.Tn = p.Tn; src.C = p.C;
+  src.K = p.K; src.t = t;
+  src.dense = ps >= 0 ? (const T *)p.g_fb + (size_t)ps * p.F : nullptr;
+  src.dense_tile = p.C;
+  src.dense_all = true;
+  src.neg_slots = ps >= 0;
+  return src;
+}
+
 // ---------------------------------------------------------------------------
-// 2. Per-token sparse backward.  A non-overflow row takes its pairs from the
-// TwELL slots (u from u_val) and writes dz / du / h at the slots; an overflow
-// row takes its pairs from its dense backup row (g_fb, u_fb) and writes them
-// into the overflow-row arrays.  Both accumulate their dx row.
+// 2a. Per-token dh SDDMM (hybrid x dense): dh = dy . Wd[n] + lambda sign(h) at
+// every active pair, then dz, du, h of the pair -- at its TwELL slot for a
+// non-overflow row, in the overflow-row arrays for an overflow row.  Only
+// W_down rows are gathered, so the working set is W_down and dy.  The next
+// batch's rows are requested before the block reduction of the current one.
 template <class T, int VPT>
-__global__ void __launch_bounds__(512) bwd_token_kernel(BParams p) {
+__global__ void __launch_bounds__(512) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -63,111 +80,141 @@ __global__ void __launch_bounds__(512) bwd_token_kernel(BParams p) {
   __shared__ float s_tot[PB];
   __shared__ int s_total;
 
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int t = blockIdx.x, tid = threadIdx.x;
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
   const int ps = p.pos[t];
-  const bool ovf = ps >= 0;
-  if (ovf && ps >= p.cap) return;  // no dense backup row (capacity error raised)
+  if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
 
   const uint4 *dyrow = (const uint4 *)p.dy + (size_t)t * NV;
-  float dyr[VPT][EV], dxr[VPT][EV];
+  float dyr[VPT][EV];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
-    uint4 r = vi < NV ? dyrow[vi] : make_uint4(0, 0, 0, 0);
-    Vec<T>::unpack(r, dyr[v]);
-#pragma unroll
-    for (int e = 0; e < EV; ++e) dxr[v][e] = 0.f;
+    Vec<T>::unpack(vi < NV ? dyrow[vi] : make_uint4(0, 0, 0, 0), dyr[v]);
   }
-  const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu, *Wd4 = (const uint4 *)p.Wd;
+  const uint4 *Wd4 = (const uint4 *)p.Wd;
   const T *uval = (const T *)p.u_val;
   const T *ufb = (const T *)p.u_fb;
-  PairSource<T> src;
-  src.idx = p.idx; src.nnz = p.nnz; src.val = (const T *)p.val; src.Tn = p.Tn; src.C = p.C;
-  src.K = p.K; src.t = t;
-  src.dense = ovf ? (const T *)p.g_fb + (size_t)ps * p.F : nullptr;
-  src.dense_tile = p.C;
-  src.dense_all = true;
-  src.neg_slots = ovf;
-
-  int group = LIST_CAP / (ovf ? p.C : p.K);
+  const PairSource<T> src = bwd_source<T>(p, t, ps);
+  int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
   if (group > (int)blockDim.x) group = blockDim.x;
   for (int g0 = 0; g0 < nt; g0 += group) {
     const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
-    for (int i = tid; i < P; i += blockDim.x) {  // u of every pair, once
+    for (int i = tid; i < P; i += blockDim.x) {
       const int sl = s_slot[i];
-      s_u[i] = !p.gated ? 1.f : (sl >= 0 ? to_f(uval[sl]) : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
+      s_u[i] = (!p.gated || sl == PAD_SLOT) ? 1.f
+               : (sl >= 0 ? to_f(uval[sl]) : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
+    }
+    __syncthreads();
+    if (P > 0) {
+      uint4 wd[PB][VPT];
+      int nb = P < PB ? P : PB;
+      gather8<T, VPT>(Wd4, s_n, 0, nb, NV, wd);
+      for (int b0 = 0; b0 < P; b0 += PB) {
+        const int b1 = b0 + PB;
+        const int nb_next = P - b1 < PB ? P - b1 : PB;
+        float pd[PB];
+#pragma unroll
+        for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(dyr, wd[b]);
+        if (nb_next > 0) gather8<T, VPT>(Wd4, s_n, b1, nb_next, NV, wd);
+        float dot[PB];
+        block_reduce8(pd, dot, s_red, s_tot);
+        if (tid < nb) {
+          float d = 0.f;
+#pragma unroll
+          for (int b = 0; b < PB; ++b)
+            if (b == tid) d = dot[b];
+          const int i = b0 + tid;
+          const float g = s_g[i], u = s_u[i];
+          const float h = p.gated ? g * u : g;
+          const float dh = d + p.lambda * sgnf(h);
+          const bool act = g > 0.f;
+          const float dz = act ? (p.gated ? dh * u : dh) : 0.f;
+          const float du = act ? dh * g : 0.f;
+          const int sl = s_slot[i];
+          if (sl == PAD_SLOT) {
+          } else if (sl >= 0) {
+            p.dz[sl] = dz;
+            p.du[sl] = du;
+            p.hs[sl] = h;
+          } else {
+            const size_t o = (size_t)ps * p.F + (-1 - sl);
+            p.dzr[o] = dz;
+            p.dur[o] = du;
+            p.hr[o] = h;
+          }
+        }
+        nb = nb_next;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2b. Per-token dx SpMM (dense x hybrid): dx_t = sum over active pairs of
+// dz W_gate[n] + du W_up[n].  No reductions, no barriers in the pair loop;
+// the working set is W_gate and W_up.
+template <class T, int VPT>
+__global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
+  constexpr int EV = Vec<T>::EV;
+  __shared__ int s_n[LIST_CAP];
+  __shared__ float s_g[LIST_CAP];
+  __shared__ float s_z[LIST_CAP];
+  __shared__ float s_u[LIST_CAP];
+  __shared__ int s_slot[LIST_CAP];
+  __shared__ int s_wsum[32];
+  __shared__ int s_total;
+
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int nt = p.F / p.C;
+  const int NV = p.D / EV;
+  const int ps = p.pos[t];
+  if (ps >= p.cap) return;
+  float dxr[VPT][EV];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+#pragma unroll
+    for (int e = 0; e < EV; ++e) dxr[v][e] = 0.f;
+  const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu;
+  const PairSource<T> src = bwd_source<T>(p, t, ps);
+  int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
+  if (group > (int)blockDim.x) group = blockDim.x;
+  for (int g0 = 0; g0 < nt; g0 += group) {
+    const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
+    for (int i = tid; i < P; i += blockDim.x) {
+      const int sl = s_slot[i];
+      if (sl == PAD_SLOT) {
+        s_z[i] = 0.f;
+        s_u[i] = 0.f;
+        continue;
+      }
+      const size_t o = (size_t)ps * p.F + (-1 - sl);
+      s_z[i] = sl >= 0 ? p.dz[sl] : p.dzr[o];
+      s_u[i] = sl >= 0 ? p.du[sl] : p.dur[o];
     }
     __syncthreads();
     for (int b0 = 0; b0 < P; b0 += PB) {
       const int nb = P - b0 < PB ? P - b0 : PB;
-      float pd[PB];
-      {
-        uint4 wd[PB][VPT];
-#pragma unroll
-        for (int b = 0; b < PB; ++b) {
-          const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
-#pragma unroll
-          for (int v = 0; v < VPT; ++v) {
-            const int vi = tid + v * blockDim.x;
-            wd[b][v] = (b < nb && vi < NV) ? ldg_stream(Wd4 + rb + vi) : make_uint4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(dyr, wd[b]);
-      }
       uint4 wg[PB][VPT], wu[PB][VPT];
-#pragma unroll
-      for (int b = 0; b < PB; ++b) {
-        const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          const int vi = tid + v * blockDim.x;
-          const bool ok = b < nb && vi < NV;
-          wg[b][v] = ok ? ldg_stream(Wg4 + rb + vi) : make_uint4(0, 0, 0, 0);
-          wu[b][v] = (ok && p.gated) ? ldg_stream(Wu4 + rb + vi) : make_uint4(0, 0, 0, 0);
-        }
-      }
-      float dot[PB];
-      block_reduce8(pd, dot, s_red, s_tot);
-      float dzb[PB], dub[PB];
-#pragma unroll
-      for (int b = 0; b < PB; ++b) {
-        const float g = b < nb ? s_g[b0 + b] : 0.f;
-        const float u = b < nb ? s_u[b0 + b] : 0.f;
-        const float h = p.gated ? g * u : g;
-        const float dh = dot[b] + p.lambda * sgnf(h);
-        const bool act = b < nb && g > 0.f;
-        dzb[b] = act ? (p.gated ? dh * u : dh) : 0.f;
-        dub[b] = act ? dh * g : 0.f;
-        if (tid == b && b < nb) {
-          const int sl = s_slot[b0 + b];
-          if (sl >= 0) {
-            p.dz[sl] = dzb[b];
-            p.du[sl] = dub[b];
-            p.hs[sl] = h;
-          } else {
-            const size_t o = (size_t)ps * p.F + (-1 - sl);
-            p.dzr[o] = dzb[b];
-            p.dur[o] = dub[b];
-            p.hr[o] = h;
-          }
-        }
-      }
+      gather8<T, VPT>(Wg4, s_n, b0, nb, NV, wg);
+      if (p.gated) gather8<T, VPT>(Wu4, s_n, b0, nb, NV, wu);
 #pragma unroll
       for (int b = 0; b < PB; ++b) {
         if (b >= nb) break;
+        const float z = s_z[b0 + b], u = s_u[b0 + b];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
-          float fg[EV], fu[EV];
+          float fg[EV];
           Vec<T>::unpack(wg[b][v], fg);
-          Vec<T>::unpack(wu[b][v], fu);
 #pragma unroll
-          for (int e = 0; e < EV; ++e) {
-            dxr[v][e] = fmaf(dzb[b], fg[e], dxr[v][e]);
-            if (p.gated) dxr[v][e] = fmaf(dub[b], fu[e], dxr[v][e]);
+          for (int e = 0; e < EV; ++e) dxr[v][e] = fmaf(z, fg[e], dxr[v][e]);
+          if (p.gated) {
+            float fu[EV];
+            Vec<T>::unpack(wu[b][v], fu);
+#pragma unroll
+            for (int e = 0; e < EV; ++e) dxr[v][e] = fmaf(u, fu[e], dxr[v][e]);
           }
         }
       }
@@ -373,21 +420,31 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   prof_mark(KID_OVERFLOW_COMPACT, s);
   const bool bf = a.dtype == TWELL_BF16;
-  // 2. per-token slots / overflow rows + dx
+  // 2. per-token dh SDDMM (slots / overflow rows), then dx SpMM
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
   const int vpt = NV <= 512 ? 1 : 2;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   if (bf) {
-    if (vpt == 1) bwd_token_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_token_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
+    if (vpt == 1) bwd_dh_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_dh_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
   } else {
-    if (vpt == 1) bwd_token_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_token_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
+    if (vpt == 1) bwd_dh_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_dh_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_SLOTS, s);
+  if (bf) {
+    if (vpt == 1) bwd_dx_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_dx_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
+  } else {
+    if (vpt == 1) bwd_dx_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
+    else bwd_dx_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_mark(KID_BWD_DX, s);
   // 3. transpose
   const int nt = a.F / a.C;
   if (a.C == 32) twell_transpose_kernel<32><<<nt, 1024, 0, s>>>(p);

@@ -8,6 +8,9 @@ namespace twell {
 
 constexpr int LIST_CAP = 2048;  // (neuron, value) pairs staged per tile group
 constexpr int PB = 8;           // pairs consumed per batch
+// Slot code of a no-op pair (gate 0) that pads a dense tile whose positive
+// values are fewer than its count; consumers write nothing for it.
+constexpr int PAD_SLOT = -2147483647 - 1;
 
 template <class T> struct Vec;
 template <> struct Vec<bf16> {
@@ -32,6 +35,22 @@ template <> struct Vec<float> {
                       __float_as_uint(f[3]));
   }
 };
+
+// Gather PB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
+// 16-byte vectors of each row, as 128-bit read-only loads that skip L1.
+template <class T, int VPT>
+__device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb, int NV,
+                                        uint4 (&r)[PB][VPT]) {
+#pragma unroll
+  for (int b = 0; b < PB; ++b) {
+    const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int vi = threadIdx.x + v * blockDim.x;
+      r[b][v] = (b < nb && vi < NV) ? ldg_stream(base + rb + vi) : make_uint4(0, 0, 0, 0);
+    }
+  }
+}
 
 // Dot product of the thread's slice of a row held in registers with one
 // gathered row (16-byte vectors).
@@ -167,7 +186,7 @@ __device__ __forceinline__ int build_pairs(const PairSource<T> &ps, int g0, int 
       for (; k < cnt; ++k) {  // fewer positive values than counted: no-op pairs
         s_n[off + k] = j * ps.C;
         s_g[off + k] = 0.f;
-        s_slot[off + k] = -1 - j * ps.C;
+        s_slot[off + k] = PAD_SLOT;
       }
     } else {
       const size_t s0 = ((size_t)j * ps.Tn + ps.t) * (size_t)ps.K;

@@ -636,14 +636,18 @@ bool tc_available() {
 
 cudaError_t launch_tc_gate_pack(const FwdArgs &a, cudaStream_t s) {
   CUtensorMap mx, mw;
-  if (!make_map(&mx, a.x, a.D, a.T, 64, BM) || !make_map(&mw, a.Wg, a.D, a.F, 64, 128))
+  // 128 x 256 output tiles: each A tile feeds twice the MMA work of a
+  // 128 x 128 tile, which halves the A re-reads and the shared-memory
+  // operand traffic per flop.
+  constexpr int GBN = 256;
+  if (!make_map(&mx, a.x, a.D, a.T, 64, BM) || !make_map(&mw, a.Wg, a.D, a.F, 64, GBN))
     return cudaErrorInvalidValue;
   TcParams p = base_params(a);
   p.M_host = a.T;
   p.N = a.F;
   p.Kdim = a.D;
-  const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 127) / 128);
-  return launch_tc<128, 1, false, EPI_PACK>(mx, mx, mw, mw, p, tiles, s);
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.F + GBN - 1) / GBN);
+  return launch_tc<GBN, 1, false, EPI_PACK>(mx, mx, mw, mw, p, tiles, s);
 }
 
 cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {

@@ -38,20 +38,6 @@ struct UDParams {
   int32_t *status;
 };
 
-template <class T, int VPT>
-__device__ __forceinline__ void load_rows(const uint4 *base, const int *s_n, int b0, int nb, int NV,
-                                          uint4 (&r)[PB][VPT]) {
-#pragma unroll
-  for (int b = 0; b < PB; ++b) {
-    const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int vi = threadIdx.x + v * blockDim.x;
-      r[b][v] = (b < nb && vi < NV) ? ldg_stream(base + rb + vi) : make_uint4(0, 0, 0, 0);
-    }
-  }
-}
-
 }  // namespace
 
 // One CTA per token.  Rows that run on the dense GEMM path (all-dense mode, or
@@ -114,12 +100,12 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
     const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
     if (fb)
       for (int i = tid; i < P; i += blockDim.x)
-        ((T *)p.g_fb)[(size_t)ps * p.F + s_n[i]] = from_f<T>(s_g[i]);
+        if (s_slot[i] != PAD_SLOT) ((T *)p.g_fb)[(size_t)ps * p.F + s_n[i]] = from_f<T>(s_g[i]);
     if (P > 0) {
       uint4 wu[PB][VPT], wd[PB][VPT];
       int nb = P < PB ? P : PB;
-      if (p.gated) load_rows<T, VPT>(Wu4, s_n, 0, nb, NV, wu);
-      load_rows<T, VPT>(Wd4, s_n, 0, nb, NV, wd);
+      if (p.gated) gather8<T, VPT>(Wu4, s_n, 0, nb, NV, wu);
+      gather8<T, VPT>(Wd4, s_n, 0, nb, NV, wd);
       for (int b0 = 0; b0 < P; b0 += PB) {
         const int b1 = b0 + PB;
         const int nb_next = P - b1 < PB ? P - b1 : PB;
@@ -129,7 +115,7 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
 #pragma unroll
           for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(xr, wu[b]);
           // the next batch's W_up rows are in flight during the reduction
-          if (nb_next > 0) load_rows<T, VPT>(Wu4, s_n, b1, nb_next, NV, wu);
+          if (nb_next > 0) gather8<T, VPT>(Wu4, s_n, b1, nb_next, NV, wu);
           float u[PB];
           block_reduce8(pd, u, s_red, s_tot);
 #pragma unroll
@@ -141,7 +127,7 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
             for (int b = 0; b < PB; ++b)
               if (b == tid) uv = u[b];
             if (sl >= 0) ((T *)p.u_val)[sl] = from_f<T>(uv);
-            else if (fb) ((T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)] = from_f<T>(uv);
+            else if (fb && sl != PAD_SLOT) ((T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)] = from_f<T>(uv);
           }
         } else {
 #pragma unroll
@@ -158,7 +144,7 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
             for (int e = 0; e < EV; ++e) yr[v][e] = fmaf(h[b], f[e], yr[v][e]);
           }
         }
-        if (nb_next > 0) load_rows<T, VPT>(Wd4, s_n, b1, nb_next, NV, wd);
+        if (nb_next > 0) gather8<T, VPT>(Wd4, s_n, b1, nb_next, NV, wd);
         nb = nb_next;
       }
     }

@@ -302,8 +302,10 @@ def kernel_rooflines(kern, w, nnz, train):
     wrk = {
         # per pair: W_up + W_down rows; per token: x row in, y row out; TwELL read
         "twell_updown_fused": ("hbm", pairs_all * 2 * D * 2 + T * D * 2 * 2 + twell),
-        # per pair: W_down + W_gate + W_up rows; per token: dy in, dx out; u + dz/du/h
-        "bwd_slots_sddmm": ("hbm", pairs_all * 3 * D * 2 + T * D * 2 * 2 + pairs_all * 14),
+        # dh SDDMM: per pair a W_down row, u in and dz/du/h out; per token the dy row
+        "bwd_slots_sddmm": ("hbm", pairs_all * (D * 2 + 14) + T * D * 2),
+        # dx SpMM: per pair W_gate + W_up rows and dz/du in; per token the dx row out
+        "bwd_dx_spmm": ("hbm", pairs_all * (2 * D * 2 + 8) + T * D * 2),
         # per pair: x + dy rows and the pair's dz/du/h + list entry; 3 fp32 dW rows out
         "bwd_dw_gather": ("hbm", pairs_all * (2 * D * 2 + 20) + 3 * F * D * 4 + F * 4),
         "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
