@@ -66,33 +66,26 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
 // 2a. Per-token dh SDDMM (hybrid x dense): dh = dy . Wd[n] + lambda sign(h) at
 // every active pair, then dz, du, h of the pair -- at its TwELL slot for a
 // non-overflow row, in the overflow-row arrays for an overflow row.  Only
-// W_down rows are gathered, so the working set is W_down and dy.  The next
-// batch's rows are requested before the block reduction of the current one.
-template <class T, int VPT>
-__global__ void __launch_bounds__(512) bwd_dh_kernel(BParams p) {
+// W_down rows are gathered, so the working set is W_down and dy.  Each warp
+// computes whole dot products for its share of the pairs (two rows in
+// flight, warp shuffles only): no barrier inside the pair loop.
+template <class T, int VL, int PIF>
+__global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
-  __shared__ float s_u[LIST_CAP];
   __shared__ int s_slot[LIST_CAP];
+  __shared__ uint4 s_dy[1024];
   __shared__ int s_wsum[32];
-  __shared__ float s_red[PB][33];
-  __shared__ float s_tot[PB];
   __shared__ int s_total;
 
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nw = blockDim.x >> 5;
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
   const int ps = p.pos[t];
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
-
-  const uint4 *dyrow = (const uint4 *)p.dy + (size_t)t * NV;
-  float dyr[VPT][EV];
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    const int vi = tid + v * blockDim.x;
-    Vec<T>::unpack(vi < NV ? dyrow[vi] : make_uint4(0, 0, 0, 0), dyr[v]);
-  }
+  for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
   const uint4 *Wd4 = (const uint4 *)p.Wd;
   const T *uval = (const T *)p.u_val;
   const T *ufb = (const T *)p.u_fb;
@@ -101,40 +94,35 @@ __global__ void __launch_bounds__(512) bwd_dh_kernel(BParams p) {
   if (group > (int)blockDim.x) group = blockDim.x;
   for (int g0 = 0; g0 < nt; g0 += group) {
     const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
-    for (int i = tid; i < P; i += blockDim.x) {
-      const int sl = s_slot[i];
-      s_u[i] = (!p.gated || sl == PAD_SLOT) ? 1.f
-               : (sl >= 0 ? to_f(uval[sl]) : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
-    }
-    __syncthreads();
-    if (P > 0) {
-      uint4 wd[PB][VPT];
-      int nb = P < PB ? P : PB;
-      gather8<T, VPT>(Wd4, s_n, 0, nb, NV, wd);
-      for (int b0 = 0; b0 < P; b0 += PB) {
-        const int b1 = b0 + PB;
-        const int nb_next = P - b1 < PB ? P - b1 : PB;
-        float pd[PB];
+    for (int i0 = w; i0 < P; i0 += nw * PIF) {
+      uint4 wr[PIF][VL];
 #pragma unroll
-        for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(dyr, wd[b]);
-        if (nb_next > 0) gather8<T, VPT>(Wd4, s_n, b1, nb_next, NV, wd);
-        float dot[PB];
-        block_reduce8(pd, dot, s_red, s_tot);
-        if (tid < nb) {
-          float d = 0.f;
+      for (int q = 0; q < PIF; ++q) {
+        const int i = i0 + q * nw;
+        warp_row<VL>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
+      }
+      uint4 dw[VL];
 #pragma unroll
-          for (int b = 0; b < PB; ++b)
-            if (b == tid) d = dot[b];
-          const int i = b0 + tid;
-          const float g = s_g[i], u = s_u[i];
+      for (int k = 0; k < VL; ++k) {
+        const int vi = lane + 32 * k;
+        dw[k] = vi < NV ? s_dy[vi] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < PIF; ++q) {
+        const int i = i0 + q * nw;
+        const float d = warp_dot<T, VL>(dw, wr[q]);
+        if (lane == 0 && i < P) {
+          const int sl = s_slot[i];
+          if (sl == PAD_SLOT) continue;
+          const float g = s_g[i];
+          const float u = !p.gated ? 1.f : (sl >= 0 ? to_f(uval[sl])
+                                                    : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
           const float h = p.gated ? g * u : g;
           const float dh = d + p.lambda * sgnf(h);
           const bool act = g > 0.f;
           const float dz = act ? (p.gated ? dh * u : dh) : 0.f;
           const float du = act ? dh * g : 0.f;
-          const int sl = s_slot[i];
-          if (sl == PAD_SLOT) {
-          } else if (sl >= 0) {
+          if (sl >= 0) {
             p.dz[sl] = dz;
             p.du[sl] = du;
             p.hs[sl] = h;
@@ -145,10 +133,9 @@ __global__ void __launch_bounds__(512) bwd_dh_kernel(BParams p) {
             p.hr[o] = h;
           }
         }
-        nb = nb_next;
       }
     }
-    __syncthreads();
+    __syncthreads();  // the list is rewritten by the next group
   }
 }
 
@@ -425,13 +412,23 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int NV = a.D / EV;
   const int vpt = NV <= 512 ? 1 : 2;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
-  if (bf) {
-    if (vpt == 1) bwd_dh_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_dh_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
-  } else {
-    if (vpt == 1) bwd_dh_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_dh_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
-  }
+  const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
+#define TW_DH(TT, L) bwd_dh_kernel<TT, L, (L <= 8 ? 2 : 1)><<<a.T, 256, 0, s>>>(p)
+#define TW_DH_T(TT)                                                                            \
+  do {                                                                                         \
+    switch (vl) {                                                                              \
+      case 1: TW_DH(TT, 1); break;                                                             \
+      case 2: TW_DH(TT, 2); break;                                                             \
+      case 4: TW_DH(TT, 4); break;                                                             \
+      case 8: TW_DH(TT, 8); break;                                                             \
+      case 16: TW_DH(TT, 16); break;                                                           \
+      default: TW_DH(TT, 32); break;                                                           \
+    }                                                                                          \
+  } while (0)
+  if (bf) TW_DH_T(bf16);
+  else TW_DH_T(float);
+#undef TW_DH_T
+#undef TW_DH
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_SLOTS, s);

@@ -69,6 +69,50 @@ __device__ __forceinline__ float slice_dot(const float (&xr)[VPT][Vec<T>::EV],
   return s;
 }
 
+// ---- warp-level rows: lane l owns the 16-byte vectors l, l+32, ... of a row
+// (VPL = ceil(NV / 32) of them).  A warp reduces its own dot products with
+// shuffles, so pairs handled by different warps need no CTA barrier.
+template <int VPL>
+__device__ __forceinline__ void warp_row(const uint4 *row, int NV, bool valid, uint4 (&r)[VPL]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const int vi = lane + 32 * k;
+    r[k] = (valid && vi < NV) ? ldg_stream(row + vi) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// The lane's slice of a row kept in registers (cached loads: every warp of
+// the CTA reads the same row).
+template <int VPL>
+__device__ __forceinline__ void warp_row_cached(const uint4 *row, int NV, uint4 (&r)[VPL]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const int vi = lane + 32 * k;
+    r[k] = vi < NV ? row[vi] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Full dot product of two rows held as lane slices (warp-wide sum; every
+// lane gets the result).
+template <class T, int VPL>
+__device__ __forceinline__ float warp_dot(const uint4 (&a)[VPL], const uint4 (&b)[VPL]) {
+  constexpr int EV = Vec<T>::EV;
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    float fa[EV], fb[EV];
+    Vec<T>::unpack(a[k], fa);
+    Vec<T>::unpack(b[k], fb);
+#pragma unroll
+    for (int e = 0; e < EV; ++e) s = fmaf(fa[e], fb[e], s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
 // Reduce 8 per-lane values across the warp with 9 shuffles (a transposing
 // reduction); afterwards lane L holds the warp total of value (L >> 2) & 7.
 __device__ __forceinline__ float warp_reduce8(float (&p)[PB]) {

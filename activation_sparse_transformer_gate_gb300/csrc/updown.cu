@@ -6,17 +6,14 @@
 // keeping global-memory traffic low and working from registers and shared
 // memory.
 //
-// Design (GB300): one CTA per token.  Thread i owns the 16-byte vectors
-// i, i + blockDim, ... of the d_model axis, so every gathered weight row is read
-// by the CTA as fully coalesced 128-bit loads.  x_t and the y_t accumulators
-// stay in registers for the whole token.  The active pairs (neuron n, gate g)
-// come from the token's TwELL slots, compacted into a shared-memory list.  Pairs
-// are consumed in batches of 8: all 8 W_up and 8 W_down rows are requested
-// before any is used, the 8 partial dot products are reduced with a 9-shuffle
-// transpose-reduction per warp plus one shared-memory pass across warps, then
-// h = g * u and y += h * W_down[n].  The next batch's W_up rows are requested
-// before the reduction and its W_down rows right after the accumulation, so
-// loads stay in flight across the barriers.  All-dense mode (and overflow rows
+// Design (GB300): one CTA of 8 warps per token.  The active pairs (neuron n,
+// gate g) come from the token's TwELL slots, compacted into a shared-memory
+// list.  Phase 1: each warp computes whole dot products u = x . W_up[n] for
+// its share of the pairs (lane l owns the 16-byte vectors l, l+32, ... of the
+// row; two rows in flight per warp; warp shuffles only), so no barrier sits
+// inside the pair loop.  Phase 2: each thread owns a d_model slice of y and
+// accumulates h * W_down[n] over all pairs with 128-bit coalesced row loads,
+// 8 rows in flight.  One barrier per tile group separates the phases.  All-dense mode (and overflow rows
 // when there are many) is left to the tensor-core dense-row GEMMs; a few
 // overflow rows are handled here from the wide-tile buffer.
 #include "common.cuh"
@@ -40,19 +37,22 @@ struct UDParams {
 
 }  // namespace
 
-// One CTA per token.  Rows that run on the dense GEMM path (all-dense mode, or
-// overflow rows when there are many) are skipped; an overflow row handled
-// here takes its overflowing tiles from the wide-tile buffer and also writes
-// its dense backup row (g_fb, and u_fb when training).
-template <class T, int VPT>
-__global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
+// One CTA (8 warps) per token.  Rows that run on the dense GEMM path
+// (all-dense mode, or overflow rows when there are many) are skipped; an
+// overflow row handled here takes its overflowing tiles from the wide-tile
+// buffer and also writes its dense backup row (g_fb, and u_fb when training).
+// Per tile group: phase 1 -- warp w computes the full dot products
+// u = x . W_up[n] of pairs w, w+8, ... (two rows in flight per warp, warp
+// shuffles only); one barrier; phase 2 -- every thread accumulates its slice
+// of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
+template <class T, int VPT, int VPL, int PIF>
+__global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
   __shared__ int s_slot[LIST_CAP];
+  __shared__ uint4 s_x[1024];  // x_t, read by every warp in phase 1
   __shared__ int s_wsum[32];
-  __shared__ float s_red[PB][33];
-  __shared__ float s_tot[PB];
   __shared__ int s_total;
 
   if (p.ctl->dense) return;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
   const int ps = p.pos[t];
   const bool ovf = ps >= 0;
   if (ovf && p.ctl->ovf_gemm) return;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
   const bool fb = ovf && ps < p.cap;
@@ -73,18 +73,13 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
       if (u4) u4[v] = make_uint4(0, 0, 0, 0);
     }
   }
-
-  const uint4 *xrow = (const uint4 *)p.x + (size_t)t * NV;
-  float xr[VPT][EV], yr[VPT][EV];
+  if (p.gated)  // x_t to shared memory (visible after the barriers of build_pairs)
+    for (int v = tid; v < NV; v += blockDim.x) s_x[v] = ((const uint4 *)p.x)[(size_t)t * NV + v];
+  float yr[VPT][EV];
 #pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    const int vi = tid + v * blockDim.x;
-    uint4 r = make_uint4(0, 0, 0, 0);
-    if (p.gated && vi < NV) r = xrow[vi];
-    Vec<T>::unpack(r, xr[v]);
+  for (int v = 0; v < VPT; ++v)
 #pragma unroll
     for (int e = 0; e < EV; ++e) yr[v][e] = 0.f;
-  }
   const uint4 *Wu4 = (const uint4 *)p.Wu, *Wd4 = (const uint4 *)p.Wd;
   PairSource<T> src;
   src.idx = p.idx; src.nnz = p.nnz; src.val = (const T *)p.val; src.Tn = p.Tn; src.C = p.C;
@@ -101,51 +96,53 @@ __global__ void __launch_bounds__(512) updown_fused_kernel(UDParams p) {
     if (fb)
       for (int i = tid; i < P; i += blockDim.x)
         if (s_slot[i] != PAD_SLOT) ((T *)p.g_fb)[(size_t)ps * p.F + s_n[i]] = from_f<T>(s_g[i]);
-    if (P > 0) {
-      uint4 wu[PB][VPT], wd[PB][VPT];
-      int nb = P < PB ? P : PB;
-      if (p.gated) gather8<T, VPT>(Wu4, s_n, 0, nb, NV, wu);
-      gather8<T, VPT>(Wd4, s_n, 0, nb, NV, wd);
-      for (int b0 = 0; b0 < P; b0 += PB) {
-        const int b1 = b0 + PB;
-        const int nb_next = P - b1 < PB ? P - b1 : PB;
-        float h[PB];
-        if (p.gated) {
-          float pd[PB];
+    // ---- phase 1: u and h of every pair, one warp per pair ------------------
+    if (p.gated) {
+      for (int i0 = w; i0 < P; i0 += nw * PIF) {
+        uint4 wr[PIF][VPL];
 #pragma unroll
-          for (int b = 0; b < PB; ++b) pd[b] = slice_dot<T, VPT>(xr, wu[b]);
-          // the next batch's W_up rows are in flight during the reduction
-          if (nb_next > 0) gather8<T, VPT>(Wu4, s_n, b1, nb_next, NV, wu);
-          float u[PB];
-          block_reduce8(pd, u, s_red, s_tot);
+        for (int q = 0; q < PIF; ++q) {
+          const int i = i0 + q * nw;
+          warp_row<VPL>(Wu4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
+        }
+        uint4 xw[VPL];
 #pragma unroll
-          for (int b = 0; b < PB; ++b) h[b] = b < nb ? s_g[b0 + b] * u[b] : 0.f;
-          if (p.train && tid < nb) {
-            const int sl = s_slot[b0 + tid];
-            float uv = 0.f;
-#pragma unroll
-            for (int b = 0; b < PB; ++b)
-              if (b == tid) uv = u[b];
-            if (sl >= 0) ((T *)p.u_val)[sl] = from_f<T>(uv);
-            else if (fb && sl != PAD_SLOT) ((T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)] = from_f<T>(uv);
-          }
-        } else {
-#pragma unroll
-          for (int b = 0; b < PB; ++b) h[b] = b < nb ? s_g[b0 + b] : 0.f;
+        for (int k = 0; k < VPL; ++k) {
+          const int vi = lane + 32 * k;
+          xw[k] = vi < NV ? s_x[vi] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int b = 0; b < PB; ++b) {
-          if (b >= nb) break;
-#pragma unroll
-          for (int v = 0; v < VPT; ++v) {
-            float f[EV];
-            Vec<T>::unpack(wd[b][v], f);
-#pragma unroll
-            for (int e = 0; e < EV; ++e) yr[v][e] = fmaf(h[b], f[e], yr[v][e]);
+        for (int q = 0; q < PIF; ++q) {
+          const int i = i0 + q * nw;
+          const float u = warp_dot<T, VPL>(xw, wr[q]);
+          if (lane == 0 && i < P) {
+            s_g[i] *= u;  // h = g * u, in place
+            if (p.train) {
+              const int sl = s_slot[i];
+              if (sl >= 0) ((T *)p.u_val)[sl] = from_f<T>(u);
+              else if (fb && sl != PAD_SLOT) ((T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)] = from_f<T>(u);
+            }
           }
         }
-        if (nb_next > 0) gather8<T, VPT>(Wd4, s_n, b1, nb_next, NV, wd);
-        nb = nb_next;
+      }
+    }
+    __syncthreads();
+    // ---- phase 2: y += h * W_down[n], thread-owned slices -------------------
+    for (int b0 = 0; b0 < P; b0 += PB) {
+      const int nb = P - b0 < PB ? P - b0 : PB;
+      uint4 wd[PB][VPT];
+      gather8<T, VPT>(Wd4, s_n, b0, nb, NV, wd);
+#pragma unroll
+      for (int b = 0; b < PB; ++b) {
+        if (b >= nb) break;
+        const float h = s_g[b0 + b];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          float f[EV];
+          Vec<T>::unpack(wd[b][v], f);
+#pragma unroll
+          for (int e = 0; e < EV; ++e) yr[v][e] = fmaf(h, f[e], yr[v][e]);
+        }
       }
     }
     __syncthreads();  // the list is rewritten by the next group
@@ -166,17 +163,25 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   p.pos = a.ws.pos; p.Tn = a.T; p.D = a.D; p.F = a.F; p.C = a.C; p.K = a.K; p.gated = a.gated;
   p.train = a.train && a.gated; p.cap = a.tw.ovf_cap; p.ctl = a.ws.ctl; p.status = a.tw.status;
   const int EV = a.dtype == TWELL_BF16 ? 8 : 4;
-  const int NV = a.D / EV;
-  const int vpt = NV <= 512 ? 1 : 2;  // at most 512 threads, NV <= 1024 checked by the caller
-  int threads = (NV + vpt - 1) / vpt;
-  threads = (threads + 31) / 32 * 32;
-  if (a.dtype == TWELL_BF16) {
-    if (vpt == 1) updown_fused_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
-    else updown_fused_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
-  } else {
-    if (vpt == 1) updown_fused_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
-    else updown_fused_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
-  }
+  const int NV = a.D / EV;  // <= 1024 (checked by the caller)
+  const int vpl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
+#define TW_UD(TT, L)                                                                           \
+  updown_fused_kernel<TT, (L + 7) / 8, L, (L <= 8 ? 2 : 1)><<<a.T, 256, 0, s>>>(p)
+#define TW_UD_T(TT)                                                                            \
+  do {                                                                                         \
+    switch (vpl) {                                                                             \
+      case 1: TW_UD(TT, 1); break;                                                             \
+      case 2: TW_UD(TT, 2); break;                                                             \
+      case 4: TW_UD(TT, 4); break;                                                             \
+      case 8: TW_UD(TT, 8); break;                                                             \
+      case 16: TW_UD(TT, 16); break;                                                           \
+      default: TW_UD(TT, 32); break;                                                           \
+    }                                                                                          \
+  } while (0)
+  if (a.dtype == TWELL_BF16) TW_UD_T(bf16);
+  else TW_UD_T(float);
+#undef TW_UD_T
+#undef TW_UD
   return cudaGetLastError();
 }
 
