@@ -38,13 +38,33 @@ struct BParams {
   const int32_t *rows, *pos;
   float *dz, *du, *hs;       // slot arrays [F/C][T][K]
   float *dzr, *dur, *hr;     // overflow rows [n_ovf][F]
-  int32_t *col_start, *col_cnt, *col_tok, *col_slot;
+  int32_t *col_start, *col_cnt;
+  float4 *col_e;             // transposed entries {token bits, dz, du, h}
   void *dx;
   float *dWg, *dbg, *dWu, *dWd;
   int32_t *status;
 };
 
 __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
+
+// One list entry's weight-gradient update of a thread's 16-byte column slice:
+// ag += dz x, au += du x, ad += h dy (r = {token, dz, du, h}), packed fp32 pairs.
+template <class T>
+__device__ __forceinline__ void axpy3(float2 *ag, float2 *au, float2 *ad, const float4 &r,
+                                      const uint4 &xv, const uint4 &yv) {
+  constexpr int EV = Vec<T>::EV;
+  float fx[EV], fy[EV];
+  Vec<T>::unpack(xv, fx);
+  Vec<T>::unpack(yv, fy);
+  const float2 zz = make_float2(r.y, r.y), uu = make_float2(r.z, r.z), hh = make_float2(r.w, r.w);
+#pragma unroll
+  for (int q = 0; q < EV / 2; ++q) {
+    const float2 xf = make_float2(fx[2 * q], fx[2 * q + 1]);
+    ag[q] = __ffma2_rn(zz, xf, ag[q]);
+    au[q] = __ffma2_rn(uu, xf, au[q]);
+    ad[q] = __ffma2_rn(hh, make_float2(fy[2 * q], fy[2 * q + 1]), ad[q]);
+  }
+}
 
 }  // namespace
 
@@ -159,11 +179,11 @@ __global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
   const int NV = p.D / EV;
   const int ps = p.pos[t];
   if (ps >= p.cap) return;
-  float dxr[VPT][EV];
+  float2 dxg[VPT][EV / 2], dxu[VPT][EV / 2];  // two accumulator chains
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
 #pragma unroll
-    for (int e = 0; e < EV; ++e) dxr[v][e] = 0.f;
+    for (int e = 0; e < EV / 2; ++e) dxg[v][e] = dxu[v][e] = make_float2(0.f, 0.f);
   const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu;
   const PairSource<T> src = bwd_source<T>(p, t, ps);
   int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
@@ -193,16 +213,8 @@ __global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
         const float z = s_z[b0 + b], u = s_u[b0 + b];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
-          float fg[EV];
-          Vec<T>::unpack(wg[b][v], fg);
-#pragma unroll
-          for (int e = 0; e < EV; ++e) dxr[v][e] = fmaf(z, fg[e], dxr[v][e]);
-          if (p.gated) {
-            float fu[EV];
-            Vec<T>::unpack(wu[b][v], fu);
-#pragma unroll
-            for (int e = 0; e < EV; ++e) dxr[v][e] = fmaf(u, fu[e], dxr[v][e]);
-          }
+          axpy_vec<T>(dxg[v], z, wg[b][v]);
+          if (p.gated) axpy_vec<T>(dxu[v], u, wu[b][v]);
         }
       }
     }
@@ -212,14 +224,22 @@ __global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
-    if (vi < NV) dxrow[vi] = Vec<T>::pack(dxr[v]);
+    float o[EV];
+#pragma unroll
+    for (int e = 0; e < EV / 2; ++e) {
+      o[2 * e] = dxg[v][e].x + dxu[v][e].x;
+      o[2 * e + 1] = dxg[v][e].y + dxu[v][e].y;
+    }
+    if (vi < NV) dxrow[vi] = Vec<T>::pack(o);
   }
 }
 
 // ---------------------------------------------------------------------------
 // 3. Sparse transpose of one tile's slots into neuron-major lists.  The list of
-// neuron j*C + c occupies col_tok/col_slot[col_start .. + col_cnt) inside the
-// tile's region [j*T*K, (j+1)*T*K), ordered by token: tokens are visited 1024
+// neuron j*C + c occupies col_e[col_start .. + col_cnt) inside the tile's
+// region [j*T*K, (j+1)*T*K), ordered by token; each entry carries the token
+// and the pair's dz, du, h, so the weight-gradient pass reads one 16-byte
+// record per entry.  Tokens are visited 1024
 // at a time, and a token's rank among the tokens of its chunk that use column c
 // comes from per-warp lane masks (popc below the lane) plus per-warp offsets.
 // Overflow rows are not listed (their pairs live in the overflow-row arrays).
@@ -281,8 +301,8 @@ __global__ void __launch_bounds__(1024) twell_transpose_kernel(BParams p) {
       const int c = p.idx[s0 + k];
       if (c >= C) continue;
       const int e = woff[w][c] + __popc(occ[w][c] & lt);
-      p.col_tok[region + e] = t;
-      p.col_slot[region + e] = (int)(s0 + k);
+      const size_t sl = s0 + k;
+      p.col_e[region + e] = make_float4(__int_as_float(t), p.dz[sl], p.du[sl], p.hs[sl]);
     }
     __syncthreads();
   }
@@ -291,54 +311,51 @@ __global__ void __launch_bounds__(1024) twell_transpose_kernel(BParams p) {
 // ---------------------------------------------------------------------------
 // 4. One CTA per neuron: weight-gradient rows from the neuron's list
 // (ascending tokens), then the overflow rows (ascending).  Rows of neurons
-// that are never active are written as zeros.
+// that are never active are written as zeros.  The list is staged in shared
+// memory first (one coalesced load), so each batch of PB tokens costs one
+// round trip: its x and dy rows.
+constexpr int DW_LIST = 512;
+
 template <class T, int VPT>
-__global__ void __launch_bounds__(512) bwd_dw_kernel(BParams p) {
+__global__ void __launch_bounds__(512, 1) bwd_dw_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
+  __shared__ float4 s_e[DW_LIST];
   const int n = blockIdx.x, tid = threadIdx.x;
   const int NV = p.D / EV;
   const uint4 *x4 = (const uint4 *)p.x, *dy4 = (const uint4 *)p.dy;
-  float ag[VPT][EV], au[VPT][EV], ad[VPT][EV];
+  float2 ag[VPT][EV / 2], au[VPT][EV / 2], ad[VPT][EV / 2];
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
 #pragma unroll
-    for (int e = 0; e < EV; ++e) ag[v][e] = au[v][e] = ad[v][e] = 0.f;
+    for (int e = 0; e < EV / 2; ++e) ag[v][e] = au[v][e] = ad[v][e] = make_float2(0.f, 0.f);
   float sb = 0.f;
   const int start = p.col_start[n], cnt = p.col_cnt[n];
-  for (int e0 = 0; e0 < cnt; e0 += PB) {
-    const int nb = cnt - e0 < PB ? cnt - e0 : PB;
-    uint4 xv[PB][VPT], yv[PB][VPT];
-    float fz[PB], fu[PB], fh[PB];
+  for (int c0 = 0; c0 < cnt; c0 += DW_LIST) {
+    const int m = cnt - c0 < DW_LIST ? cnt - c0 : DW_LIST;
+    if (c0) __syncthreads();  // the previous chunk is consumed
+    for (int i = tid; i < m; i += blockDim.x) s_e[i] = p.col_e[start + c0 + i];
+    __syncthreads();
+    for (int e0 = 0; e0 < m; e0 += PB) {
+      const int nb = m - e0 < PB ? m - e0 : PB;
+      uint4 xv[PB][VPT], yv[PB][VPT];
 #pragma unroll
-    for (int b = 0; b < PB; ++b) {
-      const int e = start + e0 + (b < nb ? b : 0);
-      const int t = p.col_tok[e], sl = p.col_slot[e];
-      fz[b] = b < nb ? p.dz[sl] : 0.f;
-      fu[b] = b < nb ? p.du[sl] : 0.f;
-      fh[b] = b < nb ? p.hs[sl] : 0.f;
+      for (int b = 0; b < PB; ++b) {
+        const int t = __float_as_int(s_e[e0 + (b < nb ? b : 0)].x);
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int vi = tid + v * blockDim.x;
-        const bool ok = b < nb && vi < NV;
-        xv[b][v] = ok ? x4[(size_t)t * NV + vi] : make_uint4(0, 0, 0, 0);
-        yv[b][v] = ok ? dy4[(size_t)t * NV + vi] : make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < PB; ++b) {
-      if (b >= nb) break;
-      sb += fz[b];
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        float fx[EV], fy[EV];
-        Vec<T>::unpack(xv[b][v], fx);
-        Vec<T>::unpack(yv[b][v], fy);
-#pragma unroll
-        for (int e = 0; e < EV; ++e) {
-          ag[v][e] = fmaf(fz[b], fx[e], ag[v][e]);
-          au[v][e] = fmaf(fu[b], fx[e], au[v][e]);
-          ad[v][e] = fmaf(fh[b], fy[e], ad[v][e]);
+        for (int v = 0; v < VPT; ++v) {
+          const int vi = tid + v * blockDim.x;
+          const bool ok = b < nb && vi < NV;
+          xv[b][v] = ok ? ldg_stream(x4 + (size_t)t * NV + vi) : make_uint4(0, 0, 0, 0);
+          yv[b][v] = ok ? ldg_stream(dy4 + (size_t)t * NV + vi) : make_uint4(0, 0, 0, 0);
         }
+      }
+#pragma unroll
+      for (int b = 0; b < PB; ++b) {
+        if (b >= nb) break;
+        const float4 r = s_e[e0 + b];
+        sb += r.y;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) axpy3<T>(ag[v], au[v], ad[v], r, xv[b][v], yv[b][v]);
       }
     }
   }
@@ -348,22 +365,14 @@ __global__ void __launch_bounds__(512) bwd_dw_kernel(BParams p) {
   for (int i = 0; i < n_rows; ++i) {
     if (!(to_f(gfb[(size_t)i * p.F + n]) > 0.f)) continue;
     const int t = p.rows[i];
-    const float z = p.dzr[(size_t)i * p.F + n], u = p.dur[(size_t)i * p.F + n];
-    const float h = p.hr[(size_t)i * p.F + n];
-    sb += z;
+    const float4 r = make_float4(0.f, p.dzr[(size_t)i * p.F + n], p.dur[(size_t)i * p.F + n],
+                                 p.hr[(size_t)i * p.F + n]);
+    sb += r.y;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int vi = tid + v * blockDim.x;
       if (vi >= NV) continue;
-      float fx[EV], fy[EV];
-      Vec<T>::unpack(x4[(size_t)t * NV + vi], fx);
-      Vec<T>::unpack(dy4[(size_t)t * NV + vi], fy);
-#pragma unroll
-      for (int e = 0; e < EV; ++e) {
-        ag[v][e] = fmaf(z, fx[e], ag[v][e]);
-        au[v][e] = fmaf(u, fx[e], au[v][e]);
-        ad[v][e] = fmaf(h, fy[e], ad[v][e]);
-      }
+      axpy3<T>(ag[v], au[v], ad[v], r, x4[(size_t)t * NV + vi], dy4[(size_t)t * NV + vi]);
     }
   }
   float4 *og = (float4 *)(p.dWg + (size_t)n * p.D), *od = (float4 *)(p.dWd + (size_t)n * p.D);
@@ -374,10 +383,10 @@ __global__ void __launch_bounds__(512) bwd_dw_kernel(BParams p) {
     if (vi >= NV) continue;
 #pragma unroll
     for (int q = 0; q < EV / 4; ++q) {
-      og[vi * (EV / 4) + q] = make_float4(ag[v][4 * q], ag[v][4 * q + 1], ag[v][4 * q + 2], ag[v][4 * q + 3]);
-      od[vi * (EV / 4) + q] = make_float4(ad[v][4 * q], ad[v][4 * q + 1], ad[v][4 * q + 2], ad[v][4 * q + 3]);
+      og[vi * (EV / 4) + q] = make_float4(ag[v][2 * q].x, ag[v][2 * q].y, ag[v][2 * q + 1].x, ag[v][2 * q + 1].y);
+      od[vi * (EV / 4) + q] = make_float4(ad[v][2 * q].x, ad[v][2 * q].y, ad[v][2 * q + 1].x, ad[v][2 * q + 1].y);
       if (ou)
-        ou[vi * (EV / 4) + q] = make_float4(au[v][4 * q], au[v][4 * q + 1], au[v][4 * q + 2], au[v][4 * q + 3]);
+        ou[vi * (EV / 4) + q] = make_float4(au[v][2 * q].x, au[v][2 * q].y, au[v][2 * q + 1].x, au[v][2 * q + 1].y);
     }
   }
   if (tid == 0) p.dbg[n] = sb;
@@ -394,8 +403,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   p.ctl = a.ws.ctl; p.rows = a.ws.rows; p.pos = a.ws.pos;
   p.dz = a.ws.dz; p.du = a.ws.du; p.hs = a.ws.hs;
   p.dzr = a.ws.dzr; p.dur = a.ws.dur; p.hr = a.ws.hr;
-  p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_tok = a.ws.col_tok;
-  p.col_slot = a.ws.col_slot;
+  p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_e = a.ws.col_e;
   p.dx = a.dx; p.dWg = a.dWg; p.dbg = a.dbg; p.dWu = a.dWu; p.dWd = a.dWd;
   p.status = a.tw.status;
 

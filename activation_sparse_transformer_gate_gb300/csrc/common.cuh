@@ -36,12 +36,30 @@ __device__ __forceinline__ uint32_t store_bits(float v, bf16 *) {
   return (uint32_t)(*reinterpret_cast<uint16_t *>(&b));
 }
 
-// 16-byte read-only load that does not allocate in L1 (streamed weight rows).
+// L2 cache policy of gathered rows.  A read-only load that skips L1 otherwise
+// enters L2 with evict-first priority, and a gathered weight row is read again
+// by many other tokens: with evict-first the weight matrices miss L2 although
+// they fit in it.  L2_FIRST keeps that priority for rows read once.
+// (Pure asm: the compiler may hoist and share it.)
+enum L2Pol { L2_NORMAL = 0, L2_FIRST = 1 };
+
+template <int POL>
+__device__ __forceinline__ uint64_t gather_policy() {
+  uint64_t pol;
+  if (POL == L2_FIRST)
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte read-only load of a gathered row: no L1 allocation, L2 policy POL.
+template <int POL = L2_NORMAL>
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(gather_policy<POL>()));
   return r;
 }
 

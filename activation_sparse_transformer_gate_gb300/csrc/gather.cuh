@@ -36,13 +36,13 @@ template <> struct Vec<float> {
   }
 };
 
-// Gather PB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
+// Gather NB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
 // 16-byte vectors of each row, as 128-bit read-only loads that skip L1.
-template <class T, int VPT>
+template <class T, int VPT, int NB = PB>
 __device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb, int NV,
-                                        uint4 (&r)[PB][VPT]) {
+                                        uint4 (&r)[NB][VPT]) {
 #pragma unroll
-  for (int b = 0; b < PB; ++b) {
+  for (int b = 0; b < NB; ++b) {
     const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -52,113 +52,72 @@ __device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b
   }
 }
 
-// Dot product of the thread's slice of a row held in registers with one
-// gathered row (16-byte vectors).
-template <class T, int VPT>
-__device__ __forceinline__ float slice_dot(const float (&xr)[VPT][Vec<T>::EV],
-                                           const uint4 (&w)[VPT]) {
+// acc[0 .. EV/2) += h * (the EV values of a 16-byte vector), as packed fp32
+// pair FMAs (one instruction per two products).
+template <class T>
+__device__ __forceinline__ void axpy_vec(float2 *acc, float h, const uint4 &w) {
   constexpr int EV = Vec<T>::EV;
-  float s = 0.f;
+  float f[EV];
+  Vec<T>::unpack(w, f);
+  const float2 hh = make_float2(h, h);
 #pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    float f[EV];
-    Vec<T>::unpack(w[v], f);
-#pragma unroll
-    for (int e = 0; e < EV; ++e) s = fmaf(xr[v][e], f[e], s);
-  }
-  return s;
+  for (int q = 0; q < EV / 2; ++q) acc[q] = __ffma2_rn(hh, make_float2(f[2 * q], f[2 * q + 1]), acc[q]);
+}
+
+// c + a.lo * b.lo + a.hi * b.hi for bf16 pairs packed in 32-bit words: fused
+// multiply-adds with bf16 operands and an fp32 accumulator (the bf16 product
+// is exact in fp32, so each step equals fmaf on the widened operands).
+__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %0;}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
 }
 
 // ---- warp-level rows: lane l owns the 16-byte vectors l, l+32, ... of a row
 // (VPL = ceil(NV / 32) of them).  A warp reduces its own dot products with
 // shuffles, so pairs handled by different warps need no CTA barrier.
-template <int VPL>
+template <int VPL, int POL = L2_NORMAL>
 __device__ __forceinline__ void warp_row(const uint4 *row, int NV, bool valid, uint4 (&r)[VPL]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 0; k < VPL; ++k) {
     const int vi = lane + 32 * k;
-    r[k] = (valid && vi < NV) ? ldg_stream(row + vi) : make_uint4(0, 0, 0, 0);
-  }
-}
-
-// The lane's slice of a row kept in registers (cached loads: every warp of
-// the CTA reads the same row).
-template <int VPL>
-__device__ __forceinline__ void warp_row_cached(const uint4 *row, int NV, uint4 (&r)[VPL]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int k = 0; k < VPL; ++k) {
-    const int vi = lane + 32 * k;
-    r[k] = vi < NV ? row[vi] : make_uint4(0, 0, 0, 0);
+    r[k] = (valid && vi < NV) ? ldg_stream<POL>(row + vi) : make_uint4(0, 0, 0, 0);
   }
 }
 
 // Full dot product of two rows held as lane slices (warp-wide sum; every
-// lane gets the result).
+// lane gets the result).  Two accumulator chains per lane.
 template <class T, int VPL>
 __device__ __forceinline__ float warp_dot(const uint4 (&a)[VPL], const uint4 (&b)[VPL]) {
-  constexpr int EV = Vec<T>::EV;
-  float s = 0.f;
+  float s0 = 0.f, s1 = 0.f;
+  if constexpr (Vec<T>::EV == 8) {  // bf16: mixed-precision FMAs, no widening
 #pragma unroll
-  for (int k = 0; k < VPL; ++k) {
-    float fa[EV], fb[EV];
-    Vec<T>::unpack(a[k], fa);
-    Vec<T>::unpack(b[k], fb);
+    for (int k = 0; k < VPL; ++k) {
+      s0 = dot2_bf16(a[k].x, b[k].x, s0);
+      s1 = dot2_bf16(a[k].y, b[k].y, s1);
+      s0 = dot2_bf16(a[k].z, b[k].z, s0);
+      s1 = dot2_bf16(a[k].w, b[k].w, s1);
+    }
+  } else {
 #pragma unroll
-    for (int e = 0; e < EV; ++e) s = fmaf(fa[e], fb[e], s);
+    for (int k = 0; k < VPL; ++k) {
+      s0 = fmaf(__uint_as_float(a[k].x), __uint_as_float(b[k].x), s0);
+      s1 = fmaf(__uint_as_float(a[k].y), __uint_as_float(b[k].y), s1);
+      s0 = fmaf(__uint_as_float(a[k].z), __uint_as_float(b[k].z), s0);
+      s1 = fmaf(__uint_as_float(a[k].w), __uint_as_float(b[k].w), s1);
+    }
   }
+  float s = s0 + s1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
-}
-
-// Reduce 8 per-lane values across the warp with 9 shuffles (a transposing
-// reduction); afterwards lane L holds the warp total of value (L >> 2) & 7.
-__device__ __forceinline__ float warp_reduce8(float (&p)[PB]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool hi = lane & 16;
-    const float send = hi ? p[i] : p[i + 4];
-    const float keep = hi ? p[i + 4] : p[i];
-    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool hi = lane & 8;
-    const float send = hi ? p[i] : p[i + 2];
-    const float keep = hi ? p[i + 2] : p[i];
-    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  {
-    const bool hi = lane & 4;
-    const float send = hi ? p[0] : p[1];
-    const float keep = hi ? p[1] : p[0];
-    p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-  p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
-  p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
-  return p[0];
-}
-
-// Sum the PB per-thread partial values across the CTA.  Every thread gets
-// the PB totals in out[] (fixed reduction order: deterministic).
-// s_red must hold PB x 33 floats and s_tot PB floats; contains 2 barriers.
-__device__ __forceinline__ void block_reduce8(float (&pd)[PB], float (&out)[PB],
-                                              float (*s_red)[33], float *s_tot) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const float wsum = warp_reduce8(pd);
-  if ((lane & 3) == 0) s_red[lane >> 2][w] = wsum;
-  __syncthreads();
-  if (threadIdx.x < PB) {
-    float u = 0.f;
-    for (int q = 0; q < nw; ++q) u += s_red[threadIdx.x][q];
-    s_tot[threadIdx.x] = u;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int b = 0; b < PB; ++b) out[b] = s_tot[b];
 }
 
 // Where the active pairs of one (row, tile) come from.  Rows whose tiles all

@@ -27,8 +27,7 @@ struct Workspace {
   float *hs;          // [F/C][T][K] fp32: h at the slots
   int32_t *col_ptr;   // [F+1] neuron-major (transposed) pointers
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
-  int32_t *col_tok;   // [T*(F/C)*K] token of each transposed entry
-  int32_t *col_slot;  // [T*(F/C)*K] slot of each transposed entry
+  float4 *col_e;      // [T*(F/C)*K] transposed entries {token (int bits), dz, du, h}
   float *dzr;         // [T][F] fp32: dz rows of the overflow rows
   float *dur;         // [T][F] fp32: du rows of the overflow rows
   float *hr;          // [T][F] fp32: h rows of the overflow rows

@@ -45,7 +45,7 @@ struct UDParams {
 // u = x . W_up[n] of pairs w, w+8, ... (two rows in flight per warp, warp
 // shuffles only); one barrier; phase 2 -- every thread accumulates its slice
 // of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
-template <class T, int VPT, int VPL, int PIF>
+template <class T, int VPT, int VPL, int PIF, int PB2>
 __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -75,11 +75,11 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   }
   if (p.gated)  // x_t to shared memory (visible after the barriers of build_pairs)
     for (int v = tid; v < NV; v += blockDim.x) s_x[v] = ((const uint4 *)p.x)[(size_t)t * NV + v];
-  float yr[VPT][EV];
+  float2 yr[VPT][EV / 2];
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
 #pragma unroll
-    for (int e = 0; e < EV; ++e) yr[v][e] = 0.f;
+    for (int e = 0; e < EV / 2; ++e) yr[v][e] = make_float2(0.f, 0.f);
   const uint4 *Wu4 = (const uint4 *)p.Wu, *Wd4 = (const uint4 *)p.Wd;
   PairSource<T> src;
   src.idx = p.idx; src.nnz = p.nnz; src.val = (const T *)p.val; src.Tn = p.Tn; src.C = p.C;
@@ -128,21 +128,16 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
     }
     __syncthreads();
     // ---- phase 2: y += h * W_down[n], thread-owned slices -------------------
-    for (int b0 = 0; b0 < P; b0 += PB) {
-      const int nb = P - b0 < PB ? P - b0 : PB;
-      uint4 wd[PB][VPT];
-      gather8<T, VPT>(Wd4, s_n, b0, nb, NV, wd);
+    for (int b0 = 0; b0 < P; b0 += PB2) {
+      const int nb = P - b0 < PB2 ? P - b0 : PB2;
+      uint4 wd[PB2][VPT];
+      gather8<T, VPT, PB2>(Wd4, s_n, b0, nb, NV, wd);
 #pragma unroll
-      for (int b = 0; b < PB; ++b) {
+      for (int b = 0; b < PB2; ++b) {
         if (b >= nb) break;
         const float h = s_g[b0 + b];
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          float f[EV];
-          Vec<T>::unpack(wd[b][v], f);
-#pragma unroll
-          for (int e = 0; e < EV; ++e) yr[v][e] = fmaf(h, f[e], yr[v][e]);
-        }
+        for (int v = 0; v < VPT; ++v) axpy_vec<T>(yr[v], h, wd[b][v]);
       }
     }
     __syncthreads();  // the list is rewritten by the next group
@@ -152,7 +147,7 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
-    if (vi < NV) yrow[vi] = Vec<T>::pack(yr[v]);
+    if (vi < NV) yrow[vi] = Vec<T>::pack(reinterpret_cast<const float *>(yr[v]));
   }
 }
 
@@ -166,7 +161,7 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   const int NV = a.D / EV;  // <= 1024 (checked by the caller)
   const int vpl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 #define TW_UD(TT, L)                                                                           \
-  updown_fused_kernel<TT, (L + 7) / 8, L, (L <= 8 ? 2 : 1)><<<a.T, 256, 0, s>>>(p)
+  updown_fused_kernel<TT, (L + 7) / 8, L, (L <= 8 ? 2 : 1), 16><<<a.T, 256, 0, s>>>(p)
 #define TW_UD_T(TT)                                                                            \
   do {                                                                                         \
     switch (vpl) {                                                                             \
