@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
 // 2b. Per-token dx SpMM (dense x hybrid): dx_t = sum over active pairs of
 // dz W_gate[n] + du W_up[n].  No reductions, no barriers in the pair loop;
 // the working set is W_gate and W_up.
-template <class T, int VPT>
-__global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
+template <class T, int VPT, int NB>
+__global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -202,13 +202,13 @@ __global__ void __launch_bounds__(512) bwd_dx_kernel(BParams p) {
       s_u[i] = sl >= 0 ? p.du[sl] : p.dur[o];
     }
     __syncthreads();
-    for (int b0 = 0; b0 < P; b0 += PB) {
-      const int nb = P - b0 < PB ? P - b0 : PB;
-      uint4 wg[PB][VPT], wu[PB][VPT];
-      gather8<T, VPT>(Wg4, s_n, b0, nb, NV, wg);
-      if (p.gated) gather8<T, VPT>(Wu4, s_n, b0, nb, NV, wu);
+    for (int b0 = 0; b0 < P; b0 += NB) {
+      const int nb = P - b0 < NB ? P - b0 : NB;
+      uint4 wg[NB][VPT], wu[NB][VPT];
+      gather8<T, VPT, NB>(Wg4, s_n, b0, nb, NV, wg);
+      if (p.gated) gather8<T, VPT, NB>(Wu4, s_n, b0, nb, NV, wu);
 #pragma unroll
-      for (int b = 0; b < PB; ++b) {
+      for (int b = 0; b < NB; ++b) {
         if (b >= nb) break;
         const float z = s_z[b0 + b], u = s_u[b0 + b];
 #pragma unroll
@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(1024) twell_transpose_kernel(BParams p) {
 // round trip: its x and dy rows.
 constexpr int DW_LIST = 512;
 
-template <class T, int VPT>
-__global__ void __launch_bounds__(512, 1) bwd_dw_kernel(BParams p) {
+template <class T, int VPT, int NB>
+__global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ float4 s_e[DW_LIST];
   const int n = blockIdx.x, tid = threadIdx.x;
@@ -335,11 +335,11 @@ __global__ void __launch_bounds__(512, 1) bwd_dw_kernel(BParams p) {
     if (c0) __syncthreads();  // the previous chunk is consumed
     for (int i = tid; i < m; i += blockDim.x) s_e[i] = p.col_e[start + c0 + i];
     __syncthreads();
-    for (int e0 = 0; e0 < m; e0 += PB) {
-      const int nb = m - e0 < PB ? m - e0 : PB;
-      uint4 xv[PB][VPT], yv[PB][VPT];
+    for (int e0 = 0; e0 < m; e0 += NB) {
+      const int nb = m - e0 < NB ? m - e0 : NB;
+      uint4 xv[NB][VPT], yv[NB][VPT];
 #pragma unroll
-      for (int b = 0; b < PB; ++b) {
+      for (int b = 0; b < NB; ++b) {
         const int t = __float_as_int(s_e[e0 + (b < nb ? b : 0)].x);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(512, 1) bwd_dw_kernel(BParams p) {
         }
       }
 #pragma unroll
-      for (int b = 0; b < PB; ++b) {
+      for (int b = 0; b < NB; ++b) {
         if (b >= nb) break;
         const float4 r = s_e[e0 + b];
         sb += r.y;
@@ -418,7 +418,9 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // 2. per-token dh SDDMM (slots / overflow rows), then dx SpMM
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
-  const int vpt = NV <= 512 ? 1 : 2;
+  // token / neuron CTAs: each thread owns two 16-byte vectors of a row (half
+  // the per-row overhead of one), batches of 4 rows per matrix in flight
+  const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 #define TW_DH(TT, L) bwd_dh_kernel<TT, L, (L <= 8 ? 2 : 1)><<<a.T, 256, 0, s>>>(p)
@@ -440,13 +442,14 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_SLOTS, s);
-  if (bf) {
-    if (vpt == 1) bwd_dx_kernel<bf16, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_dx_kernel<bf16, 2><<<a.T, threads, 0, s>>>(p);
-  } else {
-    if (vpt == 1) bwd_dx_kernel<float, 1><<<a.T, threads, 0, s>>>(p);
-    else bwd_dx_kernel<float, 2><<<a.T, threads, 0, s>>>(p);
-  }
+#define TW_VPT(K, TT, G)                                                                       \
+  do {                                                                                         \
+    if (vpt == 1) K<TT, 1, 8><<<G, threads, 0, s>>>(p);                                        \
+    else if (vpt == 2) K<TT, 2, 4><<<G, threads, 0, s>>>(p);                                   \
+    else K<TT, 4, 2><<<G, threads, 0, s>>>(p);                                                 \
+  } while (0)
+  if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T);
+  else TW_VPT(bwd_dx_kernel, float, a.T);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_DX, s);
@@ -459,13 +462,9 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_TRANSPOSE, s);
   // 4. weight gradients
-  if (bf) {
-    if (vpt == 1) bwd_dw_kernel<bf16, 1><<<a.F, threads, 0, s>>>(p);
-    else bwd_dw_kernel<bf16, 2><<<a.F, threads, 0, s>>>(p);
-  } else {
-    if (vpt == 1) bwd_dw_kernel<float, 1><<<a.F, threads, 0, s>>>(p);
-    else bwd_dw_kernel<float, 2><<<a.F, threads, 0, s>>>(p);
-  }
+  if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F);
+  else TW_VPT(bwd_dw_kernel, float, a.F);
+#undef TW_VPT
   e = cudaGetLastError();
   prof_mark(KID_BWD_DW, s);
   return e;

@@ -37,13 +37,14 @@ template <> struct Vec<float> {
 };
 
 // Gather NB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
-// 16-byte vectors of each row, as 128-bit read-only loads that skip L1.
+// 16-byte vectors of each row, as 128-bit read-only loads that skip L1.  Rows
+// b >= nb (nb may be 0) are zero and read nothing.
 template <class T, int VPT, int NB = PB>
 __device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb, int NV,
                                         uint4 (&r)[NB][VPT]) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
-    const size_t rb = (size_t)s_n[b0 + (b < nb ? b : 0)] * NV;
+    const size_t rb = (size_t)s_n[b < nb ? b0 + b : 0] * NV;  // b0 may lie past the list
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int vi = threadIdx.x + v * blockDim.x;

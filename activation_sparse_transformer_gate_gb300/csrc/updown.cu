@@ -6,16 +6,18 @@
 // keeping global-memory traffic low and working from registers and shared
 // memory.
 //
-// Design (GB300): one CTA of 8 warps per token.  The active pairs (neuron n,
+// Design (GB300): one CTA of 4 warps per token.  The active pairs (neuron n,
 // gate g) come from the token's TwELL slots, compacted into a shared-memory
 // list.  Phase 1: each warp computes whole dot products u = x . W_up[n] for
 // its share of the pairs (lane l owns the 16-byte vectors l, l+32, ... of the
 // row; two rows in flight per warp; warp shuffles only), so no barrier sits
-// inside the pair loop.  Phase 2: each thread owns a d_model slice of y and
-// accumulates h * W_down[n] over all pairs with 128-bit coalesced row loads,
-// 8 rows in flight.  One barrier per tile group separates the phases.  All-dense mode (and overflow rows
-// when there are many) is left to the tensor-core dense-row GEMMs; a few
-// overflow rows are handled here from the wide-tile buffer.
+// inside the pair loop.  Phase 2: each thread owns a d_model slice of y (two
+// 16-byte vectors at d_model 2048, which halves the per-row address and loop
+// work of one) and accumulates h * W_down[n] over all pairs with 128-bit
+// coalesced row loads, 8 rows in flight.  One barrier per tile group separates
+// the phases.  All-dense mode (and overflow rows when there are many) is left
+// to the tensor-core dense-row GEMMs; a few overflow rows are handled here
+// from the wide-tile buffer.
 #include "common.cuh"
 #include "gather.cuh"
 #include "kernels.h"
@@ -37,12 +39,12 @@ struct UDParams {
 
 }  // namespace
 
-// One CTA (8 warps) per token.  Rows that run on the dense GEMM path
+// One CTA (4 warps) per token.  Rows that run on the dense GEMM path
 // (all-dense mode, or overflow rows when there are many) are skipped; an
 // overflow row handled here takes its overflowing tiles from the wide-tile
 // buffer and also writes its dense backup row (g_fb, and u_fb when training).
 // Per tile group: phase 1 -- warp w computes the full dot products
-// u = x . W_up[n] of pairs w, w+8, ... (two rows in flight per warp, warp
+// u = x . W_up[n] of pairs w, w+4, ... (two rows in flight per warp, warp
 // shuffles only); one barrier; phase 2 -- every thread accumulates its slice
 // of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
 template <class T, int VPT, int VPL, int PIF, int PB2>
@@ -161,7 +163,7 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   const int NV = a.D / EV;  // <= 1024 (checked by the caller)
   const int vpl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 #define TW_UD(TT, L)                                                                           \
-  updown_fused_kernel<TT, (L + 7) / 8, L, (L <= 8 ? 2 : 1), 16><<<a.T, 256, 0, s>>>(p)
+  updown_fused_kernel<TT, (L + 3) / 4, L, (L <= 8 ? 2 : 1), 16 / ((L + 3) / 4)><<<a.T, 128, 0, s>>>(p)
 #define TW_UD_T(TT)                                                                            \
   do {                                                                                         \
     switch (vpl) {                                                                             \
