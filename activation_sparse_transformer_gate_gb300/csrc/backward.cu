@@ -16,8 +16,9 @@
 //      SpMM).  Pairs come from the TwELL slots, or from the dense backup row
 //      of an overflow row.  Two passes keep each pass's working set (one or
 //      two weight matrices) small enough to stay in L2.
-//   3. one CTA per tile: deterministic transpose of the slots into
-//      neuron-major lists ordered by token (sparse transpose)
+//   3. a CTA per (tile, chunk of 1024 tokens), two passes: deterministic
+//      transpose of the slots into neuron-major lists ordered by token
+//      (sparse transpose)
 //   4. one CTA per neuron: dWg, dWu, dWd rows and dbg from gathered x / dy rows
 //      of its list, then the overflow rows' contributions (dense x hybrid)
 #include "common.cuh"
@@ -38,7 +39,7 @@ struct BParams {
   const int32_t *rows, *pos;
   float *dz, *du, *hs;       // slot arrays [F/C][T][K]
   float *dzr, *dur, *hr;     // overflow rows [n_ovf][F]
-  int32_t *col_start, *col_cnt;
+  int32_t *col_start, *col_cnt, *col_chunk;
   float4 *col_e;             // transposed entries {token bits, dz, du, h}
   void *dx;
   float *dWg, *dbg, *dWu, *dWd;
@@ -235,76 +236,113 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// 3. Sparse transpose of one tile's slots into neuron-major lists.  The list of
-// neuron j*C + c occupies col_e[col_start .. + col_cnt) inside the tile's
-// region [j*T*K, (j+1)*T*K), ordered by token; each entry carries the token
-// and the pair's dz, du, h, so the weight-gradient pass reads one 16-byte
-// record per entry.  Tokens are visited 1024
-// at a time, and a token's rank among the tokens of its chunk that use column c
-// comes from per-warp lane masks (popc below the lane) plus per-warp offsets.
-// Overflow rows are not listed (their pairs live in the overflow-row arrays).
+// 3. Sparse transpose of the slots into neuron-major lists.  The list of
+// neuron j*C + c occupies col_e[col_start .. + col_cnt) inside tile j's region
+// [j*T*K, (j+1)*T*K), ordered by token; each entry carries the token and the
+// pair's dz, du, h, so the weight-gradient pass reads one 16-byte record per
+// entry.  Overflow rows are not listed (their pairs live in the overflow-row
+// arrays).  Two passes over a (tile, chunk of 1024 tokens) grid:
+//   3a. count the entries of every column in the chunk;
+//   3b. the chunk's first entry per column = the column's start in the tile
+//       (prefix over columns of the totals) + the counts of earlier chunks;
+//       a token's rank among the chunk's tokens that use column c comes from
+//       per-warp lane masks (popc below the lane) plus per-warp offsets.
+constexpr int TR_CHUNK = 1024;
+
 template <int C>
-__global__ void __launch_bounds__(1024) twell_transpose_kernel(BParams p) {
-  __shared__ uint32_t occ[32][C];
-  __shared__ int woff[32][C];
-  __shared__ int cnt[C], run[C];
-  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+__global__ void __launch_bounds__(TR_CHUNK) twell_count_kernel(BParams p) {
+  __shared__ int cnt[C];
+  const int j = blockIdx.x, ch = blockIdx.y, tid = threadIdx.x;
   const int K = p.K, Tn = p.Tn;
-  const size_t region = (size_t)j * Tn * K;
   for (int c = tid; c < C; c += blockDim.x) cnt[c] = 0;
   __syncthreads();
-  for (int base = 0; base < Tn; base += blockDim.x) {
-    const int t = base + tid;
-    if (t < Tn && p.pos[t] < 0) {
-      const int n = p.nnz[(size_t)j * Tn + t];
-      const size_t s0 = ((size_t)j * Tn + t) * K;
-      for (int k = 0; k < n && k < K; ++k) {
-        const int c = p.idx[s0 + k];
-        if (c < C) atomicAdd(&cnt[c], 1);
-      }
+  const int t = ch * TR_CHUNK + tid;
+  if (t < Tn && p.pos[t] < 0) {
+    const int n = p.nnz[(size_t)j * Tn + t];
+    const size_t s0 = ((size_t)j * Tn + t) * K;
+    for (int k = 0; k < n && k < K; ++k) {
+      const int c = p.idx[s0 + k];
+      if (c < C) atomicAdd(&cnt[c], 1);
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int r = 0;
-    for (int c = 0; c < C; ++c) {
-      run[c] = r;
-      p.col_start[j * C + c] = (int)(region + r);
-      p.col_cnt[j * C + c] = cnt[c];
-      r += cnt[c];
+  for (int c = tid; c < C; c += blockDim.x)
+    p.col_chunk[((size_t)j * gridDim.y + ch) * C + c] = cnt[c];
+}
+
+template <int C>
+__global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
+  __shared__ uint32_t occ[32][C];
+  __shared__ int woff[32][C];
+  __shared__ int run[C], tot[C];
+  __shared__ int wsum[32];
+  const int j = blockIdx.x, ch = blockIdx.y, nch = gridDim.y;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int K = p.K, Tn = p.Tn;
+  const size_t region = (size_t)j * Tn * K;
+  const int32_t *cc = p.col_chunk + (size_t)j * nch * C;
+  // per column: entries of earlier chunks and of all chunks
+  for (int c = tid; c < C; c += blockDim.x) {
+    int before = 0, all = 0;
+    for (int q = 0; q < nch; ++q) {
+      const int v = cc[(size_t)q * C + c];
+      all += v;
+      if (q < ch) before += v;
     }
+    run[c] = before;
+    tot[c] = all;
+  }
+  for (int i = tid; i < 32 * C; i += blockDim.x) (&occ[0][0])[i] = 0u;
+  __syncthreads();
+  // exclusive prefix of the column totals (C <= 128: four warps of 32)
+  if (tid < C) {
+    const int v = tot[tid];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[w] = incl;
+    tot[tid] = incl - v;  // exclusive within the warp for now
   }
   __syncthreads();
+  if (tid < C) {
+    int off = 0;
+    for (int q = 0; q < w; ++q) off += wsum[q];
+    const int start = tot[tid] + off;
+    run[tid] += start;
+    if (ch == 0) {
+      p.col_start[j * C + tid] = (int)(region + start);
+      int all = 0;
+      for (int q = 0; q < nch; ++q) all += cc[(size_t)q * C + tid];
+      p.col_cnt[j * C + tid] = all;
+    }
+  }
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = 0; base < Tn; base += blockDim.x) {
-    for (int i = tid; i < 32 * C; i += blockDim.x) (&occ[0][0])[i] = 0u;
-    __syncthreads();
-    const int t = base + tid;
-    const bool act = t < Tn && p.pos[t] < 0;
-    const int n = act ? (int)p.nnz[(size_t)j * Tn + t] : 0;
-    const size_t s0 = ((size_t)j * Tn + (act ? t : 0)) * K;
-    for (int k = 0; k < n && k < K; ++k) {
-      const int c = p.idx[s0 + k];
-      if (c < C) atomicOr(&occ[w][c], 1u << lane);
+  const int t = ch * TR_CHUNK + tid;
+  const bool act = t < Tn && p.pos[t] < 0;
+  const int n = act ? (int)p.nnz[(size_t)j * Tn + t] : 0;
+  const size_t s0 = ((size_t)j * Tn + (act ? t : 0)) * K;
+  for (int k = 0; k < n && k < K; ++k) {
+    const int c = p.idx[s0 + k];
+    if (c < C) atomicOr(&occ[w][c], 1u << lane);
+  }
+  __syncthreads();
+  for (int c = tid; c < C; c += blockDim.x) {
+    int r = run[c];
+    for (int q = 0; q < 32; ++q) {
+      woff[q][c] = r;
+      r += __popc(occ[q][c]);
     }
-    __syncthreads();
-    for (int c = tid; c < C; c += blockDim.x) {
-      int r = run[c];
-      for (int q = 0; q < 32; ++q) {
-        woff[q][c] = r;
-        r += __popc(occ[q][c]);
-      }
-      run[c] = r;
-    }
-    __syncthreads();
-    for (int k = 0; k < n && k < K; ++k) {
-      const int c = p.idx[s0 + k];
-      if (c >= C) continue;
-      const int e = woff[w][c] + __popc(occ[w][c] & lt);
-      const size_t sl = s0 + k;
-      p.col_e[region + e] = make_float4(__int_as_float(t), p.dz[sl], p.du[sl], p.hs[sl]);
-    }
-    __syncthreads();
+  }
+  __syncthreads();
+  for (int k = 0; k < n && k < K; ++k) {
+    const int c = p.idx[s0 + k];
+    if (c >= C) continue;
+    const int e = woff[w][c] + __popc(occ[w][c] & lt);
+    const size_t sl = s0 + k;
+    p.col_e[region + e] = make_float4(__int_as_float(t), p.dz[sl], p.du[sl], p.hs[sl]);
   }
 }
 
@@ -403,7 +441,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   p.ctl = a.ws.ctl; p.rows = a.ws.rows; p.pos = a.ws.pos;
   p.dz = a.ws.dz; p.du = a.ws.du; p.hs = a.ws.hs;
   p.dzr = a.ws.dzr; p.dur = a.ws.dur; p.hr = a.ws.hr;
-  p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_e = a.ws.col_e;
+  p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_e = a.ws.col_e; p.col_chunk = a.ws.col_chunk;
   p.dx = a.dx; p.dWg = a.dWg; p.dbg = a.dbg; p.dWu = a.dWu; p.dWd = a.dWd;
   p.status = a.tw.status;
 
@@ -455,9 +493,17 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   prof_mark(KID_BWD_DX, s);
   // 3. transpose
   const int nt = a.F / a.C;
-  if (a.C == 32) twell_transpose_kernel<32><<<nt, 1024, 0, s>>>(p);
-  else if (a.C == 64) twell_transpose_kernel<64><<<nt, 1024, 0, s>>>(p);
-  else twell_transpose_kernel<128><<<nt, 1024, 0, s>>>(p);
+  const dim3 tgrid(nt, (a.T + TR_CHUNK - 1) / TR_CHUNK);
+  if (a.C == 32) {
+    twell_count_kernel<32><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    twell_transpose_kernel<32><<<tgrid, TR_CHUNK, 0, s>>>(p);
+  } else if (a.C == 64) {
+    twell_count_kernel<64><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    twell_transpose_kernel<64><<<tgrid, TR_CHUNK, 0, s>>>(p);
+  } else {
+    twell_count_kernel<128><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    twell_transpose_kernel<128><<<tgrid, TR_CHUNK, 0, s>>>(p);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_TRANSPOSE, s);

@@ -28,6 +28,7 @@ struct Workspace {
   int32_t *col_ptr;   // [F+1] neuron-major (transposed) pointers
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
   float4 *col_e;      // [T*(F/C)*K] transposed entries {token (int bits), dz, du, h}
+  int32_t *col_chunk; // [(F/C) * ceil(T/1024) * C] per-(tile, token chunk) column counts
   float *dzr;         // [T][F] fp32: dz rows of the overflow rows
   float *dur;         // [T][F] fp32: du rows of the overflow rows
   float *hr;          // [T][F] fp32: h rows of the overflow rows

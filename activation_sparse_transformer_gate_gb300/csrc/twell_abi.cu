@@ -87,6 +87,7 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.col_ptr = (int32_t *)take(4 * ((size_t)F + 1));
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_e = (float4 *)take(16 * slots);
+    w.col_chunk = (int32_t *)take(4 * (size_t)F * (((size_t)T + 1023) / 1024));
     w.dzr = (float *)take(4 * (size_t)T * F);
     w.dur = (float *)take(4 * (size_t)T * F);
     w.hr = (float *)take(4 * (size_t)T * F);

@@ -120,6 +120,17 @@ def test_many_overflow_rows_dense_gemm_path():
     check_backward(a, w, g, 1e-3)
 
 
+def test_transpose_several_token_chunks_ragged():
+    """T = 2500: the sparse transpose runs over three chunks of 1024 tokens, the
+    last one partial, so every list spans chunk boundaries."""
+    w = synth.Workload("bchunk", 2500, 256, 512, 128, 8, "bf16", True, -1.2, 27, hot_tokens=2,
+                       seq_len=500, hot_bias=1.5, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3)
+    assert g["code"] == 0 and g["n_ovf"] >= 1
+    check_backward(a, w, g, 1e-3)
+
+
 @pytest.mark.parametrize("C,K", [(32, 2), (64, 16), (128, 32)])
 def test_tile_shapes(C, K):
     w = synth.Workload(f"bt{C}{K}", 96, 128, 512, C, K, "bf16", True, -1.9, 25 + K, train=True)
