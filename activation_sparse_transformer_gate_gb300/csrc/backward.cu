@@ -88,8 +88,10 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
 // every active pair, then dz, du, h of the pair -- at its TwELL slot for a
 // non-overflow row, in the overflow-row arrays for an overflow row.  Only
 // W_down rows are gathered, so the working set is W_down and dy.  Each warp
-// computes whole dot products for its share of the pairs (two rows in
-// flight, warp shuffles only): no barrier inside the pair loop.
+// computes whole dot products for its share of the pairs (PIF rows in flight,
+// warp shuffles only): no barrier inside the pair loop.  One row per warp
+// keeps the registers low enough for three CTAs per SM, which hides more
+// latency than a second row per warp.
 template <class T, int VL, int PIF>
 __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
@@ -461,7 +463,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
-#define TW_DH(TT, L) bwd_dh_kernel<TT, L, (L <= 8 ? 2 : 1)><<<a.T, 256, 0, s>>>(p)
+#define TW_DH(TT, L) bwd_dh_kernel<TT, L, 1><<<a.T, 256, 0, s>>>(p)
 #define TW_DH_T(TT)                                                                            \
   do {                                                                                         \
     switch (vl) {                                                                              \
