@@ -459,7 +459,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
   // token / neuron CTAs: each thread owns two 16-byte vectors of a row (half
-  // the per-row overhead of one), batches of 4 rows per matrix in flight
+  // the per-row overhead of one), batches of 3 rows per matrix in flight
   const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
@@ -485,7 +485,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
 #define TW_VPT(K, TT, G)                                                                       \
   do {                                                                                         \
     if (vpt == 1) K<TT, 1, 8><<<G, threads, 0, s>>>(p);                                        \
-    else if (vpt == 2) K<TT, 2, 4><<<G, threads, 0, s>>>(p);                                   \
+    else if (vpt == 2) K<TT, 2, 3><<<G, threads, 0, s>>>(p);                                   \
     else K<TT, 4, 2><<<G, threads, 0, s>>>(p);                                                 \
   } while (0)
   if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T);

@@ -59,6 +59,9 @@ struct BwdArgs {
 };
 
 // pack.cu
+// Streaming multiprocessors of the current device (queried once).
+int num_sms();
+
 cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // Hybrid split.  With a workspace: reads the overflow-row bitmap (which must
 // hold the flags of this call), writes the row list / positions / control

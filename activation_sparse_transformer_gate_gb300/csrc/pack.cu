@@ -232,8 +232,8 @@ cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaSt
   cudaError_t e = cudaMemsetAsync(ws.ovf_bits, 0, 4 * (((size_t)tw.T + 31) / 32), s);
   if (e != cudaSuccess) return e;
   const long total = (long)tw.T * (tw.F / tw.C);
-  long blocks = (total + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
+  long blocks = (total + 255) / 256;  // usually idle (all-dense mode only)
+  if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
   flags_from_nnz_kernel<<<(unsigned)blocks, 256, 0, s>>>(tw.nnz, total, tw.T, tw.K, ws.ovf_bits);
   return cudaGetLastError();
 }
@@ -278,7 +278,8 @@ __global__ void gather_rows_kernel(const uint4 *__restrict__ src, uint4 *__restr
 cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
                                int dtype, cudaStream_t s) {
   const int es = dtype == TWELL_BF16 ? 2 : 4;
-  int blocks = T < 1216 ? T : 1216;
+  // Usually idle (no overflow-row GEMM): a small grid that loops over the rows.
+  int blocks = T < 2 * num_sms() ? T : 2 * num_sms();
   gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, D * es / 16, ws.ctl,
                                             ws.rows);
   return cudaGetLastError();
@@ -355,8 +356,8 @@ __global__ void fill_u_slots_kernel(const Ctl *__restrict__ ctl, const int32_t *
 
 cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s) {
   const long total = (long)a.T * (a.F / a.C);
-  long blocks = (total + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
+  long blocks = (total + 255) / 256;  // usually idle (all-dense mode only)
+  if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
   if (a.dtype == TWELL_BF16)
     fill_u_slots_kernel<bf16><<<(unsigned)blocks, 256, 0, s>>>(
         a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const bf16 *)a.ws.urows, (bf16 *)a.tw.u_val,
