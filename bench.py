@@ -306,8 +306,9 @@ def kernel_rooflines(kern, w, nnz, train):
         "bwd_slots_sddmm": ("hbm", pairs_all * (D * 2 + 14) + T * D * 2),
         # dx SpMM: per pair W_gate + W_up rows and dz/du in; per token the dx row out
         "bwd_dx_spmm": ("hbm", pairs_all * (2 * D * 2 + 8) + T * D * 2),
-        # per pair: x + dy rows and the pair's dz/du/h + list entry; 3 fp32 dW rows out
-        "bwd_dw_gather": ("hbm", pairs_all * (2 * D * 2 + 20) + 3 * F * D * 4 + F * 4),
+        # per pair: x + dy rows and its 16-byte list record {token, dz, du, h};
+        # 3 fp32 dW rows and dbg out
+        "bwd_dw_gather": ("hbm", pairs_all * (2 * D * 2 + 16) + 3 * F * D * 4 + F * 4),
         "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
     }
     out = {}
@@ -317,8 +318,8 @@ def kernel_rooflines(kern, w, nnz, train):
         sec = kern[k]["avg_ms"] / 1e3
         if bound == "hbm":
             ach, peak, unit = work / sec / 1e9, peaks["hbm_gbs"], "GB/s"
-        else:
-            ach, peak, unit = work / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        else:  # timed inside back-to-back steps: the sustained (power-capped) peak
+            ach, peak, unit = work / sec / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
         out[k] = dict(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak,
                       algorithmic=work, peak_source=peaks["source"])
     out.setdefault("_counts", {"bound": "-", "pairs_twell_rows": pairs, "pairs_all": pairs_all,
