@@ -52,7 +52,9 @@
  *     multiples of 16 bytes.
  *   - Supported: dtype F32 (CUDA-core FFMA, no TF32) and BF16 (tensor cores,
  *     fp32 accumulation); C in {32, 64, 128}; F % C == 0;
- *     K in {1, 2, 4, 8, 16, 32}, K <= C; 1 <= T; 8 <= D <= 16384.
+ *     K in {1, 2, 4, 8, 16, 32}, K <= C; 1 <= T; 8 <= D with
+ *     D*elem_size <= 16384 bytes (d_model <= 8192 in bf16, <= 4096 in fp32);
+ *     T*(F/C)*K < 2^31.  Other shapes return TWELL_ERR_ARG.
  *   - Thread safety: calls on distinct twell_t / workspaces may run
  *     concurrently on different streams.
  */
