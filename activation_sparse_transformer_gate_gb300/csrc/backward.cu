@@ -92,7 +92,7 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
 // warp shuffles only): no barrier inside the pair loop.  One row per warp
 // keeps the registers low enough for three CTAs per SM, which hides more
 // latency than a second row per warp.
-template <class T, int VL, int PIF>
+template <class T, int VL, int PIF, bool EXACT>
 __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
 #pragma unroll
       for (int q = 0; q < PIF; ++q) {
         const int i = i0 + q * nw;
-        warp_row<VL>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
+        // exact rows: load the (valid, clamped) row unconditionally, discard its dot
+        warp_row<VL, L2_NORMAL, EXACT>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, EXACT || i < P, wr[q]);
       }
       uint4 dw[VL];
 #pragma unroll
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
 // 2b. Per-token dx SpMM (dense x hybrid): dx_t = sum over active pairs of
 // dz W_gate[n] + du W_up[n].  No reductions, no barriers in the pair loop;
 // the working set is W_gate and W_up.
-template <class T, int VPT, int NB>
+template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -208,8 +209,13 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
     for (int b0 = 0; b0 < P; b0 += NB) {
       const int nb = P - b0 < NB ? P - b0 : NB;
       uint4 wg[NB][VPT], wu[NB][VPT];
-      gather8<T, VPT, NB>(Wg4, s_n, b0, nb, NV, wg);
-      if (p.gated) gather8<T, VPT, NB>(Wu4, s_n, b0, nb, NV, wu);
+      if (NTH > 0 && nb == NB) {
+        gather8<T, VPT, NB, NTH>(Wg4, s_n, b0, nb, NV, wg);
+        if (p.gated) gather8<T, VPT, NB, NTH>(Wu4, s_n, b0, nb, NV, wu);
+      } else {
+        gather8<T, VPT, NB>(Wg4, s_n, b0, nb, NV, wg);
+        if (p.gated) gather8<T, VPT, NB>(Wu4, s_n, b0, nb, NV, wu);
+      }
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         if (b >= nb) break;
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
 // round trip: its x and dy rows.
 constexpr int DW_LIST = 512;
 
-template <class T, int VPT, int NB>
+template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ float4 s_e[DW_LIST];
@@ -381,12 +387,21 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const int t = __float_as_int(s_e[e0 + (b < nb ? b : 0)].x);
+        const uint4 *xr = x4 + (size_t)t * NV + tid, *yr = dy4 + (size_t)t * NV + tid;
+        if (NTH > 0 && nb == NB) {  // full batch of exact rows: constant offsets
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          const int vi = tid + v * blockDim.x;
-          const bool ok = b < nb && vi < NV;
-          xv[b][v] = ok ? ldg_stream(x4 + (size_t)t * NV + vi) : make_uint4(0, 0, 0, 0);
-          yv[b][v] = ok ? ldg_stream(dy4 + (size_t)t * NV + vi) : make_uint4(0, 0, 0, 0);
+          for (int v = 0; v < VPT; ++v) {
+            xv[b][v] = ldg_stream(xr + v * NTH);
+            yv[b][v] = ldg_stream(yr + v * NTH);
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < VPT; ++v) {
+            const int vi = tid + v * blockDim.x;
+            const bool ok = b < nb && vi < NV;
+            xv[b][v] = ok ? ldg_stream(xr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+            yv[b][v] = ok ? ldg_stream(yr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+          }
         }
       }
 #pragma unroll
@@ -463,7 +478,11 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
-#define TW_DH(TT, L) bwd_dh_kernel<TT, L, 1><<<a.T, 256, 0, s>>>(p)
+#define TW_DH(TT, L)                                                                           \
+  do {                                                                                         \
+    if (NV == 32 * (L)) bwd_dh_kernel<TT, L, 1, true><<<a.T, 256, 0, s>>>(p);                  \
+    else bwd_dh_kernel<TT, L, 1, false><<<a.T, 256, 0, s>>>(p);                                \
+  } while (0)
 #define TW_DH_T(TT)                                                                            \
   do {                                                                                         \
     switch (vl) {                                                                              \
@@ -484,9 +503,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   prof_mark(KID_BWD_SLOTS, s);
 #define TW_VPT(K, TT, G)                                                                       \
   do {                                                                                         \
-    if (vpt == 1) K<TT, 1, 8><<<G, threads, 0, s>>>(p);                                        \
-    else if (vpt == 2) K<TT, 2, 3><<<G, threads, 0, s>>>(p);                                   \
-    else K<TT, 4, 2><<<G, threads, 0, s>>>(p);                                                 \
+    if (vpt == 1) K<TT, 1, 8, 0><<<G, threads, 0, s>>>(p);                                     \
+    else if (vpt == 2 && NV == 256) K<TT, 2, 3, 128><<<G, 128, 0, s>>>(p);                     \
+    else if (vpt == 2) K<TT, 2, 3, 0><<<G, threads, 0, s>>>(p);                                \
+    else K<TT, 4, 2, 0><<<G, threads, 0, s>>>(p);                                              \
   } while (0)
   if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T);
   else TW_VPT(bwd_dx_kernel, float, a.T);

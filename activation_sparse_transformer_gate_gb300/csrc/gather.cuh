@@ -37,18 +37,26 @@ template <> struct Vec<float> {
 };
 
 // Gather NB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
-// 16-byte vectors of each row, as 128-bit read-only loads that skip L1.  Rows
-// b >= nb (nb may be 0) are zero and read nothing.
-template <class T, int VPT, int NB = PB>
+// 16-byte vectors of each row, as 128-bit read-only loads that skip L1.
+// NTH == 0: any block size; vectors past the row end and rows b >= nb (nb may
+// be 0) are zero.  NTH > 0: a full batch (nb == NB) of exact rows, VPT * NTH
+// vectors each, in a block of NTH threads: constant offsets, no predicates.
+template <class T, int VPT, int NB = PB, int NTH = 0>
 __device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb, int NV,
                                         uint4 (&r)[NB][VPT]) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
-    const size_t rb = (size_t)s_n[b < nb ? b0 + b : 0] * NV;  // b0 may lie past the list
+    if (NTH > 0) {
+      const uint4 *row = base + (size_t)s_n[b0 + b] * NV + threadIdx.x;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int vi = threadIdx.x + v * blockDim.x;
-      r[b][v] = (b < nb && vi < NV) ? ldg_stream(base + rb + vi) : make_uint4(0, 0, 0, 0);
+      for (int v = 0; v < VPT; ++v) r[b][v] = ldg_stream(row + v * NTH);
+    } else {
+      const uint4 *row = base + (size_t)s_n[b < nb ? b0 + b : 0] * NV + threadIdx.x;  // b0 may lie past the list
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int vi = threadIdx.x + v * blockDim.x;
+        r[b][v] = (b < nb && vi < NV) ? ldg_stream(row + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+      }
     }
   }
 }
@@ -83,9 +91,18 @@ __device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
 // ---- warp-level rows: lane l owns the 16-byte vectors l, l+32, ... of a row
 // (VPL = ceil(NV / 32) of them).  A warp reduces its own dot products with
 // shuffles, so pairs handled by different warps need no CTA barrier.
-template <int VPL, int POL = L2_NORMAL>
+// EXACT: the row is exactly 32 * VPL vectors (constant offsets, no vector
+// predicates); an invalid row is then left unloaded (its result is discarded).
+template <int VPL, int POL = L2_NORMAL, bool EXACT = false>
 __device__ __forceinline__ void warp_row(const uint4 *row, int NV, bool valid, uint4 (&r)[VPL]) {
   const int lane = threadIdx.x & 31;
+  if (EXACT) {
+    if (valid) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) r[k] = ldg_stream<POL>(row + lane + 32 * k);
+    }
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < VPL; ++k) {
     const int vi = lane + 32 * k;

@@ -26,6 +26,8 @@ namespace twell {
 
 namespace {
 
+constexpr int UD_THREADS = 128;  // 4 warps per token CTA
+
 struct UDParams {
   const void *x, *Wu, *Wd;
   const uint8_t *idx, *nnz;
@@ -47,7 +49,7 @@ struct UDParams {
 // u = x . W_up[n] of pairs w, w+4, ... (two rows in flight per warp, warp
 // shuffles only); one barrier; phase 2 -- every thread accumulates its slice
 // of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
-template <class T, int VPT, int VPL, int PIF, int PB2>
+template <class T, int VPT, int VPL, int PIF, int PB2, bool EXACT>
 __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -105,13 +107,14 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
 #pragma unroll
         for (int q = 0; q < PIF; ++q) {
           const int i = i0 + q * nw;
-          warp_row<VPL>(Wu4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
+          // exact rows: load the (valid, clamped) row unconditionally, discard its dot
+          warp_row<VPL, L2_NORMAL, EXACT>(Wu4 + (size_t)s_n[i < P ? i : i0] * NV, NV, EXACT || i < P, wr[q]);
         }
         uint4 xw[VPL];
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
           const int vi = lane + 32 * k;
-          xw[k] = vi < NV ? s_x[vi] : make_uint4(0, 0, 0, 0);
+          xw[k] = (EXACT || vi < NV) ? s_x[vi] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int q = 0; q < PIF; ++q) {
@@ -133,7 +136,8 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
     for (int b0 = 0; b0 < P; b0 += PB2) {
       const int nb = P - b0 < PB2 ? P - b0 : PB2;
       uint4 wd[PB2][VPT];
-      gather8<T, VPT, PB2>(Wd4, s_n, b0, nb, NV, wd);
+      if (EXACT && nb == PB2) gather8<T, VPT, PB2, UD_THREADS>(Wd4, s_n, b0, nb, NV, wd);
+      else gather8<T, VPT, PB2>(Wd4, s_n, b0, nb, NV, wd);
 #pragma unroll
       for (int b = 0; b < PB2; ++b) {
         if (b >= nb) break;
@@ -163,7 +167,15 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   const int NV = a.D / EV;  // <= 1024 (checked by the caller)
   const int vpl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 #define TW_UD(TT, L)                                                                           \
-  updown_fused_kernel<TT, (L + 3) / 4, L, (L <= 8 ? 2 : 1), 16 / ((L + 3) / 4)><<<a.T, 128, 0, s>>>(p)
+  do {                                                                                         \
+    constexpr int VPT_ = (L + 3) / 4;                                                          \
+    if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                             \
+      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, true>                      \
+          <<<a.T, UD_THREADS, 0, s>>>(p);                                                      \
+    else                                                                                       \
+      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>                     \
+          <<<a.T, UD_THREADS, 0, s>>>(p);                                                      \
+  } while (0)
 #define TW_UD_T(TT)                                                                            \
   do {                                                                                         \
     switch (vpl) {                                                                             \
