@@ -92,7 +92,7 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
 // warp shuffles only): no barrier inside the pair loop.  One row per warp
 // keeps the registers low enough for three CTAs per SM, which hides more
 // latency than a second row per warp.
-template <class T, int VL, int PIF, bool EXACT>
+template <class T, int VL, int PIF>
 __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -122,8 +122,7 @@ __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
 #pragma unroll
       for (int q = 0; q < PIF; ++q) {
         const int i = i0 + q * nw;
-        // exact rows: load the (valid, clamped) row unconditionally, discard its dot
-        warp_row<VL, L2_NORMAL, EXACT>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, EXACT || i < P, wr[q]);
+        warp_row<VL>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
       }
       uint4 dw[VL];
 #pragma unroll
@@ -478,11 +477,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
-#define TW_DH(TT, L)                                                                           \
-  do {                                                                                         \
-    if (NV == 32 * (L)) bwd_dh_kernel<TT, L, 1, true><<<a.T, 256, 0, s>>>(p);                  \
-    else bwd_dh_kernel<TT, L, 1, false><<<a.T, 256, 0, s>>>(p);                                \
-  } while (0)
+// (the constant-offset row loads that help the SpMM kernels made this one slower)
+#define TW_DH(TT, L) bwd_dh_kernel<TT, L, 1><<<a.T, 256, 0, s>>>(p)
 #define TW_DH_T(TT)                                                                            \
   do {                                                                                         \
     switch (vl) {                                                                              \
