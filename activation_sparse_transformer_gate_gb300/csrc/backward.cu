@@ -89,11 +89,12 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
 // non-overflow row, in the overflow-row arrays for an overflow row.  Only
 // W_down rows are gathered, so the working set is W_down and dy.  Each warp
 // computes whole dot products for its share of the pairs (PIF rows in flight,
-// warp shuffles only): no barrier inside the pair loop.  One row per warp
-// keeps the registers low enough for three CTAs per SM, which hides more
-// latency than a second row per warp.
+// warp shuffles only): no barrier inside the pair loop.  One row per warp,
+// with dy read from shared memory inside the dot, fits 64 registers at
+// d_model <= 2048 (four CTAs per SM), which hides more latency than a second
+// row per warp.
 template <class T, int VL, int PIF>
-__global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
+__global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -124,16 +125,10 @@ __global__ void __launch_bounds__(256, 2) bwd_dh_kernel(BParams p) {
         const int i = i0 + q * nw;
         warp_row<VL>(Wd4 + (size_t)s_n[i < P ? i : i0] * NV, NV, i < P, wr[q]);
       }
-      uint4 dw[VL];
-#pragma unroll
-      for (int k = 0; k < VL; ++k) {
-        const int vi = lane + 32 * k;
-        dw[k] = vi < NV ? s_dy[vi] : make_uint4(0, 0, 0, 0);
-      }
 #pragma unroll
       for (int q = 0; q < PIF; ++q) {
         const int i = i0 + q * nw;
-        const float d = warp_dot<T, VL>(dw, wr[q]);
+        const float d = warp_dot_smem<T, VL>(s_dy, NV, wr[q]);
         if (lane == 0 && i < P) {
           const int sl = s_slot[i];
           if (sl == PAD_SLOT) continue;
@@ -500,7 +495,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
 #define TW_VPT(K, TT, G)                                                                       \
   do {                                                                                         \
     if (vpt == 1) K<TT, 1, 8, 0><<<G, threads, 0, s>>>(p);                                     \
-    else if (vpt == 2 && NV == 256) K<TT, 2, 3, 128><<<G, 128, 0, s>>>(p);                     \
+    else if (vpt == 2 && NV == 256) K<TT, 2, 4, 128><<<G, 128, 0, s>>>(p);                     \
     else if (vpt == 2) K<TT, 2, 3, 0><<<G, threads, 0, s>>>(p);                                \
     else K<TT, 4, 2, 0><<<G, threads, 0, s>>>(p);                                              \
   } while (0)

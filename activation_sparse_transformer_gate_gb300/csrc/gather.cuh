@@ -138,6 +138,35 @@ __device__ __forceinline__ float warp_dot(const uint4 (&a)[VPL], const uint4 (&b
   return s;
 }
 
+// warp_dot with the first operand read from shared memory vector by vector
+// (lane l reads vectors l, l+32, ...; zero past NV), so it holds no
+// registers across the row loads.
+template <class T, int VPL>
+__device__ __forceinline__ float warp_dot_smem(const uint4 *s_a, int NV, const uint4 (&b)[VPL]) {
+  const int lane = threadIdx.x & 31;
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const int vi = lane + 32 * k;
+    const uint4 a = vi < NV ? s_a[vi] : make_uint4(0, 0, 0, 0);
+    if constexpr (Vec<T>::EV == 8) {
+      s0 = dot2_bf16(a.x, b[k].x, s0);
+      s1 = dot2_bf16(a.y, b[k].y, s1);
+      s0 = dot2_bf16(a.z, b[k].z, s0);
+      s1 = dot2_bf16(a.w, b[k].w, s1);
+    } else {
+      s0 = fmaf(__uint_as_float(a.x), __uint_as_float(b[k].x), s0);
+      s1 = fmaf(__uint_as_float(a.y), __uint_as_float(b[k].y), s1);
+      s0 = fmaf(__uint_as_float(a.z), __uint_as_float(b[k].z), s0);
+      s1 = fmaf(__uint_as_float(a.w), __uint_as_float(b[k].w), s1);
+    }
+  }
+  float s = s0 + s1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
 // Where the active pairs of one (row, tile) come from.  Rows whose tiles all
 // fit their K slots read the TwELL slots; an overflow row reads a dense vector
 // of C ReLU values for each tile (the wide-tile buffer in the forward, the

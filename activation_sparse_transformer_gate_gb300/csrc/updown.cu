@@ -170,7 +170,7 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   do {                                                                                         \
     constexpr int VPT_ = (L + 3) / 4;                                                          \
     if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                             \
-      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, true>                      \
+      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>                      \
           <<<a.T, UD_THREADS, 0, s>>>(p);                                                      \
     else                                                                                       \
       updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>                     \
