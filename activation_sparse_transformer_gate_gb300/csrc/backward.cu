@@ -48,6 +48,12 @@ struct BParams {
 
 __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
 
+// Four fp32 values (two pairs) as the bit pattern of one 16-byte store.
+__device__ __forceinline__ uint4 f4bits(const float2 &a, const float2 &b) {
+  return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b.x),
+                    __float_as_uint(b.y));
+}
+
 // One list entry's weight-gradient update of a thread's 16-byte column slice:
 // ag += dz x, au += du x, ad += h dy (r = {token, dz, du, h}), packed fp32 pairs.
 template <class T>
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
       o[2 * e] = dxg[v][e].x + dxu[v][e].x;
       o[2 * e + 1] = dxg[v][e].y + dxu[v][e].y;
     }
-    if (vi < NV) dxrow[vi] = Vec<T>::pack(o);
+    if (vi < NV) stg_stream(dxrow + vi, Vec<T>::pack(o));
   }
 }
 
@@ -432,10 +438,9 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
     if (vi >= NV) continue;
 #pragma unroll
     for (int q = 0; q < EV / 4; ++q) {
-      og[vi * (EV / 4) + q] = make_float4(ag[v][2 * q].x, ag[v][2 * q].y, ag[v][2 * q + 1].x, ag[v][2 * q + 1].y);
-      od[vi * (EV / 4) + q] = make_float4(ad[v][2 * q].x, ad[v][2 * q].y, ad[v][2 * q + 1].x, ad[v][2 * q + 1].y);
-      if (ou)
-        ou[vi * (EV / 4) + q] = make_float4(au[v][2 * q].x, au[v][2 * q].y, au[v][2 * q + 1].x, au[v][2 * q + 1].y);
+      stg_stream(og + vi * (EV / 4) + q, f4bits(ag[v][2 * q], ag[v][2 * q + 1]));
+      stg_stream(od + vi * (EV / 4) + q, f4bits(ad[v][2 * q], ad[v][2 * q + 1]));
+      if (ou) stg_stream(ou + vi * (EV / 4) + q, f4bits(au[v][2 * q], au[v][2 * q + 1]));
     }
   }
   if (tid == 0) p.dbg[n] = sb;

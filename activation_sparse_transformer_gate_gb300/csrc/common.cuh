@@ -63,6 +63,15 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return r;
 }
 
+// 16-byte store of a row that is not read again by the same kernel (y, dx,
+// dW rows): no L1 allocation, evict-first in L2, so the stream of outputs
+// does not displace the gathered weight rows.
+__device__ __forceinline__ void stg_stream(void *p, const uint4 &v) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+               ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(gather_policy<L2_FIRST>())
+               : "memory");
+}
+
 // ---- device status word ------------------------------------------------------
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
   if (st) atomicCAS(st, 0, code);

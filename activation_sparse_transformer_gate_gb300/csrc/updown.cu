@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
     }
   }
   if (p.gated)  // x_t to shared memory (visible after the barriers of build_pairs)
-    for (int v = tid; v < NV; v += blockDim.x) s_x[v] = ((const uint4 *)p.x)[(size_t)t * NV + v];
+    for (int v = tid; v < NV; v += blockDim.x)  // x_t is read once here: evict-first
+      s_x[v] = ldg_stream<L2_FIRST>((const uint4 *)p.x + (size_t)t * NV + v);
   float2 yr[VPT][EV / 2];
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
-    if (vi < NV) yrow[vi] = Vec<T>::pack(reinterpret_cast<const float *>(yr[v]));
+    if (vi < NV) stg_stream(yrow + vi, Vec<T>::pack(reinterpret_cast<const float *>(yr[v])));
   }
 }
 
