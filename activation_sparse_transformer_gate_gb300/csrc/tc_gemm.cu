@@ -186,7 +186,9 @@ struct Cfg {
   static constexpr int TMEM_COLS = TMEM_COLS_USED <= 32 ? 32 : TMEM_COLS_USED <= 64 ? 64
                                    : TMEM_COLS_USED <= 128 ? 128 : TMEM_COLS_USED <= 256 ? 256
                                                                                          : 512;
-  static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 : 0;  // idx + bf16 val, K<=32
+  // EPI_PACK: per row idx (32 B) + bf16 val (64 B) slots, K <= 32, and a
+  // 32-column bf16 staging row (64 B)
+  static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64 : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
   static_assert(STAGES >= 2, "too few stages");
   static_assert(TMEM_COLS_USED <= 512, "TMEM overflow");
@@ -379,6 +381,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         const int K = p.Kslots;
         uint8_t *my_idx = s_slots + row * 32;
         bf16 *my_val = (bf16 *)(s_slots + 128 * 32) + row * 32;
+        bf16 *my_z = (bf16 *)(s_slots + 128 * 32 * 3) + row * 32;
         for (int jt = 0; jt < BN / p.C; ++jt) {
           const int j = (n0 + jt * p.C) / p.C;      // global TwELL tile index
           const bool tile_ok = n0 + jt * p.C < p.N;
@@ -386,20 +389,36 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             my_idx[k] = 0xFF;
             my_val[k] = __float2bfloat16_rn(0.f);
           }
+          // Per 32-column block: z and its activity mask without branches (a
+          // branch per value serialised the add -> compare -> branch chain of
+          // the one epilogue warp per SM sub-partition); only a block with an
+          // active column (about a quarter of them at 1% density) stages its
+          // bf16 values and appends the active columns in ascending order.
           int cnt = 0;
           for (int c0 = 0; c0 < p.C; c0 += 32) {
             float v[32];
             tmem_ld32(tacc + jt * p.C + c0, v);
-  #pragma unroll
+            const float *bb = s_bias + jt * p.C + c0;
+            uint32_t msk = 0;
+#pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float z = (v[i] + s_bias[jt * p.C + c0 + i]) + rbv;
-              if (z > 0.f) {
+              v[i] = (v[i] + bb[i]) + rbv;  // z
+              msk |= (v[i] > 0.f ? 1u : 0u) << i;
+            }
+            if (msk) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8)
+                *(uint4 *)(my_z + i) = make_uint4(pack_bf2(v[i], v[i + 1]), pack_bf2(v[i + 2], v[i + 3]),
+                                                  pack_bf2(v[i + 4], v[i + 5]), pack_bf2(v[i + 6], v[i + 7]));
+              do {
+                const int b = __ffs(msk) - 1;
+                msk &= msk - 1;
                 if (cnt < K) {
-                  my_idx[cnt] = (uint8_t)(c0 + i);
-                  my_val[cnt] = __float2bfloat16_rn(z);
+                  my_idx[cnt] = (uint8_t)(c0 + b);
+                  my_val[cnt] = my_z[b];
                 }
                 ++cnt;
-              }
+              } while (msk);
             }
           }
           if (row_ok && tile_ok) {
