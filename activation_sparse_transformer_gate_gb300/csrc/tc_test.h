@@ -1,5 +1,5 @@
-// tc_test.h -- test hook of the tcgen05 GEMM engine (exported, not part of the
-// public ABI in include/twell.h): fp32 C[M][N] = A[M][K] B^T with B [N][K]
+// tc_test.h -- test and measurement hooks (exported, not part of the public ABI
+// in include/twell.h).  The tcgen05 GEMM engine: fp32 C[M][N] = A[M][K] B^T with B [N][K]
 // (b_mn = 0) or A B with B [K][N] (b_mn = 1); A, B bf16 device pointers,
 // K % 8 == 0 (16-byte row pitch), N % 8 == 0 when b_mn = 1.  Returns a
 // twell_status code; device-side errors go to *status.
@@ -10,6 +10,12 @@ extern "C" {
 #endif
 int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K, int b_mn,
                        int32_t *status, void *stream);
+
+// Measurement hook: gather n_rows rows (indices in rows[], each < the row count
+// of W, checked by the caller) of row_bytes each from W with `blocks` CTAs of
+// 256 threads; out receives blocks * 8 checksums.  Asynchronous on stream.
+int twell_test_gather_probe(const void *W, int row_bytes, const int32_t *rows, int n_rows,
+                            int blocks, uint32_t *out, void *stream);
 #ifdef __cplusplus
 }
 #endif

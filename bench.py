@@ -247,6 +247,17 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic_for(dominant, args.workload, train),
                 "peak_source": r["peak_source"]}
 
+    # the memory system's rate for the same gather pattern (probe kernel)
+    gceil = gather_ceiling(torch, lib, dev, d["Wu"] if w.gated else d["Wd"], w,
+                           rl["_counts"]["pairs_all"], timed, sh)
+    if gceil:
+        for k, r in rl.items():
+            if r.get("bound") == "hbm":
+                r["frac_of_l2_gather"] = r["achieved"] / gceil
+        if roof and roof["bound"] == "hbm":
+            roof["l2_gather_gbs"] = round(gceil, 1)
+            roof["frac_of_l2_gather"] = round(roof["achieved"] / gceil, 4)
+
     dense = None if args.no_dense else dense_reference(torch, d, w, train, timed, args)
     e2e = None if args.no_e2e else end_to_end(torch, d, step, y, dx, w, train, timed, args)
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(a, w, train, args.cpu_seconds)
@@ -286,6 +297,34 @@ def load_peaks():
                 "source": "of measured (MEASURED_PEAKS.json)"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "of fallback (no MEASURED_PEAKS.json)"}
+
+
+def gather_ceiling(torch, lib, dev, W, w, pairs, timed, sh):
+    """GB/s at which the GPU gathers `pairs` rows of W (F x d_model, bf16) in
+    a uniform random order with plain 16-byte loads: the measured ceiling
+    for the sparse kernels' row gathers (L2-served when W fits in L2), timed
+    like the step (events on the stream, L2 flushed before every run)."""
+    if pairs < 1:
+        return None
+    rng = np.random.default_rng(7)
+    rows = torch.from_numpy(rng.integers(0, w.F, size=pairs).astype(np.int32)).to(dev)
+    blocks = 6 * torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty((blocks * 8,), dtype=torch.int32, device=dev)
+    f = lib.twell_test_gather_probe
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    row_bytes = w.D * 2
+
+    def run():
+        rc = f(W.data_ptr(), row_bytes, rows.data_ptr(), pairs, blocks, out.data_ptr(), sh)
+        if rc != 0:
+            raise SystemExit(f"gather probe failed: {rc}")
+
+    for _ in range(3):
+        run()
+    n = 20
+    ms = timed(run, n) / n
+    return pairs * row_bytes / (ms / 1e3) / 1e9
 
 
 def kernel_rooflines(kern, w, nnz, train):
