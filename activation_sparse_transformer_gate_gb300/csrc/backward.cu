@@ -89,6 +89,33 @@ __device__ __forceinline__ PairSource<T> bwd_source(const BParams &p, int t, int
   return src;
 }
 
+// The pair's gradients from its dot d = dy . W_down[n]: dh = d + lambda
+// sign(h), dz = [g > 0] dh u, du = [g > 0] dh g, and h = g u (plain FFN:
+// u = 1), stored at the TwELL slot (sl >= 0) or in the overflow-row arrays
+// (sl = -1 - n).  Pad pairs (PAD_SLOT) store nothing.
+template <class T>
+__device__ __forceinline__ void dh_finish(const BParams &p, int ps, int sl, float g, float d) {
+  if (sl == PAD_SLOT) return;
+  const float u = !p.gated ? 1.f
+                           : (sl >= 0 ? to_f(((const T *)p.u_val)[sl])
+                                      : to_f(((const T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)]));
+  const float h = p.gated ? g * u : g;
+  const float dh = d + p.lambda * sgnf(h);
+  const bool act = g > 0.f;
+  const float dz = act ? (p.gated ? dh * u : dh) : 0.f;
+  const float du = act ? dh * g : 0.f;
+  if (sl >= 0) {
+    p.dz[sl] = dz;
+    p.du[sl] = du;
+    p.hs[sl] = h;
+  } else {
+    const size_t o = (size_t)ps * p.F + (-1 - sl);
+    p.dzr[o] = dz;
+    p.dur[o] = du;
+    p.hr[o] = h;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 2a. Per-token dh SDDMM (hybrid x dense): dh = dy . Wd[n] + lambda sign(h) at
 // every active pair, then dz, du, h of the pair -- at its TwELL slot for a
@@ -117,8 +144,6 @@ __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p)
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
   for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
   const uint4 *Wd4 = (const uint4 *)p.Wd;
-  const T *uval = (const T *)p.u_val;
-  const T *ufb = (const T *)p.u_fb;
   const PairSource<T> src = bwd_source<T>(p, t, ps);
   int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
   if (group > (int)blockDim.x) group = blockDim.x;
@@ -135,12 +160,106 @@ __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p)
       for (int q = 0; q < PIF; ++q) {
         const int i = i0 + q * nw;
         const float d = warp_dot_smem<T, VL>(s_dy, NV, wr[q]);
-        if (lane == 0 && i < P) {
-          const int sl = s_slot[i];
-          if (sl == PAD_SLOT) continue;
-          const float g = s_g[i];
-          const float u = !p.gated ? 1.f : (sl >= 0 ? to_f(uval[sl])
-                                                    : to_f(ufb[(size_t)ps * p.F + (-1 - sl)]));
+        if (lane == 0 && i < P) dh_finish<T>(p, ps, s_slot[i], s_g[i], d);
+      }
+    }
+    __syncthreads();  // the list is rewritten by the next group
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2a'. The same dh SDDMM on the tensor cores (bf16, d_model a multiple of 256).
+// One CTA (8 warps) per token; the pairs are taken 16 at a time, and warp w
+// covers the w-th eighth of d_model for all 16: per 32-element chunk one
+// mma.sync.m16n8k16 pair with A = the 16 gathered W_down rows (thread (g, q)
+// loads 16 bytes of rows g and g + 8) and B = the dy chunk in column 0 (lanes
+// 0-3; the other columns are zero).  A and B take the chunk's elements in the
+// same order, so C[r][0] is the partial dot of row r.  The eight partials of
+// a pair are summed in a fixed order in shared memory, then one thread per
+// pair applies dh_finish.  The tensor core does the multiply-adds and the
+// reduction that the warp-level kernel spends most of its instructions on.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+      " {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int DH_WARPS = 8;
+constexpr int DH_CHUNK = 256;  // pairs whose partial dots are held before the finish
+
+template <int U>
+__global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
+    bwd_dh_mma_kernel(BParams p) {
+  __shared__ int s_n[LIST_CAP];
+  __shared__ float s_g[LIST_CAP];
+  __shared__ int s_slot[LIST_CAP];
+  __shared__ uint4 s_dy[1024];
+  __shared__ float s_u[DH_CHUNK];
+  __shared__ float s_part[DH_WARPS][DH_CHUNK];
+  __shared__ int s_wsum[32];
+  __shared__ int s_total;
+
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gq = lane >> 2, q = lane & 3;
+  const int nt = p.F / p.C;
+  const int NV = p.D / 8;               // 16-byte vectors per row
+  const int CPW = NV / (4 * DH_WARPS);  // 32-element chunks per warp (NV % 32 == 0)
+  const int ps = p.pos[t];
+  if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
+  for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
+  const uint4 *Wd4 = (const uint4 *)p.Wd;
+  const uint4 *dyw = s_dy + 4 * w * CPW + q;  // this lane's dy vectors (read by lanes 0-3)
+  const bf16 *uval = (const bf16 *)p.u_val, *ufb = (const bf16 *)p.u_fb;
+  const PairSource<bf16> src = bwd_source<bf16>(p, t, ps);
+  int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
+  if (group > (int)blockDim.x) group = blockDim.x;
+  for (int g0 = 0; g0 < nt; g0 += group) {
+    const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
+    for (int cb = 0; cb < P; cb += DH_CHUNK) {
+      const int PC = P - cb < DH_CHUNK ? P - cb : DH_CHUNK;
+      // u of the chunk's pairs, fetched while the rows stream in
+      if (tid < PC) {
+        const int sl = s_slot[cb + tid];
+        s_u[tid] = (!p.gated || sl == PAD_SLOT) ? 1.f
+                   : to_f(sl >= 0 ? uval[sl] : ufb[(size_t)ps * p.F + (-1 - sl)]);
+      }
+      for (int pb = 0; pb < PC; pb += 16) {
+        // rows g and g + 8 of the block (past the chunk: its first row, result unused)
+        const int r0 = pb + gq < PC ? pb + gq : pb, r1 = pb + gq + 8 < PC ? pb + gq + 8 : pb;
+        const uint4 *w0 = Wd4 + (size_t)s_n[cb + r0] * NV + 4 * w * CPW + q;
+        const uint4 *w1 = Wd4 + (size_t)s_n[cb + r1] * NV + 4 * w * CPW + q;
+        // two accumulator chains (even / odd half of each chunk)
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c0 = 0; c0 < CPW; c0 += U) {
+          uint4 A0[U], A1[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            A0[u] = ldg_stream(w0 + 4 * (c0 + u));
+            A1[u] = ldg_stream(w1 + 4 * (c0 + u));
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const uint4 b = gq == 0 ? dyw[4 * (c0 + u)] : make_uint4(0, 0, 0, 0);
+            mma_bf16_16816(c, A0[u].x, A1[u].x, A0[u].y, A1[u].y, b.x, b.y);
+            mma_bf16_16816(e, A0[u].z, A1[u].z, A0[u].w, A1[u].w, b.z, b.w);
+          }
+        }
+        if (q == 0) {  // C[g][0] and C[g + 8][0]
+          if (pb + gq < PC) s_part[w][pb + gq] = c[0] + e[0];
+          if (pb + gq + 8 < PC) s_part[w][pb + gq + 8] = c[2] + e[2];
+        }
+      }
+      __syncthreads();
+      if (tid < PC) {  // one thread per pair: partials in a fixed order
+        float d = 0.f;
+#pragma unroll
+        for (int k = 0; k < DH_WARPS; ++k) d += s_part[k][tid];
+        const int i = cb + tid, sl = s_slot[i];
+        if (sl != PAD_SLOT) {
+          const float g = s_g[i], u = s_u[tid];
           const float h = p.gated ? g * u : g;
           const float dh = d + p.lambda * sgnf(h);
           const bool act = g > 0.f;
@@ -158,8 +277,8 @@ __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p)
           }
         }
       }
+      __syncthreads();  // s_part / s_u are rewritten by the next chunk
     }
-    __syncthreads();  // the list is rewritten by the next group
   }
 }
 
@@ -490,8 +609,18 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
       default: TW_DH(TT, 32); break;                                                           \
     }                                                                                          \
   } while (0)
-  if (bf) TW_DH_T(bf16);
-  else TW_DH_T(float);
+  if (bf && NV % (4 * DH_WARPS) == 0) {
+    // tensor-core dh SDDMM: chunks per warp = NV / 32; U of them per load
+    // batch (4: three CTAs per SM, measured faster than 8 at two)
+    const int cpw = NV / (4 * DH_WARPS);
+    if (cpw % 4 == 0) bwd_dh_mma_kernel<4><<<a.T, DH_WARPS * 32, 0, s>>>(p);
+    else if (cpw % 2 == 0) bwd_dh_mma_kernel<2><<<a.T, DH_WARPS * 32, 0, s>>>(p);
+    else bwd_dh_mma_kernel<1><<<a.T, DH_WARPS * 32, 0, s>>>(p);
+  } else if (bf) {
+    TW_DH_T(bf16);
+  } else {
+    TW_DH_T(float);
+  }
 #undef TW_DH_T
 #undef TW_DH
   e = cudaGetLastError();
