@@ -131,6 +131,27 @@ def test_transpose_several_token_chunks_ragged():
     check_backward(a, w, g, 1e-3)
 
 
+@pytest.mark.parametrize("D", [512, 1024])
+def test_bf16_dmodel_shapes(D):
+    """d_model 512 and 1024: the tensor-core dh SDDMM with 2 and 4 chunks per
+    warp, and the generic two-vector dx / dW paths."""
+    w = synth.Workload(f"bdm{D}", 160, D, 512, 128, 8, "bf16", True, -1.9, 40 + D // 512,
+                       hot_tokens=2, seq_len=80, hot_bias=1.5, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3)
+    assert g["code"] == 0 and g["n_ovf"] >= 1
+    check_backward(a, w, g, 1e-3)
+
+
+def test_fp32_dmodel1024_exact_shapes():
+    """fp32 d_model 1024: 256 vectors per row, the exact-shape dx and dW paths."""
+    w = synth.Workload("bf32d1k", 96, 1024, 256, 64, 4, "f32", True, -1.7, 43, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3)
+    assert g["code"] == 0
+    check_backward(a, w, g, 1e-3)
+
+
 @pytest.mark.parametrize("C,K", [(32, 2), (64, 16), (128, 32)])
 def test_tile_shapes(C, K):
     w = synth.Workload(f"bt{C}{K}", 96, 128, 512, C, K, "bf16", True, -1.9, 25 + K, train=True)

@@ -159,6 +159,27 @@ def test_integer_grid_bit_exact():
     check_forward(a, w, g, exact=True)
 
 
+@pytest.mark.parametrize("D", [512, 1024])
+def test_bf16_dmodel_shapes(D):
+    """d_model 512 (64 vectors per row: generic fused up/down path) and 1024
+    (128 vectors: the exact-shape path, one vector per thread)."""
+    w = synth.Workload(f"dm{D}", 200, D, 512, 128, 8, "bf16", True, -1.9, 30 + D // 512,
+                       hot_tokens=2, seq_len=100, hot_bias=1.5)
+    a = synth.generate(w)
+    g = run_forward(a, w)
+    assert g["code"] == 0 and g["n_ovf"] >= 1
+    check_forward(a, w, g)
+
+
+def test_fp32_dmodel1024_exact_shapes():
+    """fp32 d_model 1024: 256 vectors per row, the exact-shape fused path."""
+    w = synth.Workload("f32d1k", 96, 1024, 256, 64, 4, "f32", True, -1.7, 33)
+    a = synth.generate(w)
+    g = run_forward(a, w)
+    assert g["code"] == 0
+    check_forward(a, w, g)
+
+
 def test_fp32_gated_small_tiles():
     w = synth.Workload("f32g", 130, 64, 256, 32, 2, "f32", True, -1.6, 9)
     a = synth.generate(w)
