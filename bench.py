@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import datetime
 import ctypes
 import hashlib
 import io
@@ -53,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-dense", action="store_true", help="skip the cuBLAS dense FFN")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-energy", action="store_true",
+                    help="skip the saved-memory and energy-per-token leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -260,6 +263,10 @@ def run_ours(args, rank, world, local_rank):
 
     dense = None if args.no_dense else dense_reference(torch, d, w, train, timed, args)
     e2e = None if args.no_e2e else end_to_end(torch, d, step, y, dx, w, train, timed, args)
+    mem = energy = None
+    if not args.no_energy:
+        mem, energy = memory_and_energy(torch, dev, local_rank, d, w, train, step, bufs, nws,
+                                        int(row_ovf_count(bufs, w)))
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(a, w, train, args.cpu_seconds)
 
     row_ovf = (nnz > w.K).any(axis=0)
@@ -281,6 +288,8 @@ def run_ours(args, rank, world, local_rank):
         "kernel_roofline": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                                 for kk, vv in v.items()} for k, v in rl.items()},
         "sparsity": {"active_frac": float(nnz.sum() / (T * F)), "n_ovf": int(row_ovf.sum())},
+        "memory": mem,
+        "energy": energy,
     }
     if dense:
         line["dense_cublas"] = dense
@@ -389,8 +398,16 @@ def traffic_for(kernel, workload, train):
     return e.get("dram_bytes_per_launch")
 
 
-def dense_reference(torch, d, w, train, timed, args):
-    """The same FFN with cuBLAS GEMMs through torch (bf16, fp32 accumulate)."""
+def row_ovf_count(bufs, w):
+    """Overflow rows of the current TwELL (a row overflows if any tile does)."""
+    nnz = bufs.nnz.cpu().numpy()
+    return int((nnz > w.K).any(axis=0).sum())
+
+
+def dense_step_fn(torch, d, w, train):
+    """One step of the same FFN with cuBLAS GEMMs through torch (bf16 operands,
+    fp32 accumulation): forward, and for training the backward with the L1
+    term."""
     x, Wg, Wu, Wd, rb, dy = d["x"], d["Wg"], d["Wu"], d["Wd"], d["rb"], d["dy"]
     bgb = d["bg"].to(torch.bfloat16)
     lam = w.lam
@@ -409,6 +426,119 @@ def dense_reference(torch, d, w, train, timed, args):
         dz = torch.where(z > 0, dh * u, torch.zeros_like(dh))
         du = dh * g
         return (dz @ Wg + du @ Wu, dz.t() @ x, du.t() @ x, h.t() @ dy, dz.float().sum(0))
+
+    return step
+
+
+class PowerSampler:
+    """nvidia-smi power.draw samples (20 ms) with their timestamps."""
+
+    def __init__(self, index: int):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=timestamp,power.draw",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        samples = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 2:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(r[1])))
+            except ValueError:
+                continue
+        return samples
+
+
+def memory_and_energy(torch, dev, index, d, w, train, ours_step, bufs, nws, n_ovf, seconds=2.5):
+    """Saved-activation bytes (forward -> backward) and device memory of the
+    sparse path against the dense one, and energy per token of each measured
+    with the GPU's energy counter over a few seconds of back-to-back steps."""
+    T, F = w.T, w.F
+    es = 2  # bf16
+    nt = F // w.C
+    twell = nt * T * (w.K * (1 + es) + 1) + (nt * T * w.K * es if train else 0)
+    fb = n_ovf * F * es * (2 if train else 1) + 4 * n_ovf
+    dense_step = dense_step_fn(torch, d, w, train)
+    dense_step()
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    dense_step()
+    torch.cuda.synchronize(dev)
+    dense_peak = torch.cuda.max_memory_allocated(dev) - base
+    buf_bytes = sum(t.numel() * t.element_size() for t in
+                    (bufs.idx, bufs.val, bufs.nnz, bufs.ovf_rows, bufs.g_fb, bufs.u_val, bufs.u_fb)
+                    if t is not None)
+    mem = {
+        "saved_activation_bytes_sparse": twell + fb,
+        "saved_activation_bytes_dense": (3 * T * F * es) if train else 0,
+        "note_saved": "sparse: TwELL idx/val/nnz (+u at the slots) and the used overflow rows; "
+                      "dense: z, u, h [T][F] bf16 kept for the backward",
+        "dense_step_peak_extra_bytes": int(dense_peak),
+        "sparse_buffers_allocated_bytes": int(buf_bytes),
+        "sparse_workspace_bytes": int(nws),
+        "note_alloc": "buffers sized for ovf_cap = T overflow rows and a workspace sized for the "
+                      "all-dense fallback: allocations, not what a step keeps",
+    }
+
+    def joules_per_token(fn):
+        """Mean board power over a few seconds of back-to-back steps x their
+        time / tokens (power samples inside the loop's wall-clock window)."""
+        fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < 0.3:
+            fn()
+            n += 1
+        torch.cuda.synchronize(dev)
+        per = (time.perf_counter() - t0) / n
+        reps = max(10, int(seconds / per))
+        ps = PowerSampler(index)
+        time.sleep(0.5)
+        w0 = time.time()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        w1 = time.time()
+        samples = ps.stop()
+        inside = [pw for ts, pw in samples if w0 + 0.1 <= ts <= w1]
+        if len(inside) < 5:
+            return None
+        watts = float(np.mean(inside))
+        return {"j_per_token": watts * wall / (reps * T), "mean_w": watts, "samples": len(inside),
+                "s": round(wall, 3)}
+
+    es_, ed_ = joules_per_token(ours_step), joules_per_token(dense_step)
+    energy = None
+    if es_ and ed_:
+        energy = {"sparse_j_per_token": es_["j_per_token"], "dense_j_per_token": ed_["j_per_token"],
+                  "ratio": es_["j_per_token"] / ed_["j_per_token"],
+                  "sparse_mean_w": es_["mean_w"], "dense_mean_w": ed_["mean_w"],
+                  "how": f"mean nvidia-smi power.draw (20 ms samples) x time over >= {seconds} s of "
+                         "back-to-back steps (no L2 flush), whole board"}
+    return mem, energy
+
+
+def dense_reference(torch, d, w, train, timed, args):
+    """The same FFN with cuBLAS GEMMs through torch (bf16, fp32 accumulate)."""
+    step = dense_step_fn(torch, d, w, train)
 
     for _ in range(max(args.warmup, 3)):
         step()
