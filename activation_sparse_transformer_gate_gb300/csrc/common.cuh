@@ -86,10 +86,11 @@ constexpr int OVF_GEMM_MIN = 128;
 
 struct Ctl {
   int32_t n_rows;   // rows on the dense GEMM path: T (all-dense), n_ovf (ovf_gemm) or 0
-  int32_t dense;    // 1: every row runs densely (n_ovf > dense_switch * T)
+  int32_t dense;    // 1: every row runs densely (n_ovf > dense_switch * T, or dense slots)
   int32_t n_ovf;    // true number of overflow rows
   int32_t ovf_gemm; // 1: overflow rows run on the dense GEMM path
-  int32_t pad[12];
+  unsigned long long slots;  // TwELL slots written by the gate epilogue (zeroed before it)
+  int32_t pad[10];
 };
 
 }  // namespace twell

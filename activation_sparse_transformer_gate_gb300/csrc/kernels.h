@@ -46,6 +46,7 @@ struct FwdArgs {
   void *y;
   Workspace ws;
   float dense_switch;
+  float dense_density;  // <= 0: no density test
 };
 
 struct BwdArgs {
@@ -68,8 +69,11 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // block and -- when write_user -- the caller's ovf_rows and n_ovf.  Without a
 // workspace: derives the flags from nnz (one CTA) and writes only the caller's
 // list and count.
+// dense_density > 0: all-dense also when ctl->slots (zeroed before the gate,
+// summed by its epilogue) exceeds dense_density * T * F; <= 0 ignores slots.
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
-                                    cudaStream_t s, bool write_user = true);
+                                    cudaStream_t s, bool write_user = true,
+                                    float dense_density = -1.f);
 // Overflow-row bitmap from the nnz counts (clears the bitmap first).
 cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s);
 // Dense backup rows of overflow rows that do not take the dense GEMM path.

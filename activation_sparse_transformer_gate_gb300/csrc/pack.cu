@@ -75,8 +75,14 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s) 
 }
 
 // Mode decisions taken on the device after the overflow rows are counted.
-__device__ __forceinline__ void write_ctl(Ctl *ctl, int n_ovf, int Tn, float dense_switch) {
-  const int dense = (float)n_ovf > dense_switch * (float)Tn ? 1 : 0;
+// All-dense when too many rows overflow, or when the slots the gate epilogue
+// wrote (active entries, at most K per row and tile, so overflow rows count
+// little) exceed dense_density * T * F: gathers then cost more than GEMMs.
+__device__ __forceinline__ void write_ctl(Ctl *ctl, int n_ovf, int Tn, int F, float dense_switch,
+                                          float dense_density) {
+  const bool too_dense =
+      dense_density > 0.f && (double)ctl->slots > (double)dense_density * (double)Tn * (double)F;
+  const int dense = ((float)n_ovf > dense_switch * (float)Tn || too_dense) ? 1 : 0;
   const int og = (!dense && n_ovf >= OVF_GEMM_MIN) ? 1 : 0;
   ctl->n_ovf = n_ovf;
   ctl->dense = dense;
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(1024)
 overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
                      int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf, int32_t *status,
                      Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
-                     float dense_switch) {
+                     int F, float dense_switch, float dense_density) {
   __shared__ int warp_off[32];
   __shared__ int word_off[1024];
   __shared__ int total;
@@ -198,17 +204,17 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
   if (tid == 0) {
     if (n_ovf) *n_ovf = running;
     if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
-    write_ctl(ctl, running, Tn, dense_switch);
+    write_ctl(ctl, running, Tn, F, dense_switch, dense_density);
   }
 }
 
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
-                                    cudaStream_t s, bool write_user) {
+                                    cudaStream_t s, bool write_user, float dense_density) {
   if (ws) {
     overflow_scan_kernel<<<1, 1024, 0, s>>>(ws->ovf_bits, tw.T, tw.ovf_cap,
                                             write_user ? tw.ovf_rows : nullptr,
                                             write_user ? tw.n_ovf : nullptr, tw.status, ws->ctl,
-                                            ws->rows, ws->pos, dense_switch);
+                                            ws->rows, ws->pos, tw.F, dense_switch, dense_density);
     return cudaGetLastError();
   }
   overflow_compact_kernel<<<1, 1024, 0, s>>>(tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,

@@ -35,7 +35,7 @@ simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
                       const float *__restrict__ bg, const float *__restrict__ rb, int Tn, int D,
                       int F, int K, uint8_t *__restrict__ idx, T *__restrict__ val,
                       uint8_t *__restrict__ nnz, uint32_t *__restrict__ ovf_bits,
-                      T *__restrict__ wide) {
+                      T *__restrict__ wide, unsigned long long *__restrict__ slots) {
   constexpr int TN = BN / 16;
   constexpr int E = BN / 32;
   __shared__ float smem[BM * (BN + 1) > BK * (BM + 4) + BK * (BN + 4) ? BM * (BN + 1)
@@ -127,6 +127,7 @@ simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
     if (lane == 0) {
       nnz[(size_t)j * Tn + t] = (uint8_t)cnt;
       if (cnt > K) atomicOr(&ovf_bits[t >> 5], 1u << (t & 31));
+      if (filled && slots) atomicAdd(slots, (unsigned long long)filled);  // dispatcher's density
     }
     if (cnt > K) {  // overflowing (row, tile): keep the full ReLU(z) tile
       T *wd = wide + ((size_t)j * Tn + t) * BN;
@@ -141,7 +142,7 @@ cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s) {
 #define TW_GP(TT, BNN)                                                                         \
   simt_gate_pack_kernel<TT, BNN><<<grid, NT, 0, s>>>(                                          \
       (const TT *)a.x, (const TT *)a.Wg, a.bg, a.rb, a.T, a.D, a.F, a.K, a.tw.idx,             \
-      (TT *)a.tw.val, a.tw.nnz, a.ws.ovf_bits, (TT *)a.ws.wide)
+      (TT *)a.tw.val, a.tw.nnz, a.ws.ovf_bits, (TT *)a.ws.wide, &a.ws.ctl->slots)
   if (a.dtype == TWELL_BF16) {
     if (a.C == 32) TW_GP(bf16, 32); else if (a.C == 64) TW_GP(bf16, 64); else TW_GP(bf16, 128);
   } else {

@@ -169,6 +169,7 @@ struct TcParams {
   const int32_t *rows, *pos;
   uint8_t *idx, *nnz;
   uint32_t *ovf_bits;
+  unsigned long long *slots;  // EPI_PACK: total slots written (the dispatcher's density)
   bf16 *val;
   bf16 *h, *g_fb, *u_fb, *y;
   bf16 *wide, *urows;
@@ -382,6 +383,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         uint8_t *my_idx = s_slots + row * 32;
         bf16 *my_val = (bf16 *)(s_slots + 128 * 32) + row * 32;
         bf16 *my_z = (bf16 *)(s_slots + 128 * 32 * 3) + row * 32;
+        uint32_t my_slots = 0;  // slots this row writes in this output tile
         for (int jt = 0; jt < BN / p.C; ++jt) {
           const int j = (n0 + jt * p.C) / p.C;      // global TwELL tile index
           const bool tile_ok = n0 + jt * p.C < p.N;
@@ -441,6 +443,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             }
             p.nnz[(size_t)j * p.Tn + m] = (uint8_t)cnt;
             if (cnt > K) atomicOr(&p.ovf_bits[m >> 5], 1u << (m & 31));
+            my_slots += (uint32_t)(cnt < K ? cnt : K);
           }
           // An overflowing (row, tile) also keeps its full ReLU(z) tile (the
           // accumulator is read again; the load is warp-collective).
@@ -464,6 +467,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             }
           }
         }
+        const uint32_t warp_slots = __reduce_add_sync(0xffffffffu, my_slots);
+        if (lane == 0 && warp_slots && p.slots) atomicAdd(p.slots, (unsigned long long)warp_slots);
       } else if (EPI == EPI_GU) {
         const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
         const float rbv = (p.rb && row_ok) ? p.rb[tok] : 0.f;
@@ -631,6 +636,7 @@ TcParams base_params(const FwdArgs &a) {
   p.gated = a.gated; p.train = a.train; p.bg = a.bg; p.rb = a.rb; p.rows = a.ws.rows;
   p.pos = a.ws.pos; p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val;
   p.ovf_bits = a.ws.ovf_bits;
+  p.slots = &a.ws.ctl->slots;
   p.wide = (bf16 *)a.ws.wide;
   p.urows = (bf16 *)a.ws.urows;
   p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;

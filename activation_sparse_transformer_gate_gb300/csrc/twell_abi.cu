@@ -149,18 +149,25 @@ twell_status check_ws(void *ws, size_t ws_bytes, const Workspace &need) {
 }
 
 float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_switch : 0.5f; }
+// Slot density above which the forward runs densely (0 -> 0.013, < 0 -> off).
+float density_of(const twell_t *tw) {
+  return tw->dense_density == 0.f ? 0.013f : (tw->dense_density > 0.f ? tw->dense_density : -1.f);
+}
 
 bool use_tc(int dtype) { return dtype == TWELL_BF16 && tc_available(); }
 
 // Steps 1-2 of the forward (shared by twell_pack and twell_ffn_forward).
 cudaError_t run_gate_and_split(FwdArgs &a, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(a.ws.ovf_bits, 0, 4 * (((size_t)a.T + 31) / 32), s);
+  // control block (its slot counter) and the overflow bitmap are adjacent
+  const size_t clear = (size_t)((const char *)a.ws.ovf_bits - (const char *)a.ws.ctl) +
+                       4 * (((size_t)a.T + 31) / 32);
+  cudaError_t e = cudaMemsetAsync(a.ws.ctl, 0, clear, s);
   if (e != cudaSuccess) return e;
   prof_mark(KID_START, s);
   e = use_tc(a.dtype) ? launch_tc_gate_pack(a, s) : launch_simt_gate_pack(a, s);
   if (e != cudaSuccess) return e;
   prof_mark(KID_GATE_PACK, s);
-  e = launch_overflow_compact(a.tw, &a.ws, a.dense_switch, s);
+  e = launch_overflow_compact(a.tw, &a.ws, a.dense_switch, s, true, a.dense_density);
   prof_mark(KID_OVERFLOW_COMPACT, s);
   return e;
 }
@@ -234,6 +241,7 @@ twell_status twell_pack(const void *x, const void *Wg, const float *bg, const fl
   a.gated = 0; a.train = 0; a.x = x; a.Wg = Wg; a.bg = bg; a.rb = row_bias; a.tw = *tw;
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 0);
   a.dense_switch = 2.0f;  // the pack never switches to all-dense mode
+  a.dense_density = -1.f;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = run_gate_and_split(a, s);
   if (e == cudaSuccess) {  // dense backup rows: assembled (few rows) or recomputed (many)
@@ -267,6 +275,7 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.bg = bg; a.rb = row_bias; a.tw = *tw; a.y = y;
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, train);
   a.dense_switch = switch_of(tw);
+  a.dense_density = density_of(tw);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = run_gate_and_split(a, s);
   if (e == cudaSuccess) {

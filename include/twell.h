@@ -102,6 +102,11 @@ typedef struct {
   int32_t *status;        /* device int32, must be 0 before the first call   */
   float dense_switch;     /* forward runs every row densely when
                              n_ovf > dense_switch * T; <= 0 selects 0.5      */
+  float dense_density;    /* ... or when the slots written (active entries,
+                             at most K per row and tile) exceed
+                             dense_density * T * F: at such densities the
+                             gathers cost more than dense GEMMs.  0 selects
+                             0.013; < 0 disables this test                  */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward
@@ -124,7 +129,8 @@ twell_status twell_pack(const void *x, const void *Wg, const float *bg, const fl
 
 /* FFN forward (sections 2.A + 2.B): twell_pack, then the fused up + down
  * projection over the TwELL slots for non-overflow rows, and dense up + down
- * for the overflow rows (all rows when n_ovf > dense_switch * T).
+ * for the overflow rows (all rows when n_ovf > dense_switch * T or the
+ * slots exceed dense_density * T * F).
  * Wu == NULL selects the plain FFN y = ReLU(z) Wd.  y [T][D] dtype.
  * train != 0 additionally stores u at the slots (tw->u_val) and the u rows of
  * the overflow rows (tw->u_fb) for twell_ffn_backward. */

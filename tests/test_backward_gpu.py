@@ -21,15 +21,21 @@ def _lib():
     tw.load()
 
 
-def run_train(a, w, lam, ovf_cap=None):
+def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None):
+    """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
+    the density test of the dispatcher off, so that moderately dense test
+    workloads still run the gather kernels; out (dict) receives the
+    workspace's control block."""
     T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
     dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     d = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
-    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True)
+    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density)
     ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
     y = torch.empty((T, D), dtype=tdt, device="cuda")
     tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 1, bufs.t, y, ws, nws)
+    if out is not None:
+        out["ctl"] = ws[:24].cpu().numpy().copy()
     dx = torch.full((T, D), float("nan"), dtype=tdt, device="cuda")
     dWg = torch.full((F, D), float("nan"), dtype=torch.float32, device="cuda")
     dWu = torch.full_like(dWg, float("nan")) if d["Wu"] is not None else None
@@ -128,6 +134,19 @@ def test_transpose_several_token_chunks_ragged():
     a = synth.generate(w)
     g = run_train(a, w, 1e-3)
     assert g["code"] == 0 and g["n_ovf"] >= 1
+    check_backward(a, w, g, 1e-3)
+
+
+def test_backward_after_density_switched_dense_forward():
+    """~5% active, K = 16: the forward runs every row densely (density test on,
+    u at the slots filled from the dense u rows); the backward then gathers
+    from the slots and matches the oracle."""
+    w = synth.Workload("bdens", 160, 256, 1024, 128, 16, "bf16", True, -1.64, 44, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, dense_density=0.0, out=out)
+    assert g["code"] == 0
+    assert int(out["ctl"][4:8].view(np.int32)[0]) == 1  # the forward ran densely
     check_backward(a, w, g, 1e-3)
 
 

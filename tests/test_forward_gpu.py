@@ -21,20 +21,24 @@ def _lib():
     tw.load()
 
 
-def run_forward(a, w, train=False, ovf_cap=None, dense_switch=0.0, D=None):
+def run_forward(a, w, train=False, ovf_cap=None, dense_switch=0.0, D=None, dense_density=-1.0):
+    """Forward through the C ABI.  dense_density < 0 keeps the dispatcher's
+    density test off (moderately dense test workloads still take the gather
+    kernels); the workspace's control block is returned as "ctl"."""
     T, F, C, K = a["x"].shape[0], a["Wg"].shape[0], w.C, w.K
     D = a["x"].shape[1]
     dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dev = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb")}
-    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train, dense_switch=dense_switch)
+    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train, dense_switch=dense_switch,
+                           dense_density=dense_density)
     ws, nws = tw.workspace(T, D, F, C, K, dtype, train)
     y = torch.full((T, D), float("nan"), dtype=tdt, device="cuda")
     tw.twell_ffn_forward(dev["x"], dev["Wg"], dev["bg"], dev["rb"], dev["Wu"], dev["Wd"], D,
                          int(train), bufs.t, y, ws, nws)
     code, n_ovf = tw.twell_get_status(bufs.t)
     n_keep = min(n_ovf, bufs.cap)
-    return dict(code=code, n_ovf=n_ovf, y=to_np64(y), idx=bufs.idx.cpu().numpy(),
+    return dict(code=code, n_ovf=n_ovf, y=to_np64(y), ctl=ws[:24].cpu().numpy().copy(), idx=bufs.idx.cpu().numpy(),
                 val=to_np64(bufs.val), nnz=bufs.nnz.cpu().numpy(),
                 ovf_rows=bufs.ovf_rows[:n_keep].cpu().numpy(), g_fb=to_np64(bufs.g_fb[:n_keep]),
                 u_val=None if bufs.u_val is None else to_np64(bufs.u_val),
@@ -178,6 +182,44 @@ def test_fp32_dmodel1024_exact_shapes():
     g = run_forward(a, w)
     assert g["code"] == 0
     check_forward(a, w, g)
+
+
+def _ctl(g):
+    """(dense flag, slot counter) of the workspace's control block."""
+    c = g["ctl"]
+    return int(c[4:8].view(np.int32)[0]), int(c[16:24].view(np.uint64)[0])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_density_switch_runs_dense_rows(dtype):
+    """~5% active with K = 16: few rows overflow, but the slots written exceed
+    the default density threshold, so the whole forward runs on the dense
+    path; with the test disabled the gathers run.  Both match the oracle; the
+    slot counter equals sum(min(nnz, K)) exactly."""
+    w = synth.Workload(f"dens{dtype}", 192, 256, 1024, 128, 16, dtype, True, -1.64, 34)
+    a = synth.generate(w)
+    on = run_forward(a, w, dense_density=0.0)
+    off = run_forward(a, w, dense_density=-1.0)
+    for g in (on, off):
+        assert g["code"] == 0
+        check_forward(a, w, g)
+    dense_on, slots_on = _ctl(on)
+    dense_off, slots_off = _ctl(off)
+    expect = int(np.minimum(on["nnz"].astype(np.int64), w.K).sum())
+    assert slots_on == expect and slots_off == expect
+    assert expect > 0.013 * w.T * w.F
+    assert dense_on == 1 and dense_off == 0
+
+
+def test_density_switch_keeps_sparse_workloads_sparse():
+    """1% active (the pages' regime): the default threshold keeps the gathers."""
+    w = synth.Workload("dens1", 256, 256, 1024, 128, 8, "bf16", True, -2.33, 35)
+    a = synth.generate(w)
+    g = run_forward(a, w, dense_density=0.0)
+    assert g["code"] == 0
+    check_forward(a, w, g)
+    dense, slots = _ctl(g)
+    assert dense == 0 and 0 < slots < 0.013 * w.T * w.F
 
 
 def test_fp32_gated_small_tiles():
