@@ -694,6 +694,7 @@ cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
 // Down projection of the dense-path rows: A = h rows (dense-path order),
 // B = W_down read MN-major from its neuron-major [F][D] storage.
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
+  // 128 x 256 output tiles (as the gate GEMM): half the A re-reads of 128 x 128
   CUtensorMap mh, md;
   if (!make_map(&mh, a.ws.h, a.F, a.T, 64, BM) || !make_map(&md, a.Wd, a.D, a.F, 64, 64))
     return cudaErrorInvalidValue;
@@ -702,8 +703,8 @@ cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   p.ctl = a.ws.ctl;
   p.N = a.D;
   p.Kdim = a.F;
-  const int tiles = ((a.T + BM - 1) / BM) * ((a.D + 127) / 128);
-  return launch_tc<128, 1, true, EPI_DOWN>(mh, mh, md, md, p, tiles, s);
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.D + 255) / 256);
+  return launch_tc<256, 1, true, EPI_DOWN>(mh, mh, md, md, p, tiles, s);
 }
 
 // Test hook: fp32 C[M][N] = A[M][K] B^T (B [N][K], b_mn = 0) or A B (B [K][N],
