@@ -40,7 +40,7 @@ namespace {
 constexpr int BM = 128, BK = 64, NTHREADS = 192;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3 };
+enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4 };
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -189,7 +189,9 @@ struct Cfg {
                                                                                          : 512;
   // EPI_PACK: per row idx (32 B) + bf16 val (64 B) slots, K <= 32, and a
   // 32-column bf16 staging row (64 B)
-  static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64 : 0;
+  static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64
+                                    : EPI == EPI_U  ? 128 * 64  // a 32-column bf16 g row
+                                                    : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
   static_assert(STAGES >= 2, "too few stages");
   static_assert(TMEM_COLS_USED <= 512, "TMEM overflow");
@@ -517,6 +519,72 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             }
           }
         }
+      } else if (EPI == EPI_U) {
+        // Dense-path rows of the gated FFN with B = W_up only: g is not
+        // recomputed but read back from what the gate epilogue stored (the
+        // bf16 value of every active entry: the wide tile of an overflowing
+        // (row, tile), else the TwELL slots), so this GEMM does half the work
+        // of the gate + up one.  Stores as EPI_GU.
+        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
+        const int ps = row_ok ? (dense_all ? p.pos[tok] : m) : -1;
+        const bool fb_ok = ps >= 0 && ps < p.cap;
+        const int K = p.Kslots;
+        bf16 *gz = (bf16 *)s_slots + row * 32;  // this row's g for the current 32 columns
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float zu[32];
+          tmem_ld32(tacc + c0, zu);
+          if (!row_ok || n0 + c0 >= p.N) continue;
+          const int j = (n0 + c0) / p.C, cl = (n0 + c0) % p.C;
+          const size_t jt = (size_t)j * p.Tn + tok;
+          const int nz = p.nnz[jt];
+          if (nz > K) {
+            const uint4 *wr = (const uint4 *)(p.wide + jt * p.C + cl);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) ((uint4 *)gz)[v4] = wr[v4];
+          } else {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < nz; ++k) {
+              const int c = p.idx[jt * K + k] - cl;
+              if (c >= 0 && c < 32) gz[c] = p.val[jt * K + k];
+            }
+          }
+          uint32_t hw[16], uw[16];
+          const uint4 *g4 = (const uint4 *)gz;
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const uint4 gv = g4[v4];
+            const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+              const int i = 8 * v4 + 2 * q2;
+              const float g0 = bf_lo(gp[q2]), g1 = bf_hi(gp[q2]);
+              hw[i / 2] = pack_bf2(g0 * zu[i], g1 * zu[i + 1]);
+              uw[i / 2] = pack_bf2(zu[i], zu[i + 1]);
+            }
+          }
+          uint4 *hd = (uint4 *)(p.h + (size_t)m * p.F + n0 + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+          if (dense_all && p.train) {  // u at the slots of non-overflow rows
+            uint4 *ur = (uint4 *)(p.urows + (size_t)m * p.F + n0 + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              ur[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+          }
+          if (fb_ok) {
+            uint4 *gd = (uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) gd[v4] = g4[v4];
+            if (p.train) {
+              uint4 *ud = (uint4 *)(p.u_fb + (size_t)ps * p.F + n0 + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                ud[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+            }
+          }
+        }
       } else if (EPI == EPI_DOWN) {
         const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -686,8 +754,13 @@ cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
   p.ctl = a.ws.ctl;
   p.N = a.F;
   p.Kdim = a.D;
+  if (a.gated) {  // up only (g from the stored TwELL / wide tiles), 128 x 256 tiles
+    CUtensorMap mu256;
+    if (!make_map(&mu256, a.Wu, a.D, a.F, 64, 256)) return cudaErrorInvalidValue;
+    const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 255) / 256);
+    return launch_tc<256, 1, false, EPI_U>(mxg, mx, mu256, mu256, p, tiles, s);
+  }
   const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 127) / 128);
-  if (a.gated) return launch_tc<128, 2, false, EPI_GU>(mxg, mx, mg, mu, p, tiles, s);
   return launch_tc<128, 1, false, EPI_GU>(mxg, mx, mg, mg, p, tiles, s);
 }
 
