@@ -43,8 +43,16 @@ struct BParams {
   float4 *col_e;             // transposed entries {token bits, dz, du, h}
   void *dx;
   float *dWg, *dbg, *dWu, *dWd;
+  int gemm_rows;             // 1: the dense-path rows go through the tensor-core GEMMs
   int32_t *status;
 };
+
+// Rows that the tensor-core GEMMs handle (every row in all-dense mode, the
+// overflow rows when they take the dense GEMM path): the gather kernels skip
+// them.
+__device__ __forceinline__ bool gemm_row(const BParams &p, int ps) {
+  return p.gemm_rows && (p.ctl->dense || (p.ctl->ovf_gemm && ps >= 0));
+}
 
 __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
 
@@ -142,6 +150,7 @@ __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p)
   const int NV = p.D / EV;
   const int ps = p.pos[t];
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
+  if (gemm_row(p, ps)) return;
   for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
   const uint4 *Wd4 = (const uint4 *)p.Wd;
   const PairSource<T> src = bwd_source<T>(p, t, ps);
@@ -209,6 +218,7 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
   const int CPW = NV / (4 * DH_WARPS);  // 32-element chunks per warp (NV % 32 == 0)
   const int ps = p.pos[t];
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
+  if (gemm_row(p, ps)) return;
   for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
   const uint4 *Wd4 = (const uint4 *)p.Wd;
   const uint4 *dyw = s_dy + 4 * w * CPW + q;  // this lane's dy vectors (read by lanes 0-3)
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
   const int ps = p.pos[t];
-  if (ps >= p.cap) return;
+  if (ps >= p.cap || gemm_row(p, ps)) return;
   float2 dxg[VPT][EV / 2], dxu[VPT][EV / 2];  // two accumulator chains
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
@@ -384,7 +394,7 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_count_kernel(BParams p) {
   for (int c = tid; c < C; c += blockDim.x) cnt[c] = 0;
   __syncthreads();
   const int t = ch * TR_CHUNK + tid;
-  if (t < Tn && p.pos[t] < 0) {
+  if (t < Tn && p.pos[t] < 0 && !(p.gemm_rows && p.ctl->dense)) {
     const int n = p.nnz[(size_t)j * Tn + t];
     const size_t s0 = ((size_t)j * Tn + t) * K;
     for (int k = 0; k < n && k < K; ++k) {
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
   }
   const unsigned lt = (1u << lane) - 1u;
   const int t = ch * TR_CHUNK + tid;
-  const bool act = t < Tn && p.pos[t] < 0;
+  const bool act = t < Tn && p.pos[t] < 0 && !(p.gemm_rows && p.ctl->dense);
   const int n = act ? (int)p.nnz[(size_t)j * Tn + t] : 0;
   const size_t s0 = ((size_t)j * Tn + (act ? t : 0)) * K;
   for (int k = 0; k < n && k < K; ++k) {
@@ -485,6 +495,7 @@ template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
   constexpr int EV = Vec<T>::EV;
   __shared__ float4 s_e[DW_LIST];
+  if (p.gemm_rows && p.ctl->dense) return;  // the GEMMs write every row
   const int n = blockIdx.x, tid = threadIdx.x;
   const int NV = p.D / EV;
   const uint4 *x4 = (const uint4 *)p.x, *dy4 = (const uint4 *)p.dy;
@@ -533,8 +544,8 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
       }
     }
   }
-  // overflow rows (dense backup)
-  const int n_rows = min(p.ctl->n_ovf, p.cap);
+  // overflow rows (dense backup), unless the GEMMs add them afterwards
+  const int n_rows = (p.gemm_rows && p.ctl->ovf_gemm) ? 0 : min(p.ctl->n_ovf, p.cap);
   const T *gfb = (const T *)p.g_fb;
   for (int i = 0; i < n_rows; ++i) {
     if (!(to_f(gfb[(size_t)i * p.F + n]) > 0.f)) continue;
@@ -579,15 +590,32 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   p.col_start = a.ws.col_ptr; p.col_cnt = a.ws.col_cnt; p.col_e = a.ws.col_e; p.col_chunk = a.ws.col_chunk;
   p.dx = a.dx; p.dWg = a.dWg; p.dbg = a.dbg; p.dWu = a.dWu; p.dWd = a.dWd;
   p.status = a.tw.status;
+  const bool bf = a.dtype == TWELL_BF16;
+  const bool gemm = bf && tc_available();
+  p.gemm_rows = gemm ? 1 : 0;
 
-  // 1. hybrid split of the saved activations into this workspace
+  // 1. hybrid split of the saved activations into this workspace, with the
+  // forward's dispatcher rules when the dense-path rows have GEMMs
+  prof_mark(KID_START, s);
   cudaError_t e = launch_flags_from_nnz(a.tw, a.ws, s);
   if (e != cudaSuccess) return e;
-  prof_mark(KID_START, s);
-  e = launch_overflow_compact(a.tw, &a.ws, 2.0f, s, /*write_user=*/false);
+  e = launch_overflow_compact(a.tw, &a.ws, gemm ? a.dense_switch : 2.0f, s, /*write_user=*/false,
+                              gemm ? a.dense_density : -1.f);
   if (e != cudaSuccess) return e;
-  prof_mark(KID_OVERFLOW_COMPACT, s);
-  const bool bf = a.dtype == TWELL_BF16;
+  prof_mark(KID_OVERFLOW_COMPACT, s, 2);
+  // 1'. dense-path rows on the tensor cores (idle when there are none):
+  // gathered dy / x rows, dh -> dz / du / h, dx
+  if (gemm) {
+    e = launch_bwd_prep_rows(a, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_BWD_PREP, s);
+    e = launch_tc_bwd_dh(a, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_BWD_DENSE, s);
+    e = launch_tc_bwd_dx(a, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_BWD_DENSE_DX, s);
+  }
   // 2. per-token dh SDDMM (slots / overflow rows), then dx SpMM
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
@@ -653,13 +681,18 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prof_mark(KID_BWD_TRANSPOSE, s);
+  prof_mark(KID_BWD_TRANSPOSE, s, 2);
   // 4. weight gradients
   if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F);
   else TW_VPT(bwd_dw_kernel, float, a.F);
 #undef TW_VPT
   e = cudaGetLastError();
   prof_mark(KID_BWD_DW, s);
+  // 5. weight gradients of the dense-path rows (added to those of step 4)
+  if (e == cudaSuccess && gemm) {
+    e = launch_tc_bwd_dw(a, s);
+    prof_mark(KID_BWD_DENSE_DW, s);
+  }
   return e;
 }
 

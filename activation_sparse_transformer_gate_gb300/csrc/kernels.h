@@ -17,10 +17,13 @@ struct Workspace {
   uint32_t *ovf_bits; // [ceil(T/32)] overflow-row bitmap (set by the gate epilogue)
   int32_t *rows;      // [T] rows of the dense path (hybrid: overflow rows)
   int32_t *pos;       // [T] overflow position of each row, -1 if none
-  void *h;            // [T][F] dtype: h rows of the dense path
-  void *xg;           // [T][D] dtype: gathered x rows of the dense path
+  // (the row buffers hold Tp = T rounded up to 128 rows)
+  void *h;            // [Tp][F] dtype: h rows of the dense path
+  void *xg;           // [Tp][D] dtype: gathered x rows of the dense path
   void *wide;         // [F/C][T][C] dtype: full ReLU(z) of overflowing (tile, row)s
-  void *urows;        // [T][F] dtype (training): u rows from the dense path
+  void *urows;        // [Tp][F] dtype (training): u rows from the dense path
+  void *dyg;          // [Tp][D] dtype (training): gathered dy rows of the dense path
+  float *dbg_r;       // [F] fp32 (training): dbg of the dense-path rows
   // backward scratch
   float *dz;          // [F/C][T][K] fp32: dz at the slots
   float *du;          // [F/C][T][K] fp32: du at the slots
@@ -29,9 +32,10 @@ struct Workspace {
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
   float4 *col_e;      // [T*(F/C)*K] transposed entries {token (int bits), dz, du, h}
   int32_t *col_chunk; // [(F/C) * ceil(T/1024) * C] per-(tile, token chunk) column counts
-  float *dzr;         // [T][F] fp32: dz rows of the overflow rows
-  float *dur;         // [T][F] fp32: du rows of the overflow rows
-  float *hr;          // [T][F] fp32: h rows of the overflow rows
+  float *dzr;         // [T][F] fp32: dz rows of the overflow rows (gather path), or
+                      // [2 Tp][F] bf16: dz hi rows then lo rows (tensor-core rows)
+  float *dur;         // the same for du
+  float *hr;          // the same for h
   size_t bytes;       // total bytes needed
 };
 
@@ -57,6 +61,7 @@ struct BwdArgs {
   void *dx;
   float *dWg, *dbg, *dWu, *dWd;
   Workspace ws;
+  float dense_switch, dense_density;  // dispatcher of the dense-path rows (as the forward's)
 };
 
 // pack.cu
@@ -81,8 +86,14 @@ cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s);
 // All-dense training forward: u at the slots of the non-overflow rows.
 cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s);
+// dst[m] = src[rows[m]] for the m < n_rows overflow rows of the dense GEMM
+// path (none in all-dense mode), zeros for the rows up to the next multiple
+// of 128 (dst holds T rounded up to 128 rows).
 cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
                                int dtype, cudaStream_t s);
+// Backward, dense-path rows (bf16): zeroes ws.dbg_r and, for overflow rows on
+// the GEMMs, gathers their dy and x rows into ws.dyg / ws.xg.
+cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s);
 
 // simt_gemm.cu (fp32 path)
 cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s);
@@ -94,6 +105,9 @@ bool tc_available();
 cudaError_t launch_tc_gate_pack(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s);
 
 // Kernel identities for the optional per-launch timing (twell_profile_*).
 enum KernelId {
@@ -113,10 +127,14 @@ enum KernelId {
   KID_BWD_DENSE = 12,
   KID_FILL_U = 13,
   KID_ASSEMBLE_FB = 14,
-  KID_COUNT = 15
+  KID_BWD_DENSE_DX = 15,
+  KID_BWD_DENSE_DW = 16,
+  KID_BWD_PREP = 17,
+  KID_COUNT = 18
 };
-// Record a timing event after a launch of kernel `id` (no-op unless enabled).
-void prof_mark(int id, cudaStream_t s);
+// Record a timing event after `launches` kernel launches of component `id`
+// (no-op unless enabled).
+void prof_mark(int id, cudaStream_t s, int launches = 1);
 
 // updown.cu
 cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);

@@ -222,25 +222,35 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
   return cudaGetLastError();
 }
 
-// Overflow-row bitmap from nnz: one thread per (tile, row).
+// Overflow-row bitmap from nnz (a thread per (tile, row)), and the number of
+// slots in use, sum of min(nnz, K), as the gate epilogue counts it.
 __global__ void flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, long total, int Tn, int K,
-                                      uint32_t *__restrict__ bits) {
+                                      uint32_t *__restrict__ bits,
+                                      unsigned long long *__restrict__ slots) {
+  unsigned long long mine = 0;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long)gridDim.x * blockDim.x) {
-    if (nnz[i] > K) {
+    const int c = nnz[i];
+    if (c > K) {
       const int t = (int)(i % Tn);
       atomicOr(&bits[t >> 5], 1u << (t & 31));
     }
+    mine += (unsigned long long)(c < K ? c : K);
   }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mine += __shfl_down_sync(0xffffffffu, mine, o);
+  if ((threadIdx.x & 31) == 0 && mine) atomicAdd(slots, mine);
 }
 
 cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(ws.ovf_bits, 0, 4 * (((size_t)tw.T + 31) / 32), s);
+  cudaError_t e = cudaMemsetAsync(ws.ctl, 0, sizeof(Ctl), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.ovf_bits, 0, 4 * (((size_t)tw.T + 31) / 32), s);
   if (e != cudaSuccess) return e;
   const long total = (long)tw.T * (tw.F / tw.C);
-  long blocks = (total + 255) / 256;  // usually idle (all-dense mode only)
+  long blocks = (total + 255) / 256;
   if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
-  flags_from_nnz_kernel<<<(unsigned)blocks, 256, 0, s>>>(tw.nnz, total, tw.T, tw.K, ws.ovf_bits);
+  flags_from_nnz_kernel<<<(unsigned)blocks, 256, 0, s>>>(tw.nnz, total, tw.T, tw.K, ws.ovf_bits,
+                                                         &ws.ctl->slots);
   return cudaGetLastError();
 }
 
@@ -268,16 +278,22 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
 }
 
 // dst[m] = src[rows[m]] for the overflow rows when they take the dense GEMM
-// path (in all-dense mode the GEMMs read src directly).
+// path (in all-dense mode the GEMMs read src directly), then zero rows up to
+// the next multiple of 128: a GEMM that contracts over these rows reads them.
 __global__ void gather_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                    int row_vecs, const Ctl *__restrict__ ctl,
                                    const int32_t *__restrict__ rows) {
   if (ctl->dense || !ctl->ovf_gemm) return;
   const int n = ctl->n_rows;
-  for (int m = blockIdx.x; m < n; m += gridDim.x) {
-    const uint4 *a = src + (size_t)rows[m] * row_vecs;
+  const int npad = (n + 127) / 128 * 128;
+  for (int m = blockIdx.x; m < npad; m += gridDim.x) {
     uint4 *b = dst + (size_t)m * row_vecs;
-    for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) b[v] = a[v];
+    if (m < n) {
+      const uint4 *a = src + (size_t)rows[m] * row_vecs;
+      for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) b[v] = a[v];
+    } else {
+      for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) b[v] = make_uint4(0, 0, 0, 0);
+    }
   }
 }
 
@@ -372,6 +388,42 @@ cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s) {
     fill_u_slots_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
         a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const float *)a.ws.urows, (float *)a.tw.u_val,
         a.T, a.F, a.C, a.K);
+  return cudaGetLastError();
+}
+
+// Backward, dense-path rows (all rows in all-dense mode, else the overflow
+// rows when they take the GEMMs): zero the dbg partial sums, and in the
+// overflow-row case gather the dy and x rows (zero rows up to the next
+// multiple of 128).  One launch, idle when there are no such rows.
+__global__ void bwd_prep_rows_kernel(const Ctl *__restrict__ ctl, const int32_t *__restrict__ rows,
+                                     const uint4 *__restrict__ dy, const uint4 *__restrict__ x,
+                                     uint4 *__restrict__ dyg, uint4 *__restrict__ xg,
+                                     float *__restrict__ dbg_r, int row_vecs, int F) {
+  const int n = ctl->n_rows;
+  if (n == 0) return;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < F; i += gridDim.x * blockDim.x)
+    dbg_r[i] = 0.f;
+  if (ctl->dense) return;  // the GEMMs read dy and x in place
+  const int npad = (n + 127) / 128 * 128;
+  for (int m = blockIdx.x; m < npad; m += gridDim.x) {
+    uint4 *a = dyg + (size_t)m * row_vecs, *b = xg + (size_t)m * row_vecs;
+    if (m < n) {
+      const uint4 *sa = dy + (size_t)rows[m] * row_vecs, *sb = x + (size_t)rows[m] * row_vecs;
+      for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
+        a[v] = sa[v];
+        b[v] = sb[v];
+      }
+    } else {
+      for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) a[v] = b[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s) {
+  const int blocks = a.T < 2 * num_sms() ? a.T : 2 * num_sms();
+  bwd_prep_rows_kernel<<<blocks, 256, 0, s>>>(a.ws.ctl, a.ws.rows, (const uint4 *)a.dy,
+                                              (const uint4 *)a.x, (uint4 *)a.ws.dyg,
+                                              (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F);
   return cudaGetLastError();
 }
 

@@ -4,7 +4,14 @@
 //   EPI_GU   : dual B (Wg, Wu): g = ReLU(z) rounded to bf16, u, h = g*u
 //              -> h rows (+ g_fb / u_fb rows of overflow rows)       (dense rows)
 //   EPI_DOWN : y[tok] = h Wd, Wd read MN-major straight from [F][D]   (dense rows)
-//   EPI_F32  : plain fp32 C = A B^T or A B (test hook)
+//   EPI_U    : B = Wu only, g read back from the TwELL slots / wide tiles
+//   EPI_DH   : dh = dy Wd^T + lambda sign(h) -> dz, du, h rows (bf16 hi +
+//              lo parts) and column sums of dz                    (bwd rows)
+//   EPI_DX   : dx[tok] = dz Wg + du Wu (K ranges over the hi and lo parts,
+//              B MN-major)                                        (bwd rows)
+//   EPI_DW   : dW = A^T B with A, B both MN-major (token axis = K, hi and lo
+//              parts of A), fp32 rows stored or added             (bwd rows)
+//   EPI_F32  : plain fp32 C = A B^T, A B or A^T B (test hook)
 //
 // "Sparser, Faster, Lighter Transformer Language Models", technical summary
 // section 2.A: TwELL is materialised in the epilogue of an optimised dense
@@ -40,7 +47,8 @@ namespace {
 constexpr int BM = 128, BK = 64, NTHREADS = 192;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4 };
+enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4, EPI_DH = 5, EPI_DX = 6,
+           EPI_DW = 7 };
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -113,10 +121,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: D=f32, A=B=bf16, A K-major, B K- or
-// MN-major, N>>3 at bit 17, M>>4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+// Instruction descriptor, kind::f16: D=f32, A=B=bf16, A and B each K- or
+// MN-major (bits 15 and 16), N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -154,30 +162,124 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The K slots of one (row, tile) with vector loads (K in {1,2,4,8,16,32}; a
+// slot row starts at a multiple of its own size, so each load is aligned):
+// load_idx gives the idx bytes, load_vals the bf16 value pairs; words past
+// the slots are zero.
+__device__ __forceinline__ void load_idx(const uint8_t *ip, int K, uint32_t (&iw)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) iw[i] = 0u;
+  if (K >= 16) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (q * 16 < K) {
+        const uint4 a = ((const uint4 *)ip)[q];
+        iw[4 * q] = a.x; iw[4 * q + 1] = a.y; iw[4 * q + 2] = a.z; iw[4 * q + 3] = a.w;
+      }
+  } else if (K == 8) {
+    const uint2 a = *(const uint2 *)ip;
+    iw[0] = a.x; iw[1] = a.y;
+  } else if (K == 4) {
+    iw[0] = *(const uint32_t *)ip;
+  } else if (K == 2) {
+    iw[0] = *(const uint16_t *)ip;
+  } else {
+    iw[0] = *ip;
+  }
+}
+
+__device__ __forceinline__ void load_vals(const bf16 *vp, int K, uint32_t (&vw)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) vw[i] = 0u;
+  if (K >= 8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q * 8 < K) {
+        const uint4 a = ((const uint4 *)vp)[q];
+        vw[4 * q] = a.x; vw[4 * q + 1] = a.y; vw[4 * q + 2] = a.z; vw[4 * q + 3] = a.w;
+      }
+  } else if (K == 4) {
+    const uint2 a = *(const uint2 *)vp;
+    vw[0] = a.x; vw[1] = a.y;
+  } else if (K == 2) {
+    vw[0] = *(const uint32_t *)vp;
+  } else {
+    vw[0] = *(const uint16_t *)vp;
+  }
+}
+
+__device__ __forceinline__ void load_slots(const uint8_t *ip, const bf16 *vp, int K,
+                                           uint32_t (&iw)[8], uint32_t (&vw)[16]) {
+  load_idx(ip, K, iw);
+  load_vals(vp, K, vw);
+}
+
+// Slot k's local column and bf16 value bits from the words of load_slots.
+__device__ __forceinline__ int slot_col(const uint32_t (&iw)[8], int k) {
+  return (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+}
+__device__ __forceinline__ unsigned short slot_val(const uint32_t (&vw)[16], int k) {
+  return (unsigned short)(vw[k >> 1] >> (16 * (k & 1)));
+}
+
+// 32 fp32 values as bf16 hi (RNE) and lo = bf16(v - hi) parts, 64 bytes each.
+__device__ __forceinline__ void store_hi_lo(bf16 *hi, bf16 *lo, const float (&v)[32]) {
+  uint32_t hw[16], lw[16];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint32_t hp = pack_bf2(v[i], v[i + 1]);
+    hw[i / 2] = hp;
+    lw[i / 2] = pack_bf2(v[i] - bf_lo(hp), v[i + 1] - bf_hi(hp));
+  }
+  uint4 *h4 = (uint4 *)hi, *l4 = (uint4 *)lo;
+#pragma unroll
+  for (int v4 = 0; v4 < 4; ++v4) {
+    h4[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+    l4[v4] = make_uint4(lw[4 * v4], lw[4 * v4 + 1], lw[4 * v4 + 2], lw[4 * v4 + 3]);
+  }
+}
+
 __device__ __forceinline__ void epi_bar() {  // named barrier of the 4 epilogue warps
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 // --------------------------------------------------------------- params --
+// Operand tensor maps.  a[0] / b[0]: gathered rows (dense-path rows of the
+// hybrid), a[1] / b[1]: the operand in place (all-dense mode), or the second
+// operand (EPI_GU: W_up; EPI_DX: du and W_up).  EPI_DW: A of problem q is
+// a[q]; B is b[0] / b[1] (x), or b[2] / b[3] (dy) for the last problem.
+struct TcMaps {
+  CUtensorMap a[3];
+  CUtensorMap b[4];
+};
+
 struct TcParams {
   int M_host;              // rows when m_dev == nullptr
   const int32_t *m_dev;    // device row count (dense path: ctl->n_rows)
+  const int32_t *k_dev;    // device contraction length (EPI_DW: ctl->n_rows), else Kdim
   const Ctl *ctl;          // dense-path control (EPI_GU / EPI_DOWN), else null
   int N, Kdim;             // output columns, contraction length
   int Tn, F, D, C, Kslots, cap, gated, train;
+  int Tp;                  // backward: rows of a hi part (T rounded up to 128)
   const float *bg, *rb;
   const int32_t *rows, *pos;
   uint8_t *idx, *nnz;
   uint32_t *ovf_bits;
   unsigned long long *slots;  // EPI_PACK: total slots written (the dispatcher's density)
-  bf16 *val;
+  bf16 *val, *uval;         // uval: u at the slots (backward)
   bf16 *h, *g_fb, *u_fb, *y;
   bf16 *wide, *urows;
-  float *out;              // EPI_F32
+  float *out;              // EPI_F32, EPI_DW
+  float lambda;            // EPI_DH: L1 coefficient
+  bf16 *dz2, *du2, *h2;    // EPI_DH outputs, [2 Tp][F]: hi rows, then lo rows
+  float *dbg_r;            // EPI_DH: column sums of dz (zeroed before); EPI_DW: added to dbg_out
+  float *dbg_out;          // EPI_DW: dbg (added from dbg_r with the W_gate problem)
+  float *outq[3];          // EPI_DW: the fp32 output of each problem (dWg, [dWu,] dWd)
+  int nq;                  // EPI_DW: problems in the launch
   int32_t *status;
 };
 
-template <int BN, int NB, bool B_MN, int EPI>
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -190,7 +292,8 @@ struct Cfg {
   // EPI_PACK: per row idx (32 B) + bf16 val (64 B) slots, K <= 32, and a
   // 32-column bf16 staging row (64 B)
   static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64
-                                    : EPI == EPI_U  ? 128 * 64  // a 32-column bf16 g row
+                                    : EPI == EPI_U  ? 128 * 64   // a 32-column bf16 g row
+                                    : EPI == EPI_DH ? 128 * 128  // and g, u rows
                                                     : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
   static_assert(STAGES >= 2, "too few stages");
@@ -199,12 +302,10 @@ struct Cfg {
 
 }  // namespace
 
-template <int BN, int NB, bool B_MN, int EPI>
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
-               const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
-               TcParams p) {
-  using CF = Cfg<BN, NB, B_MN, EPI>;
+tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
+  using CF = Cfg<BN, NB, B_MN, EPI, A_MN>;
   constexpr int S = CF::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -226,9 +327,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const bool dense_all = p.ctl ? p.ctl->dense != 0 : false;
   const int m_blocks = (M + BM - 1) / BM;
   const int n_blocks = (p.N + BN - 1) / BN;
-  const int num_tiles = m_blocks * n_blocks;
-  const int KT = (p.Kdim + BK - 1) / BK;
-  if ((int)blockIdx.x >= num_tiles) return;  // uniform for the CTA
+  const int NQ = EPI == EPI_DW ? p.nq : 1;  // independent problems of one shape
+  const int tiles_q = m_blocks * n_blocks;
+  const int num_tiles = NQ * tiles_q;
+  // The backward GEMMs contract over several K ranges of KT1 k-blocks each:
+  // an operand rounded to bf16 is split into hi + lo parts (rows m and
+  // p.Tp + m of its buffer), each multiplied by the same other operand.
+  //   EPI_DX: dz_hi Wg, dz_lo Wg, du_hi Wu, du_lo Wu (plain FFN: the first two)
+  //   EPI_DW: A_hi B, A_lo B
+  const int Kd = p.k_dev ? *p.k_dev : p.Kdim;
+  const int KT1 = (Kd + BK - 1) / BK;
+  const int NR = EPI == EPI_DX ? (p.gated ? 4 : 2) : (EPI == EPI_DW ? 2 : 1);
+  const int KT = NR * KT1;
+  if ((int)blockIdx.x >= num_tiles || KT == 0) return;  // uniform for the CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -258,13 +369,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      const CUtensorMap *amap = (p.ctl && dense_all) ? &mapA2 : &mapA;
+      // all-dense mode reads the operand in place (a[1] / b[1]), otherwise
+      // the gathered rows (a[0] / b[0])
+      const CUtensorMap *amap0 = (EPI != EPI_DX && p.ctl && dense_all) ? &maps.a[1] : &maps.a[0];
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mb = tile / n_blocks, nb = tile % n_blocks;
+        const int q = tile / tiles_q, tq = tile - q * tiles_q;
+        const int mb = tq / n_blocks, nb = tq % n_blocks;
+        // EPI_DW: this problem's A, and B = x (or dy for the last problem)
+        const CUtensorMap *aq = EPI == EPI_DW ? &maps.a[q] : amap0;
+        const int bq = (EPI == EPI_DW && q == NQ - 1) ? 2 : 0;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -273,17 +390,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           const uint32_t sbase = smem_u32(stages + stage * CF::STAGE_BYTES);
           const uint32_t fb = full0 + 8 * stage;
           mbar_expect_tx(fb, CF::STAGE_BYTES);
-          tma_load_2d(sbase, amap, kt * BK, mb * BM, fb);
+          const int r = NR > 1 ? kt / KT1 : 0;   // K range
+          const int kc = (kt - r * KT1) * BK;     // k within the range
+          const int lo = (r & 1) ? p.Tp : 0;      // row offset of a lo part
+          const bool second = EPI == EPI_DX && r >= 2;
+          const CUtensorMap *amap = second ? &maps.a[1] : aq;
+          if (A_MN) {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(sbase + i * (64 * BK * 2), amap, mb * BM + 64 * i, kc + lo, fb);
+          } else {
+            tma_load_2d(sbase, amap, kc, mb * BM + lo, fb);
+          }
 #pragma unroll
           for (int op = 0; op < NB; ++op) {
-            const CUtensorMap *bm = op == 0 ? &mapB0 : &mapB1;
+            const CUtensorMap *bm =
+                &maps.b[bq + ((op == 1 || second || (EPI == EPI_DW && dense_all)) ? 1 : 0)];
             const uint32_t bbase = sbase + CF::A_BYTES + op * CF::B_BYTES;
             if (B_MN) {
 #pragma unroll
               for (int i = 0; i < BN / 64; ++i)
-                tma_load_2d(bbase + i * (64 * BK * 2), bm, nb * BN + 64 * i, kt * BK, fb);
+                tma_load_2d(bbase + i * (64 * BK * 2), bm, nb * BN + 64 * i, kc, fb);
             } else {
-              tma_load_2d(bbase, bm, kt * BK, nb * BN, fb);
+              tma_load_2d(bbase, bm, kc, nb * BN, fb);
             }
           }
           ++issued;
@@ -308,7 +437,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t IDESC = make_idesc(BM, BN, B_MN);
+      constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
@@ -328,7 +457,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           const uint32_t sbase = smem_u32(stages + stage * CF::STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sw128_desc(sbase + kk * 32, 16, 1024);
+            // (an MN-major A tile is laid out as an MN-major B tile: see below)
+            const uint64_t ad = A_MN ? sw128_desc(sbase + kk * 2048, 64 * BK * 2, 1024)
+                                     : sw128_desc(sbase + kk * 32, 16, 1024);
 #pragma unroll
             for (int op = 0; op < NB; ++op) {
               const uint32_t bbase = sbase + CF::A_BYTES + op * CF::B_BYTES;
@@ -362,7 +493,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const int et = threadIdx.x - 64;        // 0..127 among epilogue threads
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-      const int mb = tile / n_blocks, nb = tile % n_blocks;
+      const int q = tile / tiles_q, tq = tile - q * tiles_q;
+      const int mb = tq / n_blocks, nb = tq % n_blocks;
       const int buf = lt & 1;
       const uint32_t use = (uint32_t)(lt >> 1);
       const int n0 = nb * BN;
@@ -530,13 +662,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         const bool fb_ok = ps >= 0 && ps < p.cap;
         const int K = p.Kslots;
         bf16 *gz = (bf16 *)s_slots + row * 32;  // this row's g for the current 32 columns
+        // the slots of the current (row, tile), loaded once per tile with
+        // vector loads: idx bytes and bf16 values
+        int cur_j = -1, nz = 0;
+        uint32_t iw[8], vw[16];
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float zu[32];
           tmem_ld32(tacc + c0, zu);
           if (!row_ok || n0 + c0 >= p.N) continue;
           const int j = (n0 + c0) / p.C, cl = (n0 + c0) % p.C;
           const size_t jt = (size_t)j * p.Tn + tok;
-          const int nz = p.nnz[jt];
+          if (j != cur_j) {
+            cur_j = j;
+            nz = p.nnz[jt];
+            if (nz <= K) load_slots(p.idx + jt * K, p.val + jt * K, K, iw, vw);
+          }
           if (nz > K) {
             const uint4 *wr = (const uint4 *)(p.wide + jt * p.C + cl);
 #pragma unroll
@@ -544,9 +684,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           } else {
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
-            for (int k = 0; k < nz; ++k) {
-              const int c = p.idx[jt * K + k] - cl;
-              if (c >= 0 && c < 32) gz[c] = p.val[jt * K + k];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (k < nz) {
+                const int c = slot_col(iw, k) - cl;
+                if ((unsigned)c < 32u) gz[c] = __ushort_as_bfloat16(slot_val(vw, k));
+              }
             }
           }
           uint32_t hw[16], uw[16];
@@ -585,7 +728,137 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             }
           }
         }
-      } else if (EPI == EPI_DOWN) {
+      } else if (EPI == EPI_DH) {
+        // Backward of the dense-path rows.  g and u of the row come from what
+        // the forward saved: the dense backup rows of an overflow row, else
+        // the TwELL slots (g) and u at the slots, loaded once per tile with
+        // vector loads.  dz, du and h = g u are computed in fp32 and stored
+        // as bf16 hi + lo parts (v = hi + lo to about 2^-17 relative: the
+        // GEMMs that take them as operands then lose no more than the fp32
+        // gather path), hi at row m and lo at row Tp + m of p.dz2 / p.du2 /
+        // p.h2.  Rows past the last one (inside this tile) are written as
+        // zeros: the weight-gradient GEMMs contract over them.
+        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
+        const int ps = row_ok ? p.pos[tok] : -1;
+        const int K = p.Kslots;
+        bf16 *gz = (bf16 *)s_slots + row * 64, *uz = gz + 32;  // g, u of 32 columns
+        int cur_j = -1, nz = 0;
+        uint32_t iw[8], vw[16], qw[16];
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(tacc + c0, v);
+          if (n0 + c0 >= p.N) continue;  // uniform (F is a multiple of 32)
+          const size_t o = (size_t)m * p.F + n0 + c0, ol = o + (size_t)p.Tp * p.F;
+          float dz[32], du[32], hv[32];
+          if (row_ok) {
+            uint32_t ga[16], ua[16];  // bf16 pairs of g and u (plain FFN: u = 1)
+            if (ps >= 0) {  // overflow row: backup rows (none past the capacity: zeros)
+              const bool ok = ps < p.cap;
+              const uint4 *gr = (const uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
+              const uint4 *ur = (const uint4 *)(p.u_fb + (size_t)ps * p.F + n0 + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const uint4 gv = ok ? gr[v4] : make_uint4(0, 0, 0, 0);
+                const uint4 uv = (ok && p.gated) ? ur[v4] : make_uint4(0, 0, 0, 0);
+                ga[4 * v4] = gv.x; ga[4 * v4 + 1] = gv.y; ga[4 * v4 + 2] = gv.z; ga[4 * v4 + 3] = gv.w;
+                ua[4 * v4] = uv.x; ua[4 * v4 + 1] = uv.y; ua[4 * v4 + 2] = uv.z; ua[4 * v4 + 3] = uv.w;
+              }
+            } else {  // slots (every tile of the row holds at most K)
+              const int j = (n0 + c0) / p.C, cl = (n0 + c0) % p.C;
+              const size_t jt = (size_t)j * p.Tn + tok;
+              if (j != cur_j) {
+                cur_j = j;
+                nz = min((int)p.nnz[jt], K);
+                load_slots(p.idx + jt * K, p.val + jt * K, K, iw, vw);
+                if (p.gated) load_vals(p.uval + jt * K, K, qw);
+              }
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
+                ((uint4 *)uz)[v4] = make_uint4(0, 0, 0, 0);
+              }
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                if (k < nz) {
+                  const int c = slot_col(iw, k) - cl;
+                  if ((unsigned)c < 32u) {
+                    gz[c] = __ushort_as_bfloat16(slot_val(vw, k));
+                    if (p.gated) uz[c] = __ushort_as_bfloat16(slot_val(qw, k));
+                  }
+                }
+              }
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const uint4 gv = ((const uint4 *)gz)[v4], uv = ((const uint4 *)uz)[v4];
+                ga[4 * v4] = gv.x; ga[4 * v4 + 1] = gv.y; ga[4 * v4 + 2] = gv.z; ga[4 * v4 + 3] = gv.w;
+                ua[4 * v4] = uv.x; ua[4 * v4 + 1] = uv.y; ua[4 * v4 + 2] = uv.z; ua[4 * v4 + 3] = uv.w;
+              }
+            }
+            if (!p.gated) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ua[i] = 0x3F803F80u;  // u = 1
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = (i & 1) ? bf_hi(ga[i / 2]) : bf_lo(ga[i / 2]);
+              const float u = (i & 1) ? bf_hi(ua[i / 2]) : bf_lo(ua[i / 2]);
+              const float h = p.gated ? g * u : g;
+              const float dh = v[i] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
+              const bool act = g > 0.f;
+              dz[i] = act ? (p.gated ? dh * u : dh) : 0.f;
+              du[i] = act ? dh * g : 0.f;
+              hv[i] = h;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dz[i] = du[i] = hv[i] = 0.f;
+          }
+          store_hi_lo(p.dz2 + o, p.dz2 + ol, dz);
+          if (p.gated) store_hi_lo(p.du2 + o, p.du2 + ol, du);
+          store_hi_lo(p.h2 + o, p.h2 + ol, hv);
+          // dbg: column sums of this warp's 32 rows by recursive halving (lane
+          // l ends with column l), one atomic per column and warp
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? dz[i] : dz[i + w];
+              const float keep = up ? dz[i + w] : dz[i];
+              dz[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+          }
+          atomicAdd(p.dbg_r + n0 + c0 + lane, dz[0]);
+        }
+      } else if (EPI == EPI_DW) {
+        // Weight-gradient rows (row m = neuron, fp32) of problem q: stored
+        // in all-dense mode, added to the gather kernel's rows otherwise.
+        float *out = p.outq[q];
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(tacc + c0, v);
+          if (!row_ok || n0 + c0 >= p.N) continue;
+          float *o = out + (size_t)m * p.N + n0 + c0;
+          if (n0 + c0 + 32 > p.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (n0 + c0 + i < p.N) o[i] = dense_all ? v[i] : o[i] + v[i];
+            continue;
+          }
+          float4 *o4 = (float4 *)o;
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            float4 r = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+            if (!dense_all) {
+              const float4 q4 = o4[v4];
+              r.x += q4.x; r.y += q4.y; r.z += q4.z; r.w += q4.w;
+            }
+            o4[v4] = r;
+          }
+        }
+        if (q == 0 && nb == 0 && row_ok)
+          p.dbg_out[m] = (dense_all ? 0.f : p.dbg_out[m]) + p.dbg_r[m];
+      } else if (EPI == EPI_DOWN || EPI == EPI_DX) {
         const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
@@ -680,11 +953,10 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
          CUDA_SUCCESS;
 }
 
-template <int BN, int NB, bool B_MN, int EPI>
-cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a2, const CUtensorMap &b0,
-                      const CUtensorMap &b1, const TcParams &p, int max_tiles, cudaStream_t s) {
-  using CF = Cfg<BN, NB, B_MN, EPI>;
-  auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI>;
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
+cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cudaStream_t s) {
+  using CF = Cfg<BN, NB, B_MN, EPI, A_MN>;
+  auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI, A_MN>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
@@ -693,8 +965,17 @@ cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a2, const CUtenso
   }
   int grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, NTHREADS, CF::SMEM, s>>>(a, a2, b0, b1, p);
+  kern<<<grid, NTHREADS, CF::SMEM, s>>>(maps, p);
   return cudaGetLastError();
+}
+
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
+cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a2, const CUtensorMap &b0,
+                      const CUtensorMap &b1, const TcParams &p, int max_tiles, cudaStream_t s) {
+  TcMaps maps;
+  maps.a[0] = a; maps.a[1] = a2; maps.a[2] = a;
+  maps.b[0] = b0; maps.b[1] = b1; maps.b[2] = b0; maps.b[3] = b1;
+  return launch_tc<BN, NB, B_MN, EPI, A_MN>(maps, p, max_tiles, s);
 }
 
 TcParams base_params(const FwdArgs &a) {
@@ -780,12 +1061,97 @@ cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   return launch_tc<256, 1, true, EPI_DOWN>(mh, mh, md, md, p, tiles, s);
 }
 
-// Test hook: fp32 C[M][N] = A[M][K] B^T (B [N][K], b_mn = 0) or A B (B [K][N],
-// b_mn = 1); bf16 operands.
-cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N, int K, int b_mn,
+// ---------------------------------------------------------------------------
+// Backward of the dense-path rows: every row in all-dense mode, else the
+// overflow rows when there are at least OVF_GEMM_MIN of them (the kernels
+// return at once when there are none).  Row buffers (Tp = T rounded up to
+// 128 rows): ws.dzr / ws.dur / ws.hr = dz / du / h as bf16 hi rows then lo
+// rows ([2 Tp][F]); ws.dyg / ws.xg = gathered dy / x rows ([Tp][D]).
+namespace {
+
+TcParams bwd_params(const BwdArgs &a) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.Tn = a.T; p.F = a.F; p.D = a.D; p.C = a.C; p.Kslots = a.K; p.cap = a.tw.ovf_cap;
+  p.gated = a.gated; p.train = 1; p.rows = a.ws.rows; p.pos = a.ws.pos; p.ctl = a.ws.ctl;
+  p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val; p.uval = (bf16 *)a.tw.u_val;
+  p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb;
+  p.dz2 = (bf16 *)a.ws.dzr; p.du2 = (bf16 *)a.ws.dur; p.h2 = (bf16 *)a.ws.hr;
+  p.Tp = (a.T + BM - 1) / BM * BM;
+  p.y = (bf16 *)a.dx; p.lambda = a.lambda; p.dbg_r = a.ws.dbg_r; p.status = a.tw.status;
+  return p;
+}
+
+}  // namespace
+
+// dh = dy W_down^T over the dense-path rows, then the L1 term and dz / du / h.
+cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s) {
+  const int Tp = (a.T + BM - 1) / BM * BM;
+  CUtensorMap mdyg, mdy, mwd;
+  if (!make_map(&mdyg, a.ws.dyg, a.D, Tp, 64, BM) || !make_map(&mdy, a.dy, a.D, a.T, 64, BM) ||
+      !make_map(&mwd, a.Wd, a.D, a.F, 64, 256))
+    return cudaErrorInvalidValue;
+  TcParams p = bwd_params(a);
+  p.m_dev = &a.ws.ctl->n_rows;
+  p.N = a.F;
+  p.Kdim = a.D;
+  return launch_tc<256, 1, false, EPI_DH>(mdyg, mdy, mwd, mwd, p, (Tp / BM) * ((a.F + 255) / 256),
+                                          s);
+}
+
+// dx[tok] = dz W_gate + du W_up over the dense-path rows (one accumulator,
+// four K ranges: the hi and lo parts of dz and du; W read MN-major from
+// [F][D]).
+cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s) {
+  const int Tp = (a.T + BM - 1) / BM * BM;
+  CUtensorMap mz, mu, mwg, mwu;
+  if (!make_map(&mz, a.ws.dzr, a.F, 2 * Tp, 64, BM) ||
+      !make_map(&mu, a.ws.dur, a.F, 2 * Tp, 64, BM) || !make_map(&mwg, a.Wg, a.D, a.F, 64, 64) ||
+      !make_map(&mwu, a.gated ? a.Wu : a.Wg, a.D, a.F, 64, 64))
+    return cudaErrorInvalidValue;
+  TcParams p = bwd_params(a);
+  p.m_dev = &a.ws.ctl->n_rows;
+  p.N = a.D;
+  p.Kdim = a.F;
+  return launch_tc<256, 1, true, EPI_DX>(mz, mu, mwg, mwu, p, (Tp / BM) * ((a.D + 255) / 256), s);
+}
+
+// dWg = dz^T x (+ dbg), dWu = du^T x, dWd = h^T dy over the dense-path rows:
+// both operands MN-major, the token axis is the contraction (hi and lo parts
+// of dz / du / h as two K ranges).  Stored in all-dense mode, added to the
+// gather kernel's rows otherwise.
+cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s) {
+  const int Tp = (a.T + BM - 1) / BM * BM;
+  // problems: dWg (A = dz, B = x), [dWu (du, x),] dWd (h, dy)
+  TcMaps maps;
+  const void *A[3] = {a.ws.dzr, a.gated ? (const void *)a.ws.dur : a.ws.hr, a.ws.hr};
+  for (int q = 0; q < 3; ++q)
+    if (!make_map(&maps.a[q], A[q], a.F, 2 * Tp, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&maps.b[0], a.ws.xg, a.D, Tp, 64, 64) || !make_map(&maps.b[1], a.x, a.D, a.T, 64, 64) ||
+      !make_map(&maps.b[2], a.ws.dyg, a.D, Tp, 64, 64) ||
+      !make_map(&maps.b[3], a.dy, a.D, a.T, 64, 64))
+    return cudaErrorInvalidValue;
+  TcParams p = bwd_params(a);
+  p.k_dev = &a.ws.ctl->n_rows;
+  p.M_host = a.F;
+  p.N = a.D;
+  p.nq = a.gated ? 3 : 2;
+  p.outq[0] = a.dWg;
+  p.outq[1] = a.gated ? a.dWu : a.dWd;
+  p.outq[2] = a.dWd;
+  p.dbg_out = a.dbg;
+  const int tiles = p.nq * ((a.F + BM - 1) / BM) * ((a.D + 255) / 256);
+  return launch_tc<256, 1, true, EPI_DW, true>(maps, p, tiles, s);
+}
+
+// Test hook: fp32 C[M][N] = op(A) op(B), bf16 operands.  layout bit 0: B is
+// [K][N] (MN-major), else [N][K]; bit 1: A is [K][M] (MN-major), else [M][K].
+cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N, int K, int layout,
                          int32_t *status, cudaStream_t s) {
+  const bool b_mn = (layout & 1) != 0, a_mn = (layout & 2) != 0;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, K, M, 64, BM)) return cudaErrorInvalidValue;
+  if (a_mn ? !make_map(&ma, A, M, K, 64, 64) : !make_map(&ma, A, K, M, 64, BM))
+    return cudaErrorInvalidValue;
   if (b_mn ? !make_map(&mb, B, N, K, 64, 64) : !make_map(&mb, B, K, N, 64, 128))
     return cudaErrorInvalidValue;
   TcParams p;
@@ -796,16 +1162,22 @@ cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N
   p.out = Cout;
   p.status = status;
   const int tiles = ((M + BM - 1) / BM) * ((N + 127) / 128);
-  if (b_mn) return launch_tc<128, 1, true, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
-  return launch_tc<128, 1, false, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
+  switch (layout & 3) {
+    case 0: return launch_tc<128, 1, false, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
+    case 1: return launch_tc<128, 1, true, EPI_F32>(ma, ma, mb, mb, p, tiles, s);
+    case 2: return launch_tc<128, 1, false, EPI_F32, true>(ma, ma, mb, mb, p, tiles, s);
+    default: return launch_tc<128, 1, true, EPI_F32, true>(ma, ma, mb, mb, p, tiles, s);
+  }
 }
 
 }  // namespace twell
 
 extern "C" int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K,
-                                  int b_mn, int32_t *status, void *stream) {
+                                  int layout, int32_t *status, void *stream) {
   if (!twell::tc_available()) return TWELL_ERR_UNSUPPORTED;
-  if (!A || !B || !C || M < 1 || N < 1 || K < 8 || (K % 8) || (b_mn && (N % 8))) return TWELL_ERR_ARG;
-  cudaError_t e = twell::tc_test_gemm(A, B, C, M, N, K, b_mn, status, (cudaStream_t)stream);
+  if (!A || !B || !C || M < 1 || N < 1 || K < 8 || layout < 0 || layout > 3) return TWELL_ERR_ARG;
+  if ((layout & 1) ? (N % 8) : (K % 8)) return TWELL_ERR_ARG;
+  if ((layout & 2) ? (M % 8) : (K % 8)) return TWELL_ERR_ARG;
+  cudaError_t e = twell::tc_test_gemm(A, B, C, M, N, K, layout, status, (cudaStream_t)stream);
   return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

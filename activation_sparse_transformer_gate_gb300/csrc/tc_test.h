@@ -1,14 +1,15 @@
 // tc_test.h -- test and measurement hooks (exported, not part of the public ABI
-// in include/twell.h).  The tcgen05 GEMM engine: fp32 C[M][N] = A[M][K] B^T with B [N][K]
-// (b_mn = 0) or A B with B [K][N] (b_mn = 1); A, B bf16 device pointers,
-// K % 8 == 0 (16-byte row pitch), N % 8 == 0 when b_mn = 1.  Returns a
+// in include/twell.h).  The tcgen05 GEMM engine: fp32 C[M][N] = op(A) op(B),
+// A, B bf16 device pointers.  layout bit 0: B is [K][N] (MN-major), else
+// [N][K]; bit 1: A is [K][M] (MN-major), else [M][K].  Every row pitch must be
+// a multiple of 16 bytes (the inner extent a multiple of 8).  Returns a
 // twell_status code; device-side errors go to *status.
 #pragma once
 #include <stdint.h>
 #ifdef __cplusplus
 extern "C" {
 #endif
-int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K, int b_mn,
+int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K, int layout,
                        int32_t *status, void *stream);
 
 // Measurement hook: gather n_rows rows (indices in rows[], each < the row count

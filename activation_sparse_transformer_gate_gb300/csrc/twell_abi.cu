@@ -31,6 +31,7 @@ struct Profiler {
   bool on = false;
   std::vector<cudaEvent_t> ev;
   std::vector<int> id;
+  std::vector<int> nl;  // kernel launches in the interval that ends at each event
   size_t used = 0;
 };
 Profiler &profiler() {
@@ -39,7 +40,7 @@ Profiler &profiler() {
 }
 }  // namespace
 
-void prof_mark(int kid, cudaStream_t s) {
+void prof_mark(int kid, cudaStream_t s, int launches) {
   Profiler &p = profiler();
   if (!p.on) return;
   std::lock_guard<std::mutex> g(p.mu);
@@ -48,8 +49,10 @@ void prof_mark(int kid, cudaStream_t s) {
     if (cudaEventCreate(&e) != cudaSuccess) return;
     p.ev.push_back(e);
     p.id.push_back(0);
+    p.nl.push_back(0);
   }
   p.id[p.used] = kid;
+  p.nl[p.used] = kid < 0 ? 0 : launches;
   cudaEventRecord(p.ev[p.used], s);
   ++p.used;
 }
@@ -58,7 +61,8 @@ static const char *kKernelNames[KID_COUNT] = {
     "gate_gemm_relu_twell", "overflow_compact", "twell_updown_fused", "gather_rows",
     "dense_rows_gate_up",   "dense_rows_down",  "pack_dense",         "copy_fb_rows",
     "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
-    "bwd_dense_rows",       "fill_u_slots",     "assemble_fb_rows"};
+    "bwd_dense_dh_gemm",    "fill_u_slots",     "assemble_fb_rows",   "bwd_dense_dx_gemm",
+    "bwd_dense_dw_gemm",    "bwd_prep_rows"};
 
 Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
   Workspace w;
@@ -75,11 +79,14 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
   w.ovf_bits = (uint32_t *)take(4 * (((size_t)T + 31) / 32));
   w.rows = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   w.pos = (int32_t *)take(sizeof(int32_t) * (size_t)T);
-  w.h = take(es * (size_t)T * F);
-  w.xg = take(es * (size_t)T * D);
-  w.wide = take(es * (size_t)T * F);
+  const size_t Tp = ((size_t)T + 127) / 128 * 128;  // rows of the GEMM row buffers
+  w.h = take(es * Tp * F);
+  w.xg = take(es * Tp * D);
+  w.wide = take(es * Tp * F);
   if (train) {
-    w.urows = take(es * (size_t)T * F);
+    w.urows = take(es * Tp * F);
+    w.dyg = take(es * Tp * D);
+    w.dbg_r = (float *)take(4 * (size_t)F);
     const size_t slots = nt * (size_t)T * (size_t)K;
     w.dz = (float *)take(4 * slots);
     w.du = (float *)take(4 * slots);
@@ -88,9 +95,11 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_e = (float4 *)take(16 * slots);
     w.col_chunk = (int32_t *)take(4 * (size_t)F * (((size_t)T + 1023) / 1024));
-    w.dzr = (float *)take(4 * (size_t)T * F);
-    w.dur = (float *)take(4 * (size_t)T * F);
-    w.hr = (float *)take(4 * (size_t)T * F);
+    // fp32 [T][F] rows of the gather path, or bf16 hi + lo rows [2 Tp][F]
+    // of the tensor-core backward (never both in one call)
+    w.dzr = (float *)take(4 * Tp * F);
+    w.dur = (float *)take(4 * Tp * F);
+    w.hr = (float *)take(4 * Tp * F);
   }
   w.bytes = off;
   return w;
@@ -312,6 +321,8 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
   a.gated = gated; a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.dy = dy; a.tw = *tw;
   a.lambda = lambda; a.dx = dx; a.dWg = dWg; a.dbg = dbg; a.dWu = dWu; a.dWd = dWd;
+  a.dense_switch = switch_of(tw);
+  a.dense_density = density_of(tw);
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
   return cuda_status(launch_backward(a, (cudaStream_t)stream));
 }
@@ -325,6 +336,10 @@ int twell_profile_begin(void) {
 }
 
 int twell_profile_end(int capacity, int *kernel_ids, float *ms, int *count) {
+  return twell_profile_end_ex(capacity, kernel_ids, ms, nullptr, count);
+}
+
+int twell_profile_end_ex(int capacity, int *kernel_ids, float *ms, int *launches, int *count) {
   Profiler &p = profiler();
   std::lock_guard<std::mutex> g(p.mu);
   p.on = false;
@@ -337,6 +352,7 @@ int twell_profile_end(int capacity, int *kernel_ids, float *ms, int *count) {
     if (n < capacity) {
       if (kernel_ids) kernel_ids[n] = p.id[i];
       if (ms) ms[n] = t;
+      if (launches) launches[n] = p.nl[i];
     }
     ++n;
   }

@@ -229,13 +229,15 @@ def run_ours(args, rank, world, local_rank):
     cap = 64 * prof_steps
     ids = (ctypes.c_int * cap)()
     ms = (ctypes.c_float * cap)()
+    nl = (ctypes.c_int * cap)()
     cnt = ctypes.c_int(0)
     lib.twell_kernel_name.restype = ctypes.c_char_p
-    lib.twell_profile_end(cap, ids, ms, ctypes.byref(cnt))
+    lib.twell_profile_end_ex(cap, ids, ms, nl, ctypes.byref(cnt))
     per = {}
     for i in range(min(cnt.value, cap)):
         per.setdefault(lib.twell_kernel_name(ids[i]).decode(), []).append(ms[i])
-    launches_per_step = cnt.value / prof_steps
+    # kernel launches of the library per step (a profiled step may hold several)
+    launches_per_step = sum(nl[i] for i in range(min(cnt.value, cap))) / prof_steps
     kern = {k: {"launches_per_step": len(v) / prof_steps, "avg_ms": float(np.mean(v)),
                 "ms_per_step": float(np.sum(v)) / prof_steps} for k, v in per.items()}
 

@@ -178,14 +178,18 @@ twell_status twell_hybrid_split_static(twell_t *tw, void *stream);
 
 /* Optional per-launch timing, for benchmarks.  Between twell_profile_begin
  * and twell_profile_end every entry point records a CUDA event on its stream
- * before its first kernel and after each kernel it launches.
- * twell_profile_end waits for those events and returns, in launch order, the
- * kernel identity (see twell_kernel_name) and the milliseconds between the
- * event before and the event after that launch; *count receives the number of
- * launches (TWELL_ERR_CAPACITY when it exceeds `capacity`).  Recording is
- * process-wide; the events are created once and reused. */
+ * before its first kernel and after each step of its launch sequence (a step
+ * is one kernel, or a few launches of one component: the two passes of the
+ * sparse transpose, the three weight-gradient GEMMs).  twell_profile_end
+ * waits for those events and returns, in launch order, the step's identity
+ * (see twell_kernel_name) and the milliseconds between the event before and
+ * the event after it; *count receives the number of steps
+ * (TWELL_ERR_CAPACITY when it exceeds `capacity`).  twell_profile_end_ex
+ * also returns the kernel launches of each step (launches may be NULL).
+ * Recording is process-wide; the events are created once and reused. */
 int twell_profile_begin(void);
 int twell_profile_end(int capacity, int *kernel_ids, float *ms, int *count);
+int twell_profile_end_ex(int capacity, int *kernel_ids, float *ms, int *launches, int *count);
 const char *twell_kernel_name(int kernel_id);
 
 /* Version string of the library build. */

@@ -25,10 +25,10 @@ def hook():
     return f
 
 
-def run(hook, A, B, M, N, K, b_mn):
+def run(hook, A, B, M, N, K, layout):
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
-    code = hook(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, b_mn, st.data_ptr(),
+    code = hook(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, layout, st.data_ptr(),
                 torch.cuda.current_stream().cuda_stream)
     assert code == 0, code
     torch.cuda.synchronize()
@@ -44,31 +44,39 @@ def describe_mismatch(got, want):
             f"cols {cols[:8].tolist()}.. ({len(cols)}); got[0,:4]={got[0, :4]} want={want[0, :4]}")
 
 
-@pytest.mark.parametrize("M,N,K,b_mn", [
+def operands(g, M, N, K, layout, draw):
+    """A, B in the storage the layout names (bit 0: B [K][N], bit 1: A [K][M])
+    and the float64 product C = op(A) op(B)."""
+    A = draw((K, M) if layout & 2 else (M, K), g).to(torch.bfloat16)
+    B = draw((K, N) if layout & 1 else (N, K), g).to(torch.bfloat16)
+    a = A.double().numpy()
+    b = B.double().numpy()
+    a = a.T if layout & 2 else a
+    b = b if layout & 1 else b.T
+    return A, B, a, b
+
+
+@pytest.mark.parametrize("M,N,K,layout", [
     (128, 128, 64, 0), (256, 256, 256, 0), (200, 384, 320, 0), (77, 136, 72, 0),
     (128, 128, 64, 1), (256, 256, 256, 1), (300, 192, 512, 1), (64, 72, 200, 1),
+    (128, 128, 64, 2), (256, 136, 192, 2), (200, 256, 72, 3), (384, 264, 300, 3),
 ])
-def test_tc_gemm_integer_exact(hook, M, N, K, b_mn):
-    g = torch.Generator().manual_seed(M * 7 + N * 3 + K + b_mn)
-    A = torch.randint(-3, 4, (M, K), generator=g).to(torch.bfloat16)
-    if b_mn:
-        B = torch.randint(-3, 4, (K, N), generator=g).to(torch.bfloat16)
-        want = A.double().numpy() @ B.double().numpy()
-    else:
-        B = torch.randint(-3, 4, (N, K), generator=g).to(torch.bfloat16)
-        want = A.double().numpy() @ B.double().numpy().T
-    got = run(hook, A.cuda(), B.cuda(), M, N, K, b_mn)
+def test_tc_gemm_integer_exact(hook, M, N, K, layout):
+    """layout 2, 3: A read MN-major (the weight-gradient GEMMs of the backward),
+    with ragged M and a K that is not a multiple of the 64-deep k-block."""
+    g = torch.Generator().manual_seed(M * 7 + N * 3 + K + layout)
+    A, B, a, b = operands(g, M, N, K, layout, lambda sh, gg: torch.randint(-3, 4, sh, generator=gg))
+    want = a @ b
+    got = run(hook, A.cuda(), B.cuda(), M, N, K, layout)
     assert np.array_equal(got, want), describe_mismatch(got, want)
 
 
-@pytest.mark.parametrize("b_mn", [0, 1])
-def test_tc_gemm_gaussian(hook, b_mn):
+@pytest.mark.parametrize("layout", [0, 1, 2, 3])
+def test_tc_gemm_gaussian(hook, layout):
     M, N, K = 512, 640, 1024
-    g = torch.Generator().manual_seed(5 + b_mn)
-    A = torch.randn((M, K), generator=g).to(torch.bfloat16)
-    B = torch.randn((K, N) if b_mn else (N, K), generator=g).to(torch.bfloat16)
-    a, b = A.double().numpy(), B.double().numpy()
-    want = a @ b if b_mn else a @ b.T
-    bound = K * 2.0 ** -23 * (np.abs(a) @ (np.abs(b) if b_mn else np.abs(b).T))
-    got = run(hook, A.cuda(), B.cuda(), M, N, K, b_mn)
+    g = torch.Generator().manual_seed(5 + layout)
+    A, B, a, b = operands(g, M, N, K, layout, lambda sh, gg: torch.randn(sh, generator=gg))
+    want = a @ b
+    bound = K * 2.0 ** -23 * (np.abs(a) @ np.abs(b))
+    got = run(hook, A.cuda(), B.cuda(), M, N, K, layout)
     assert np.all(np.abs(got - want) <= bound)

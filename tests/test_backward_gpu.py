@@ -25,7 +25,8 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None):
     """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
     the density test of the dispatcher off, so that moderately dense test
     workloads still run the gather kernels; out (dict) receives the
-    workspace's control block."""
+    workspace's control block after the forward ("ctl") and after the
+    backward ("ctl_bwd")."""
     T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
     dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -43,9 +44,16 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None):
     dbg = torch.full((F,), float("nan"), dtype=torch.float32, device="cuda")
     tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], lam, D, dx, dWg, dbg,
                           dWu, dWd, ws, nws)
+    if out is not None:
+        out["ctl_bwd"] = ws[:24].cpu().numpy().copy()
     code, n_ovf = tw.twell_get_status(bufs.t)
     return dict(code=code, n_ovf=n_ovf, y=to_np64(y), dx=to_np64(dx), dWg=to_np64(dWg),
                 dbg=to_np64(dbg), dWu=None if dWu is None else to_np64(dWu), dWd=to_np64(dWd))
+
+
+def ctl_fields(c):
+    """(n_rows, dense, n_ovf, ovf_gemm) of a saved control block."""
+    return tuple(int(v) for v in c[:16].view(np.int32))
 
 
 def check_backward(a, w, g, lam, tok_sel=None, neu_sel=None):
@@ -116,13 +124,18 @@ def test_nongated_bf16_with_overflow():
 
 
 def test_many_overflow_rows_dense_gemm_path():
-    """>= 128 overflow rows (but fewer than half): the forward runs them on the
-    tensor-core dense-row GEMMs; the backward gathers them from g_fb / u_fb."""
+    """>= 128 overflow rows (but fewer than half): forward and backward run them
+    on the tensor-core dense-row GEMMs (a partial last tile of rows, so the
+    weight-gradient GEMMs contract over zero-padded rows); the other rows take
+    the gather kernels, and the two weight-gradient parts add up."""
     w = synth.Workload("bmany", 600, 256, 1024, 128, 8, "bf16", True, -2.33, 26, hot_tokens=2,
                        seq_len=7, hot_bias=1.6, train=True)
     a = synth.generate(w)
-    g = run_train(a, w, 1e-3)
-    assert g["code"] == 0 and 128 <= g["n_ovf"] < 300
+    out = {}
+    g = run_train(a, w, 1e-3, out=out)
+    assert g["code"] == 0 and 128 <= g["n_ovf"] < 300 and g["n_ovf"] % 64 != 0
+    n_rows, dense, n_ovf, ovf_gemm = ctl_fields(out["ctl_bwd"])
+    assert (dense, ovf_gemm, n_rows) == (0, 1, n_ovf) and n_ovf == g["n_ovf"]
     check_backward(a, w, g, 1e-3)
 
 
@@ -138,16 +151,62 @@ def test_transpose_several_token_chunks_ragged():
 
 
 def test_backward_after_density_switched_dense_forward():
-    """~5% active, K = 16: the forward runs every row densely (density test on,
-    u at the slots filled from the dense u rows); the backward then gathers
-    from the slots and matches the oracle."""
+    """~5% active, K = 16: forward and backward run every row densely (density
+    test on; the backward rebuilds the g / u rows from the slots)."""
     w = synth.Workload("bdens", 160, 256, 1024, 128, 16, "bf16", True, -1.64, 44, train=True)
     a = synth.generate(w)
     out = {}
     g = run_train(a, w, 1e-3, dense_density=0.0, out=out)
     assert g["code"] == 0
-    assert int(out["ctl"][4:8].view(np.int32)[0]) == 1  # the forward ran densely
+    assert ctl_fields(out["ctl"])[1] == 1  # the forward ran densely
+    assert ctl_fields(out["ctl_bwd"])[:2] == (160, 1)  # and so did the backward
     check_backward(a, w, g, 1e-3)
+
+
+@pytest.mark.parametrize("gated", [True, False])
+def test_dense_backward_all_rows_ragged(gated):
+    """Every row on the tensor-core backward (density test forced), with
+    overflow rows (g / u from the dense backup rows) among rows rebuilt from
+    their slots; T = 300 (a partial tile of rows) and d_model 200 (partial
+    K block and partial output columns in dx and dW)."""
+    w = synth.Workload(f"bdr{int(gated)}", 300, 200, 1024, 128, 8, "bf16", gated, -2.0, 45,
+                       hot_tokens=3, seq_len=100, hot_bias=1.4, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 0.05, dense_density=1e-6, out=out)
+    assert g["code"] == 0 and g["n_ovf"] >= 3
+    assert ctl_fields(out["ctl_bwd"])[:2] == (300, 1)
+    check_backward(a, w, g, 0.05)
+
+
+def test_dense_backward_l1_and_zero_down_weight():
+    """All-dense backward with W_down = 0: dh is the L1 term alone, so
+    dbg[n] = lambda * sum over active tokens of |u| (gated) exactly as on
+    the gather path."""
+    w = synth.Workload("bdwd0", 256, 256, 512, 64, 8, "bf16", True, -1.5, 46, train=True)
+    a = synth.generate(w)
+    a["Wd"] = np.zeros_like(a["Wd"])
+    out = {}
+    g = run_train(a, w, 0.25, dense_density=1e-6, out=out)
+    assert g["code"] == 0 and ctl_fields(out["ctl_bwd"])[1] == 1
+    b = check_backward(a, w, g, 0.25)
+    assert np.abs(b["dbg"]).max() > 0
+
+
+def test_dense_regime_sampled():
+    """A dense regime at scale (5% active, K = 16, T = 2048, d_model 1024,
+    d_ff 4096): the dispatcher's default density test sends forward and
+    backward to the tensor cores; sampled tokens and neurons against the
+    oracle."""
+    w = synth.Workload("bdreg", 2048, 1024, 4096, 128, 16, "bf16", True, -1.64, 47, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-4, dense_density=0.0, out=out)
+    assert g["code"] == 0 and ctl_fields(out["ctl_bwd"])[:2] == (2048, 1)
+    rng = np.random.default_rng(47)
+    ts = np.unique(np.concatenate([np.arange(4), rng.choice(w.T, 20, replace=False)]))
+    ns = np.unique(np.concatenate([np.arange(4), rng.choice(w.F, 20, replace=False)]))
+    check_backward(a, w, g, 1e-4, tok_sel=ts, neu_sel=ns)
 
 
 @pytest.mark.parametrize("D", [512, 1024])
