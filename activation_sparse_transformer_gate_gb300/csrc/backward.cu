@@ -136,6 +136,7 @@ __device__ __forceinline__ void dh_finish(const BParams &p, int ps, int sl, floa
 // row per warp.
 template <class T, int VL, int PIF>
 __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p) {
+  pdl_begin();
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -202,6 +203,7 @@ constexpr int DH_CHUNK = 256;  // pairs whose partial dots are held before the f
 template <int U>
 __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
     bwd_dh_mma_kernel(BParams p) {
+  pdl_begin();
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
   __shared__ int s_slot[LIST_CAP];
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
 // the working set is W_gate and W_up.
 template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
+  pdl_begin();
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -388,6 +391,7 @@ constexpr int TR_CHUNK = 1024;
 
 template <int C>
 __global__ void __launch_bounds__(TR_CHUNK) twell_count_kernel(BParams p) {
+  pdl_begin();
   __shared__ int cnt[C];
   const int j = blockIdx.x, ch = blockIdx.y, tid = threadIdx.x;
   const int K = p.K, Tn = p.Tn;
@@ -409,6 +413,7 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_count_kernel(BParams p) {
 
 template <int C>
 __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
+  pdl_begin();
   __shared__ uint32_t occ[32][C];
   __shared__ int woff[32][C];
   __shared__ int run[C], tot[C];
@@ -493,6 +498,7 @@ constexpr int DW_LIST = 512;
 
 template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
+  pdl_begin();
   constexpr int EV = Vec<T>::EV;
   __shared__ float4 s_e[DW_LIST];
   if (p.gemm_rows && p.ctl->dense) return;  // the GEMMs write every row
@@ -625,7 +631,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 // (the constant-offset row loads that help the SpMM kernels made this one slower)
-#define TW_DH(TT, L) bwd_dh_kernel<TT, L, 1><<<a.T, 256, 0, s>>>(p)
+#define TW_DH(TT, L) launch_k(bwd_dh_kernel<TT, L, 1>, a.T, 256, 0, s, p)
 #define TW_DH_T(TT)                                                                            \
   do {                                                                                         \
     switch (vl) {                                                                              \
@@ -641,9 +647,9 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     // tensor-core dh SDDMM: chunks per warp = NV / 32; U of them per load
     // batch (4: three CTAs per SM, measured faster than 8 at two)
     const int cpw = NV / (4 * DH_WARPS);
-    if (cpw % 4 == 0) bwd_dh_mma_kernel<4><<<a.T, DH_WARPS * 32, 0, s>>>(p);
-    else if (cpw % 2 == 0) bwd_dh_mma_kernel<2><<<a.T, DH_WARPS * 32, 0, s>>>(p);
-    else bwd_dh_mma_kernel<1><<<a.T, DH_WARPS * 32, 0, s>>>(p);
+    if (cpw % 4 == 0) launch_k(bwd_dh_mma_kernel<4>, a.T, DH_WARPS * 32, 0, s, p);
+    else if (cpw % 2 == 0) launch_k(bwd_dh_mma_kernel<2>, a.T, DH_WARPS * 32, 0, s, p);
+    else launch_k(bwd_dh_mma_kernel<1>, a.T, DH_WARPS * 32, 0, s, p);
   } else if (bf) {
     TW_DH_T(bf16);
   } else {
@@ -656,10 +662,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   prof_mark(KID_BWD_SLOTS, s);
 #define TW_VPT(K, TT, G)                                                                       \
   do {                                                                                         \
-    if (vpt == 1) K<TT, 1, 8, 0><<<G, threads, 0, s>>>(p);                                     \
-    else if (vpt == 2 && NV == 256) K<TT, 2, 4, 128><<<G, 128, 0, s>>>(p);                     \
-    else if (vpt == 2) K<TT, 2, 3, 0><<<G, threads, 0, s>>>(p);                                \
-    else K<TT, 4, 2, 0><<<G, threads, 0, s>>>(p);                                              \
+    if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, s, p);                               \
+    else if (vpt == 2 && NV == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, s, p);               \
+    else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, s, p);                          \
+    else launch_k(K<TT, 4, 2, 0>, G, threads, 0, s, p);                                        \
   } while (0)
   if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T);
   else TW_VPT(bwd_dx_kernel, float, a.T);
@@ -670,14 +676,14 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const int nt = a.F / a.C;
   const dim3 tgrid(nt, (a.T + TR_CHUNK - 1) / TR_CHUNK);
   if (a.C == 32) {
-    twell_count_kernel<32><<<tgrid, TR_CHUNK, 0, s>>>(p);
-    twell_transpose_kernel<32><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    launch_k(twell_count_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
+    launch_k(twell_transpose_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
   } else if (a.C == 64) {
-    twell_count_kernel<64><<<tgrid, TR_CHUNK, 0, s>>>(p);
-    twell_transpose_kernel<64><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    launch_k(twell_count_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
+    launch_k(twell_transpose_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
   } else {
-    twell_count_kernel<128><<<tgrid, TR_CHUNK, 0, s>>>(p);
-    twell_transpose_kernel<128><<<tgrid, TR_CHUNK, 0, s>>>(p);
+    launch_k(twell_count_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
+    launch_k(twell_transpose_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -18,6 +18,7 @@ template <class T, int E>
 __global__ void pack_dense_kernel(const T *__restrict__ H, int Tn, int F, int K,
                                   uint8_t *__restrict__ idx, T *__restrict__ val,
                                   uint8_t *__restrict__ nnz) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int C = 32 * E;
@@ -63,8 +64,8 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s) 
   const long blocks = (warps * 32 + threads - 1) / threads;
   const int E = tw.C / 32;
 #define TW_PD(TT, EE)                                                                          \
-  pack_dense_kernel<TT, EE><<<(unsigned)blocks, threads, 0, s>>>(                             \
-      (const TT *)H, tw.T, tw.F, tw.K, tw.idx, (TT *)tw.val, tw.nnz)
+  launch_k(pack_dense_kernel<TT, EE>, (unsigned)blocks, threads, 0, s, (const TT *)H, tw.T,    \
+           tw.F, tw.K, tw.idx, (TT *)tw.val, tw.nnz)
   if (tw.dtype == TWELL_BF16) {
     if (E == 1) TW_PD(bf16, 1); else if (E == 2) TW_PD(bf16, 2); else TW_PD(bf16, 4);
   } else {
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(1024)
 overflow_compact_kernel(const uint8_t *__restrict__ nnz, int Tn, int nt, int K, int cap,
                         int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf,
                         int32_t *status) {
+  pdl_begin();
   __shared__ int warp_cnt[32];
   __shared__ int warp_off[32];
   __shared__ int total;
@@ -147,6 +149,7 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
                      int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf, int32_t *status,
                      Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
                      int F, float dense_switch, float dense_density) {
+  pdl_begin();
   __shared__ int warp_off[32];
   __shared__ int word_off[1024];
   __shared__ int total;
@@ -211,14 +214,13 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user, float dense_density) {
   if (ws) {
-    overflow_scan_kernel<<<1, 1024, 0, s>>>(ws->ovf_bits, tw.T, tw.ovf_cap,
-                                            write_user ? tw.ovf_rows : nullptr,
-                                            write_user ? tw.n_ovf : nullptr, tw.status, ws->ctl,
-                                            ws->rows, ws->pos, tw.F, dense_switch, dense_density);
+    launch_k(overflow_scan_kernel, 1, 1024, 0, s, ws->ovf_bits, tw.T, tw.ovf_cap,
+             write_user ? tw.ovf_rows : nullptr, write_user ? tw.n_ovf : nullptr, tw.status,
+             ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density);
     return cudaGetLastError();
   }
-  overflow_compact_kernel<<<1, 1024, 0, s>>>(tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,
-                                             tw.ovf_rows, tw.n_ovf, tw.status);
+  launch_k(overflow_compact_kernel, 1, 1024, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,
+           tw.ovf_rows, tw.n_ovf, tw.status);
   return cudaGetLastError();
 }
 
@@ -227,6 +229,7 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
 __global__ void flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, long total, int Tn, int K,
                                       uint32_t *__restrict__ bits,
                                       unsigned long long *__restrict__ slots) {
+  pdl_begin();
   unsigned long long mine = 0;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long)gridDim.x * blockDim.x) {
@@ -249,8 +252,8 @@ cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaSt
   const long total = (long)tw.T * (tw.F / tw.C);
   long blocks = (total + 255) / 256;
   if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
-  flags_from_nnz_kernel<<<(unsigned)blocks, 256, 0, s>>>(tw.nnz, total, tw.T, tw.K, ws.ovf_bits,
-                                                         &ws.ctl->slots);
+  launch_k(flags_from_nnz_kernel, (unsigned)blocks, 256, 0, s, tw.nnz, total, tw.T, tw.K,
+           ws.ovf_bits, &ws.ctl->slots);
   return cudaGetLastError();
 }
 
@@ -258,6 +261,7 @@ cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaSt
 __global__ void copy_fb_rows_kernel(const uint4 *__restrict__ H, int row_vecs, int cap,
                                     const int32_t *__restrict__ ovf_rows,
                                     const int32_t *__restrict__ n_ovf, uint4 *__restrict__ g_fb) {
+  pdl_begin();
   const int n = min(*n_ovf, cap);
   for (int i = blockIdx.x; i < n; i += gridDim.x) {
     const uint4 *src = H + (size_t)ovf_rows[i] * row_vecs;
@@ -272,8 +276,8 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
   const int row_vecs = tw.F * es / 16;
   int blocks = tw.ovf_cap < tw.T ? tw.ovf_cap : tw.T;
   if (blocks > 1024) blocks = 1024;
-  copy_fb_rows_kernel<<<blocks, 256, 0, s>>>((const uint4 *)H, row_vecs, tw.ovf_cap,
-                                             tw.ovf_rows, tw.n_ovf, (uint4 *)tw.g_fb);
+  launch_k(copy_fb_rows_kernel, blocks, 256, 0, s, (const uint4 *)H, row_vecs, tw.ovf_cap,
+           tw.ovf_rows, tw.n_ovf, (uint4 *)tw.g_fb);
   return cudaGetLastError();
 }
 
@@ -283,6 +287,7 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
 __global__ void gather_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                    int row_vecs, const Ctl *__restrict__ ctl,
                                    const int32_t *__restrict__ rows) {
+  pdl_begin();
   if (ctl->dense || !ctl->ovf_gemm) return;
   const int n = ctl->n_rows;
   const int npad = (n + 127) / 128 * 128;
@@ -302,8 +307,8 @@ cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, 
   const int es = dtype == TWELL_BF16 ? 2 : 4;
   // Usually idle (no overflow-row GEMM): a small grid that loops over the rows.
   int blocks = T < 2 * num_sms() ? T : 2 * num_sms();
-  gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, D * es / 16, ws.ctl,
-                                            ws.rows);
+  launch_k(gather_rows_kernel, blocks, 256, 0, s, (const uint4 *)src, (uint4 *)dst, D * es / 16,
+           ws.ctl, ws.rows);
   return cudaGetLastError();
 }
 
@@ -317,6 +322,7 @@ __global__ void assemble_fb_rows_kernel(const Ctl *__restrict__ ctl,
                                         const uint8_t *__restrict__ nnz, const T *__restrict__ val,
                                         const T *__restrict__ wide, T *__restrict__ g_fb, int Tn,
                                         int F, int C, int K, int cap) {
+  pdl_begin();
   if (ctl->dense || ctl->ovf_gemm) return;
   const int n_fb = min(ctl->n_ovf, cap);
   for (int i = blockIdx.x; i < n_fb; i += gridDim.x) {
@@ -345,11 +351,11 @@ cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s) {
   int blocks = a.tw.ovf_cap < a.T ? a.tw.ovf_cap : a.T;
   if (blocks > OVF_GEMM_MIN) blocks = OVF_GEMM_MIN;
   if (a.dtype == TWELL_BF16)
-    assemble_fb_rows_kernel<bf16><<<blocks, 256, 0, s>>>(
+    launch_k(assemble_fb_rows_kernel<bf16>, blocks, 256, 0, s,
         a.ws.ctl, a.ws.rows, a.tw.idx, a.tw.nnz, (const bf16 *)a.tw.val, (const bf16 *)a.ws.wide,
         (bf16 *)a.tw.g_fb, a.T, a.F, a.C, a.K, a.tw.ovf_cap);
   else
-    assemble_fb_rows_kernel<float><<<blocks, 256, 0, s>>>(
+    launch_k(assemble_fb_rows_kernel<float>, blocks, 256, 0, s,
         a.ws.ctl, a.ws.rows, a.tw.idx, a.tw.nnz, (const float *)a.tw.val,
         (const float *)a.ws.wide, (float *)a.tw.g_fb, a.T, a.F, a.C, a.K, a.tw.ovf_cap);
   return cudaGetLastError();
@@ -362,6 +368,7 @@ __global__ void fill_u_slots_kernel(const Ctl *__restrict__ ctl, const int32_t *
                                     const uint8_t *__restrict__ idx,
                                     const uint8_t *__restrict__ nnz, const T *__restrict__ urows,
                                     T *__restrict__ u_val, int Tn, int F, int C, int K) {
+  pdl_begin();
   if (!ctl->dense) return;
   const long total = (long)Tn * (F / C);
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -381,11 +388,11 @@ cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s) {
   long blocks = (total + 255) / 256;  // usually idle (all-dense mode only)
   if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
   if (a.dtype == TWELL_BF16)
-    fill_u_slots_kernel<bf16><<<(unsigned)blocks, 256, 0, s>>>(
+    launch_k(fill_u_slots_kernel<bf16>, (unsigned)blocks, 256, 0, s,
         a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const bf16 *)a.ws.urows, (bf16 *)a.tw.u_val,
         a.T, a.F, a.C, a.K);
   else
-    fill_u_slots_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+    launch_k(fill_u_slots_kernel<float>, (unsigned)blocks, 256, 0, s,
         a.ws.ctl, a.ws.pos, a.tw.idx, a.tw.nnz, (const float *)a.ws.urows, (float *)a.tw.u_val,
         a.T, a.F, a.C, a.K);
   return cudaGetLastError();
@@ -399,6 +406,7 @@ __global__ void bwd_prep_rows_kernel(const Ctl *__restrict__ ctl, const int32_t 
                                      const uint4 *__restrict__ dy, const uint4 *__restrict__ x,
                                      uint4 *__restrict__ dyg, uint4 *__restrict__ xg,
                                      float *__restrict__ dbg_r, int row_vecs, int F) {
+  pdl_begin();
   const int n = ctl->n_rows;
   if (n == 0) return;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < F; i += gridDim.x * blockDim.x)
@@ -421,9 +429,8 @@ __global__ void bwd_prep_rows_kernel(const Ctl *__restrict__ ctl, const int32_t 
 
 cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s) {
   const int blocks = a.T < 2 * num_sms() ? a.T : 2 * num_sms();
-  bwd_prep_rows_kernel<<<blocks, 256, 0, s>>>(a.ws.ctl, a.ws.rows, (const uint4 *)a.dy,
-                                              (const uint4 *)a.x, (uint4 *)a.ws.dyg,
-                                              (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F);
+  launch_k(bwd_prep_rows_kernel, blocks, 256, 0, s, a.ws.ctl, a.ws.rows, (const uint4 *)a.dy,
+           (const uint4 *)a.x, (uint4 *)a.ws.dyg, (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F);
   return cudaGetLastError();
 }
 

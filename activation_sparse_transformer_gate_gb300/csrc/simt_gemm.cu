@@ -36,6 +36,7 @@ simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
                       int F, int K, uint8_t *__restrict__ idx, T *__restrict__ val,
                       uint8_t *__restrict__ nnz, uint32_t *__restrict__ ovf_bits,
                       T *__restrict__ wide, unsigned long long *__restrict__ slots) {
+  pdl_begin();
   constexpr int TN = BN / 16;
   constexpr int E = BN / 32;
   __shared__ float smem[BM * (BN + 1) > BK * (BM + 4) + BK * (BN + 4) ? BM * (BN + 1)
@@ -140,7 +141,7 @@ simt_gate_pack_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
 cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s) {
   dim3 grid(a.F / a.C, (a.T + BM - 1) / BM);
 #define TW_GP(TT, BNN)                                                                         \
-  simt_gate_pack_kernel<TT, BNN><<<grid, NT, 0, s>>>(                                          \
+  launch_k(simt_gate_pack_kernel<TT, BNN>, grid, NT, 0, s,                                     \
       (const TT *)a.x, (const TT *)a.Wg, a.bg, a.rb, a.T, a.D, a.F, a.K, a.tw.idx,             \
       (TT *)a.tw.val, a.tw.nnz, a.ws.ovf_bits, (TT *)a.ws.wide, &a.ws.ctl->slots)
   if (a.dtype == TWELL_BF16) {
@@ -172,6 +173,7 @@ struct RowsParams {
 
 template <class T, int MODE>
 __global__ void __launch_bounds__(NT) simt_rows_kernel(RowsParams p) {
+  pdl_begin();
   constexpr int BN = 64;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[2][BK][BN + 4];
@@ -278,16 +280,16 @@ static RowsParams rows_params(const FwdArgs &a) {
 cudaError_t launch_simt_dense_gu(const FwdArgs &a, cudaStream_t s) {
   RowsParams p = rows_params(a);
   dim3 g((a.F + 63) / 64, (a.T + BM - 1) / BM);
-  if (a.dtype == TWELL_BF16) simt_rows_kernel<bf16, MODE_GU><<<g, NT, 0, s>>>(p);
-  else simt_rows_kernel<float, MODE_GU><<<g, NT, 0, s>>>(p);
+  if (a.dtype == TWELL_BF16) launch_k(simt_rows_kernel<bf16, MODE_GU>, g, NT, 0, s, p);
+  else launch_k(simt_rows_kernel<float, MODE_GU>, g, NT, 0, s, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_simt_dense_down(const FwdArgs &a, cudaStream_t s) {
   RowsParams p = rows_params(a);
   dim3 g((a.D + 63) / 64, (a.T + BM - 1) / BM);
-  if (a.dtype == TWELL_BF16) simt_rows_kernel<bf16, MODE_D><<<g, NT, 0, s>>>(p);
-  else simt_rows_kernel<float, MODE_D><<<g, NT, 0, s>>>(p);
+  if (a.dtype == TWELL_BF16) launch_k(simt_rows_kernel<bf16, MODE_D>, g, NT, 0, s, p);
+  else launch_k(simt_rows_kernel<float, MODE_D>, g, NT, 0, s, p);
   return cudaGetLastError();
 }
 

@@ -305,6 +305,7 @@ struct Cfg {
 template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
+  pdl_begin();
   using CF = Cfg<BN, NB, B_MN, EPI, A_MN>;
   constexpr int S = CF::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -965,7 +966,7 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cuda
   }
   int grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, NTHREADS, CF::SMEM, s>>>(maps, p);
+  launch_k(kern, grid, NTHREADS, CF::SMEM, s, maps, p);
   return cudaGetLastError();
 }
 

@@ -158,9 +158,39 @@ twell_status check_ws(void *ws, size_t ws_bytes, const Workspace &need) {
 }
 
 float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_switch : 0.5f; }
-// Slot density above which the forward runs densely (0 -> 0.013, < 0 -> off).
-float density_of(const twell_t *tw) {
-  return tw->dense_density == 0.f ? 0.013f : (tw->dense_density > 0.f ? tw->dense_density : -1.f);
+// L2 bytes of the current device (queried once).
+size_t l2_bytes() {
+  static size_t n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) n = v;
+  });
+  return n;
+}
+
+// Slot density above which a call runs every row densely: the caller's
+// dense_density when > 0, none when < 0, else the default crossover of the
+// measured costs.  Per active (token, neuron) the forward gathers a W_up and
+// a W_down row (4·d_model bytes at ~14 TB/s when those matrices sit in L2)
+// where the dense path does ~6·d_model flops at ~1.3 PFLOP/s: 1.3%.  When
+// the gathered matrices exceed L2 the gathers slow in about the proportion
+// of rows that miss it (d_model 4096 / d_ff 14336 bf16: 235 MB, ~9.5 TB/s
+// measured, crossover ~0.65%), so the default scales by L2 / their bytes.
+// The backward gathers five rows per pair where its dense path does 11 GEMM
+// units against the forward's 3 (dz, du, h enter as hi + lo parts): its
+// crossover is (11/3) / (5/2) = 1.47 times the forward's.
+float density_of(const twell_t *tw, int D, int gated, bool backward) {
+  if (tw->dense_density > 0.f) return tw->dense_density;
+  if (tw->dense_density < 0.f) return -1.f;
+  const size_t es = tw->dtype == TWELL_BF16 ? 2 : 4;
+  const double wbytes = (double)(gated ? 2 : 1) * (double)tw->F * (double)D * (double)es;
+  const double l2 = (double)l2_bytes();
+  double d = 0.013;
+  if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
+  if (backward) d *= 1.47;
+  return (float)d;
 }
 
 bool use_tc(int dtype) { return dtype == TWELL_BF16 && tc_available(); }
@@ -284,7 +314,7 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.bg = bg; a.rb = row_bias; a.tw = *tw; a.y = y;
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, train);
   a.dense_switch = switch_of(tw);
-  a.dense_density = density_of(tw);
+  a.dense_density = density_of(tw, D, gated, false);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = run_gate_and_split(a, s);
   if (e == cudaSuccess) {
@@ -322,7 +352,7 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   a.gated = gated; a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.dy = dy; a.tw = *tw;
   a.lambda = lambda; a.dx = dx; a.dWg = dWg; a.dbg = dbg; a.dWu = dWu; a.dWd = dWd;
   a.dense_switch = switch_of(tw);
-  a.dense_density = density_of(tw);
+  a.dense_density = density_of(tw, D, gated, true);
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
   return cuda_status(launch_backward(a, (cudaStream_t)stream));
 }

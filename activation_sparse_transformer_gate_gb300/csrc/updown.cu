@@ -51,6 +51,7 @@ struct UDParams {
 // of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
 template <class T, int VPT, int VPL, int PIF, int PB2, bool EXACT>
 __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
+  pdl_begin();
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
   __shared__ float s_g[LIST_CAP];
@@ -171,11 +172,11 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
   do {                                                                                         \
     constexpr int VPT_ = (L + 3) / 4;                                                          \
     if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                             \
-      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>                      \
-          <<<a.T, UD_THREADS, 0, s>>>(p);                                                      \
+      launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>, a.T,        \
+               UD_THREADS, 0, s, p);                                                           \
     else                                                                                       \
-      updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>                     \
-          <<<a.T, UD_THREADS, 0, s>>>(p);                                                      \
+      launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>, a.T,       \
+               UD_THREADS, 0, s, p);                                                           \
   } while (0)
 #define TW_UD_T(TT)                                                                            \
   do {                                                                                         \

@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-energy", action="store_true",
                     help="skip the saved-memory and energy-per-token leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--dense-density", type=float, default=0.0,
+                    help="the dispatcher's density threshold (0: the library default; "
+                         "< 0: off; a tiny value forces the all-dense path)")
     return ap.parse_args()
 
 
@@ -155,7 +158,8 @@ def run_ours(args, rank, world, local_rank):
     dtype = tw.TWELL_BF16
     d = {k: upload(torch, dev, a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
     T, D, F = w.T, w.D, w.F
-    bufs = tw.TwellBuffers(T, F, w.C, w.K, dtype, train=train, device=dev)
+    bufs = tw.TwellBuffers(T, F, w.C, w.K, dtype, train=train, device=dev,
+                           dense_density=args.dense_density)
     ws, nws = tw.workspace(T, D, F, w.C, w.K, dtype, train, device=dev)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
     dx = dWg = dWu = dWd = dbg = None

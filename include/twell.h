@@ -106,7 +106,12 @@ typedef struct {
                              at most K per row and tile) exceed
                              dense_density * T * F: at such densities the
                              gathers cost more than dense GEMMs.  0 selects
-                             0.013; < 0 disables this test                  */
+                             the measured crossover: 0.013 when the gathered
+                             weights (W_up + W_down) fit in L2, scaled by
+                             L2 / their bytes when they do not, and 1.47x
+                             that in the backward; < 0 disables this test.
+                             The backward applies the same rules to the
+                             saved TwELL.                                    */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward
