@@ -65,8 +65,9 @@ struct BwdArgs {
 };
 
 // pack.cu
-// Streaming multiprocessors of the current device (queried once).
+// Streaming multiprocessors and L2 bytes of the current device (queried once).
 int num_sms();
+long long l2_size();
 
 cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // Hybrid split.  With a workspace: reads the overflow-row bitmap (which must

@@ -45,6 +45,9 @@ namespace twell {
 namespace {
 
 constexpr int BM = 128, BK = 64, NTHREADS = 192;
+// bf16 elements per row of the EPI_U g staging: 32 columns, a spare element
+// for scattered slots outside the block, padding to 16 bytes
+constexpr int GZ_STRIDE = 40;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4, EPI_DH = 5, EPI_DX = 6,
@@ -261,6 +264,7 @@ struct TcParams {
   int N, Kdim;             // output columns, contraction length
   int Tn, F, D, C, Kslots, cap, gated, train;
   int Tp;                  // backward: rows of a hi part (T rounded up to 128)
+  long long l2_bytes;      // L2 size of the device (tile order)
   const float *bg, *rb;
   const int32_t *rows, *pos;
   uint8_t *idx, *nnz;
@@ -279,6 +283,28 @@ struct TcParams {
   int32_t *status;
 };
 
+// (M-block, N-block) of tile t: groups of gm M-blocks (the last one may be
+// smaller), N-blocks outer and M-blocks inner within a group.
+__device__ __forceinline__ void tile_mn(int t, int m_blocks, int n_blocks, int gm, int &mb,
+                                        int &nb) {
+  const int g = t / (gm * n_blocks);
+  const int m0 = g * gm;
+  const int gs = min(gm, m_blocks - m0);
+  const int r = t - g * gm * n_blocks;
+  nb = r / gs;
+  mb = m0 + r % gs;
+}
+
+// nnz and the K slots (idx bytes, bf16 value pairs) of the TwELL tile that
+// holds column col of row tok; the slot words are read even when the tile
+// overflowed (then unused), so no load waits on another.
+__device__ __forceinline__ void fetch_slots(const TcParams &p, int col, int tok, int &nz,
+                                            uint32_t (&iw)[8], uint32_t (&vw)[16]) {
+  const size_t jt = (size_t)(col / p.C) * p.Tn + tok;
+  nz = p.nnz[jt];
+  load_slots(p.idx + jt * p.Kslots, p.val + jt * p.Kslots, p.Kslots, iw, vw);
+}
+
 template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -292,8 +318,8 @@ struct Cfg {
   // EPI_PACK: per row idx (32 B) + bf16 val (64 B) slots, K <= 32, and a
   // 32-column bf16 staging row (64 B)
   static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64
-                                    : EPI == EPI_U  ? 128 * 64   // a 32-column bf16 g row
-                                    : EPI == EPI_DH ? 128 * 128  // and g, u rows
+                                    : EPI == EPI_U  ? 128 * GZ_STRIDE * 2  // a 32-column bf16 g row
+                                    : EPI == EPI_DH ? 128 * GZ_STRIDE * 4  // g and u rows
                                                     : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
   static_assert(STAGES >= 2, "too few stages");
@@ -340,6 +366,17 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
   const int KT1 = (Kd + BK - 1) / BK;
   const int NR = EPI == EPI_DX ? (p.gated ? 4 : 2) : (EPI == EPI_DW ? 2 : 1);
   const int KT = NR * KT1;
+  // Tile order.  When B is larger than half of L2, groups of gm M-blocks,
+  // and within a group all N-blocks with the M-blocks innermost: the CTAs in
+  // flight then share a group's A rows (about 32 MB) and a few B tiles, and
+  // each pass over B serves gm M-blocks from L2 (d_model 4096 / d_ff 14336:
+  // B = W is 117 MB, streamed ~25 times per launch M-block by M-block,
+  // twice grouped; gate GEMM 0.68 -> 0.53 ms).  A B that stays in L2 keeps
+  // the plain M-block-major order (gm = 1), measured slightly faster there.
+  const double b_bytes = (double)p.N * NB * BK * 2.0 * (double)KT;
+  const int gm = b_bytes > 0.5 * (double)p.l2_bytes
+                     ? max(1, min(m_blocks, (32 << 20) / (BM * 2 * BK * max(KT, 1))))
+                     : 1;
   if ((int)blockIdx.x >= num_tiles || KT == 0) return;  // uniform for the CTA
 
   if (threadIdx.x == 0) {
@@ -378,8 +415,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int q = tile / tiles_q, tq = tile - q * tiles_q;
-        const int mb = tq / n_blocks, nb = tq % n_blocks;
+        const int q = tile / tiles_q;
+        int mb, nb;
+        tile_mn(tile - q * tiles_q, m_blocks, n_blocks, gm, mb, nb);
         // EPI_DW: this problem's A, and B = x (or dy for the last problem)
         const CUtensorMap *aq = EPI == EPI_DW ? &maps.a[q] : amap0;
         const int bq = (EPI == EPI_DW && q == NQ - 1) ? 2 : 0;
@@ -494,8 +532,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
     const int et = threadIdx.x - 64;        // 0..127 among epilogue threads
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-      const int q = tile / tiles_q, tq = tile - q * tiles_q;
-      const int mb = tq / n_blocks, nb = tq % n_blocks;
+      const int q = tile / tiles_q;
+      int mb, nb;
+      tile_mn(tile - q * tiles_q, m_blocks, n_blocks, gm, mb, nb);
       const int buf = lt & 1;
       const uint32_t use = (uint32_t)(lt >> 1);
       const int n0 = nb * BN;
@@ -506,6 +545,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         epi_bar();
         for (int c = et; c < BN; c += 128) s_bias[c] = (n0 + c < p.N) ? p.bg[n0 + c] : 0.f;
         epi_bar();
+      }
+      // EPI_U / EPI_DH: the slots of the tile's first TwELL tile are fetched
+      // while the accumulator is still being computed (they do not depend on
+      // it); EPI_DH also fetches u at the slots, and rows with a dense backup
+      // row (ps >= 0) read that instead
+      constexpr bool SLOTS = EPI == EPI_U || EPI == EPI_DH;
+      const int tok_u = (SLOTS && row_ok) ? (dense_all ? m : p.rows[m]) : 0;
+      const int ps_u = (EPI == EPI_DH && row_ok) ? p.pos[tok_u] : -1;
+      int pf_nz = 0;
+      uint32_t pf_iw[8], pf_vw[16], pf_qw[16];
+      if (SLOTS && row_ok && ps_u < 0) {
+        fetch_slots(p, n0, tok_u, pf_nz, pf_iw, pf_vw);
+        if (EPI == EPI_DH && p.gated)
+          load_vals(p.uval + ((size_t)(n0 / p.C) * p.Tn + tok_u) * p.Kslots, p.Kslots, pf_qw);
       }
       const bool ok = mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status);
       if (!ok) break;
@@ -657,28 +710,33 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         // recomputed but read back from what the gate epilogue stored (the
         // bf16 value of every active entry: the wide tile of an overflowing
         // (row, tile), else the TwELL slots), so this GEMM does half the work
-        // of the gate + up one.  Stores as EPI_GU.
-        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
+        // of the gate + up one.  The slots of the next TwELL tile are fetched
+        // while the current one is processed; each 32-column block scatters
+        // them branch-free (an entry outside the block goes to a spare
+        // element).  Stores as EPI_GU.
+        const int tok = tok_u;
         const int ps = row_ok ? (dense_all ? p.pos[tok] : m) : -1;
         const bool fb_ok = ps >= 0 && ps < p.cap;
         const int K = p.Kslots;
-        bf16 *gz = (bf16 *)s_slots + row * 32;  // this row's g for the current 32 columns
-        // the slots of the current (row, tile), loaded once per tile with
-        // vector loads: idx bytes and bf16 values
-        int cur_j = -1, nz = 0;
+        bf16 *gz = (bf16 *)s_slots + row * GZ_STRIDE;  // this row's g for the current 32 columns
+        const int n_end = min(n0 + BN, p.N);
+        int nz = 0;
         uint32_t iw[8], vw[16];
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float zu[32];
           tmem_ld32(tacc + c0, zu);
           if (!row_ok || n0 + c0 >= p.N) continue;
-          const int j = (n0 + c0) / p.C, cl = (n0 + c0) % p.C;
-          const size_t jt = (size_t)j * p.Tn + tok;
-          if (j != cur_j) {
-            cur_j = j;
-            nz = p.nnz[jt];
-            if (nz <= K) load_slots(p.idx + jt * K, p.val + jt * K, K, iw, vw);
+          const int cl = (n0 + c0) % p.C;
+          if (cl == 0) {  // a new TwELL tile: take the fetched slots, fetch the next tile's
+            nz = pf_nz;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) iw[i] = pf_iw[i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) vw[i] = pf_vw[i];
+            if (n0 + c0 + p.C < n_end) fetch_slots(p, n0 + c0 + p.C, tok, pf_nz, pf_iw, pf_vw);
           }
           if (nz > K) {
+            const size_t jt = (size_t)((n0 + c0) / p.C) * p.Tn + tok;
             const uint4 *wr = (const uint4 *)(p.wide + jt * p.C + cl);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) ((uint4 *)gz)[v4] = wr[v4];
@@ -687,10 +745,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             for (int v4 = 0; v4 < 4; ++v4) ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              if (k < nz) {
-                const int c = slot_col(iw, k) - cl;
-                if ((unsigned)c < 32u) gz[c] = __ushort_as_bfloat16(slot_val(vw, k));
-              }
+              if (k >= K) break;  // uniform
+              const int c = slot_col(iw, k) - cl;
+              const bool in = k < nz && (unsigned)c < 32u;
+              gz[in ? c : 32] = __ushort_as_bfloat16(slot_val(vw, k));
             }
           }
           uint32_t hw[16], uw[16];
@@ -739,12 +797,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         // gather path), hi at row m and lo at row Tp + m of p.dz2 / p.du2 /
         // p.h2.  Rows past the last one (inside this tile) are written as
         // zeros: the weight-gradient GEMMs contract over them.
-        const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
-        const int ps = row_ok ? p.pos[tok] : -1;
+        const int tok = tok_u;
+        const int ps = ps_u;
         const int K = p.Kslots;
-        bf16 *gz = (bf16 *)s_slots + row * 64, *uz = gz + 32;  // g, u of 32 columns
-        int cur_j = -1, nz = 0;
-        uint32_t iw[8], vw[16], qw[16];
+        bf16 *gz = (bf16 *)s_slots + row * 2 * GZ_STRIDE, *uz = gz + GZ_STRIDE;  // g, u of 32 columns
+        // (one set of slot registers: the first TwELL tile's were fetched
+        // before the accumulator wait, a later tile's are fetched when the
+        // tile starts; two sets would not fit the register budget)
         for (int c0 = 0; c0 < BN; c0 += 32) {
           float v[32];
           tmem_ld32(tacc + c0, v);
@@ -765,14 +824,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
                 ua[4 * v4] = uv.x; ua[4 * v4 + 1] = uv.y; ua[4 * v4 + 2] = uv.z; ua[4 * v4 + 3] = uv.w;
               }
             } else {  // slots (every tile of the row holds at most K)
-              const int j = (n0 + c0) / p.C, cl = (n0 + c0) % p.C;
-              const size_t jt = (size_t)j * p.Tn + tok;
-              if (j != cur_j) {
-                cur_j = j;
-                nz = min((int)p.nnz[jt], K);
-                load_slots(p.idx + jt * K, p.val + jt * K, K, iw, vw);
-                if (p.gated) load_vals(p.uval + jt * K, K, qw);
+              const int cl = (n0 + c0) % p.C;
+              if (cl == 0 && c0 > 0) {  // a later TwELL tile
+                fetch_slots(p, n0 + c0, tok, pf_nz, pf_iw, pf_vw);
+                if (p.gated)
+                  load_vals(p.uval + ((size_t)((n0 + c0) / p.C) * p.Tn + tok) * K, K, pf_qw);
               }
+              const int nz = min(pf_nz, K);
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4) {
                 ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
@@ -780,13 +838,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
               }
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
-                if (k < nz) {
-                  const int c = slot_col(iw, k) - cl;
-                  if ((unsigned)c < 32u) {
-                    gz[c] = __ushort_as_bfloat16(slot_val(vw, k));
-                    if (p.gated) uz[c] = __ushort_as_bfloat16(slot_val(qw, k));
-                  }
-                }
+                if (k >= K) break;  // uniform
+                const int c = slot_col(pf_iw, k) - cl;
+                const int e = (k < nz && (unsigned)c < 32u) ? c : 32;  // 32: spare element
+                gz[e] = __ushort_as_bfloat16(slot_val(pf_vw, k));
+                uz[e] = __ushort_as_bfloat16(slot_val(pf_qw, k));
               }
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4) {
@@ -905,6 +961,17 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
 }
 
 // ------------------------------------------------------------------ host --
+long long l2_size() {
+  static long long n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) n = v;
+  });
+  return n;
+}
+
 int num_sms() {
   static int n = 0;
   static std::once_flag once;
@@ -966,7 +1033,9 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cuda
   }
   int grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  launch_k(kern, grid, NTHREADS, CF::SMEM, s, maps, p);
+  TcParams q = p;
+  q.l2_bytes = l2_size();
+  launch_k(kern, grid, NTHREADS, CF::SMEM, s, maps, q);
   return cudaGetLastError();
 }
 

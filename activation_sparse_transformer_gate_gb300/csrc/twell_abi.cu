@@ -158,18 +158,6 @@ twell_status check_ws(void *ws, size_t ws_bytes, const Workspace &need) {
 }
 
 float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_switch : 0.5f; }
-// L2 bytes of the current device (queried once).
-size_t l2_bytes() {
-  static size_t n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) n = v;
-  });
-  return n;
-}
-
 // Slot density above which a call runs every row densely: the caller's
 // dense_density when > 0, none when < 0, else the default crossover of the
 // measured costs.  Per active (token, neuron) the forward gathers a W_up and
@@ -186,7 +174,7 @@ float density_of(const twell_t *tw, int D, int gated, bool backward) {
   if (tw->dense_density < 0.f) return -1.f;
   const size_t es = tw->dtype == TWELL_BF16 ? 2 : 4;
   const double wbytes = (double)(gated ? 2 : 1) * (double)tw->F * (double)D * (double)es;
-  const double l2 = (double)l2_bytes();
+  const double l2 = (double)l2_size();
   double d = 0.013;
   if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
   if (backward) d *= 1.47;
