@@ -246,7 +246,19 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": float(np.sum(v)) / prof_steps} for k, v in per.items()}
 
     nnz = bufs.nnz.cpu().numpy().astype(np.int64)
-    rl = kernel_rooflines(kern, w, nnz, train)
+    # rows the dispatcher sent to the dense path (control block: n_rows), of
+    # a lone forward and of the backward that follows it
+    tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, int(train),
+                         bufs.t, y, ws, nws, sh)
+    torch.cuda.synchronize(dev)
+    rows_f = int(ws[:4].view(torch.int32).item())
+    rows_b = 0
+    if train:
+        tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], w.lam, D, dx,
+                              dWg, dbg, dWu, dWd, ws, nws, sh)
+        torch.cuda.synchronize(dev)
+        rows_b = int(ws[:4].view(torch.int32).item())
+    rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b)
     dominant = max((k for k in kern if k in rl), key=lambda k: kern[k]["ms_per_step"], default=None)
     roof = None
     if dominant:
@@ -342,10 +354,13 @@ def gather_ceiling(torch, lib, dev, W, w, pairs, timed, sh):
     return pairs * row_bytes / (ms / 1e3) / 1e9
 
 
-def kernel_rooflines(kern, w, nnz, train):
+def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0):
     """Achieved rate of each kernel from its algorithmic work per launch:
     bytes for the gather kernels (rows gathered + rows streamed + TwELL),
-    flops for the gate GEMM.  See the design notes for the per-unit figures."""
+    flops for the gate GEMM and for the dense-path GEMMs (rows_f / rows_b
+    rows of the forward / backward; the backward's dx and dW contractions
+    take dz, du, h as hi + lo parts, counted as executed).  See the design
+    notes for the per-unit figures."""
     peaks = load_peaks()
     D, F, T, K = w.D, w.F, w.T, w.K
     row_ovf = (nnz > K).any(axis=0)
@@ -353,18 +368,38 @@ def kernel_rooflines(kern, w, nnz, train):
     pairs = int(np.minimum(nnz, K)[:, ~row_ovf].sum())          # pairs of TwELL rows
     pairs_all = int(nnz.sum())                                    # incl. overflow rows
     twell = (F // w.C) * T * (3 * K + 1)
+
+    def gathered(rows):
+        """Pairs and tokens the gather kernels take when `rows` rows are on
+        the dense path (all: none; the overflow rows: the TwELL rows only)."""
+        if rows >= T:
+            return 0, 0
+        if rows > 0:
+            return pairs, sparse_rows
+        return pairs_all, T
+
+    pf, tf = gathered(rows_f)
+    pb, tb = gathered(rows_b)
     wrk = {
         # per pair: W_up + W_down rows; per token: x row in, y row out; TwELL read
-        "twell_updown_fused": ("hbm", pairs_all * 2 * D * 2 + T * D * 2 * 2 + twell),
+        "twell_updown_fused": ("hbm", (pf * 2 * D * 2 + tf * D * 2 * 2 + twell) if tf else 0),
         # dh SDDMM: per pair a W_down row, u in and dz/du/h out; per token the dy row
-        "bwd_slots_sddmm": ("hbm", pairs_all * (D * 2 + 14) + T * D * 2),
+        "bwd_slots_sddmm": ("hbm", pb * (D * 2 + 14) + tb * D * 2),
         # dx SpMM: per pair W_gate + W_up rows and dz/du in; per token the dx row out
-        "bwd_dx_spmm": ("hbm", pairs_all * (2 * D * 2 + 8) + T * D * 2),
+        "bwd_dx_spmm": ("hbm", pb * (2 * D * 2 + 8) + tb * D * 2),
         # per pair: x + dy rows and its 16-byte list record {token, dz, du, h};
         # 3 fp32 dW rows and dbg out
-        "bwd_dw_gather": ("hbm", pairs_all * (2 * D * 2 + 16) + 3 * F * D * 4 + F * 4),
+        "bwd_dw_gather": ("hbm", pb * (2 * D * 2 + 16) + (3 * F * D * 4 + F * 4 if tb else 0)),
         "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
     }
+    wrk = {k: v for k, v in wrk.items() if v[1] > 0}
+    ng = 3 if w.gated else 2  # dW problems (dWg, [dWu,] dWd)
+    for k, rows, mult in (("dense_rows_gate_up", rows_f, 1), ("dense_rows_down", rows_f, 1),
+                          ("bwd_dense_dh_gemm", rows_b, 1),
+                          ("bwd_dense_dx_gemm", rows_b, 4 if w.gated else 2),
+                          ("bwd_dense_dw_gemm", rows_b, 2 * ng)):
+        if rows > 0:
+            wrk[k] = ("tensor", 2.0 * mult * rows * D * F)
     out = {}
     for k, (bound, work) in wrk.items():
         if k not in kern:
@@ -377,7 +412,8 @@ def kernel_rooflines(kern, w, nnz, train):
         out[k] = dict(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak,
                       algorithmic=work, peak_source=peaks["source"])
     out.setdefault("_counts", {"bound": "-", "pairs_twell_rows": pairs, "pairs_all": pairs_all,
-                               "sparse_rows": sparse_rows})
+                               "sparse_rows": sparse_rows, "dense_path_rows_fwd": rows_f,
+                               "dense_path_rows_bwd": rows_b})
     return out
 
 
