@@ -73,6 +73,8 @@ def _load():
                                                 ctypes.c_double, P, I, P, I, P, P, P, P, P]
             lib.oracle_ffn_loss.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, ctypes.c_double]
             lib.oracle_ffn_loss.restype = ctypes.c_double
+            lib.oracle_rowell_pack.argtypes = [I, I, I, P, P, P, P]
+            lib.oracle_ffn_rowell.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -204,3 +206,25 @@ def ffn_loss(x, Wg, bg, rb, Wu, Wd, dy, lam: float, dt: str, q: str) -> float:
     return float(_load().oracle_ffn_loss(T, D, F, DT[dt], QMODE[q], _p(x), _p(Wg),
                                          _p(_c(bg, np.float32)), _p(_c(rb, np.float32)),
                                          _p(Wu), _p(Wd), _p(dy), float(lam)))
+
+
+def rowell_pack(h: np.ndarray, E: int) -> dict:
+    """Classic row-ELL of a dense activation matrix h [T][F] (entries >= 0)."""
+    h = _c(h, np.float64)
+    T, F = h.shape
+    idx = np.empty((T, E), dtype=np.uint16)
+    val = np.empty((T, E), dtype=np.float64)
+    nnz = np.empty((T,), dtype=np.int32)
+    _load().oracle_rowell_pack(T, F, E, _p(h), _p(idx), _p(val), _p(nnz))
+    return dict(idx=idx, val=val, nnz=nnz, T=T, F=F, E=E)
+
+
+def ffn_rowell(x, Wu, Wd, re: dict, dt: str) -> np.ndarray:
+    """y = up + down projection from row-ELL gate values."""
+    x, Wu, Wd = (_storage(a, dt) for a in (x, Wu, Wd))
+    T, D = x.shape
+    y = np.empty((T, D), dtype=np.float64)
+    _load().oracle_ffn_rowell(T, D, re["E"], DT[dt], _p(x), _p(Wu), _p(Wd),
+                              _p(_c(re["idx"], np.uint16)), _p(_c(re["val"], np.float64)),
+                              _p(_c(re["nnz"], np.int32)), _p(y))
+    return y

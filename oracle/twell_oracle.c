@@ -278,6 +278,52 @@ void oracle_ffn_twell(int T, int D, int F, int C, int K, int dt, const void *x, 
   }
 }
 
+/* Classic row-ELL, the comparison format (section 2.A contrasts TwELL with
+ * ELLPACK): for each row, the positive entries of a dense activation matrix
+ * h [T][F] (entries >= 0, stored values) over the whole hidden axis, in
+ * ascending column order, padded to E entries (index 0xFFFF, value +0); nnz
+ * = the row's true count; entries past E are dropped. */
+void oracle_rowell_pack(int T, int F, int E, const double *h, uint16_t *idx, double *val,
+                        int32_t *nnz) {
+  for (int t = 0; t < T; ++t) {
+    int cnt = 0;
+    for (int k = 0; k < E; ++k) {
+      idx[(size_t)t * E + k] = 0xFFFF;
+      val[(size_t)t * E + k] = 0.0;
+    }
+    for (int n = 0; n < F; ++n) {
+      double v = h[(size_t)t * F + n];
+      if (!(v > 0.0)) continue;
+      if (cnt < E) {
+        idx[(size_t)t * E + cnt] = (uint16_t)n;
+        val[(size_t)t * E + cnt] = v;
+      }
+      ++cnt;
+    }
+    nnz[t] = cnt;
+  }
+}
+
+/* Up + down projection from row-ELL gate values (section 2.B inference, with
+ * the row-ELL format): y[t] = sum over the row's first min(nnz, E) entries,
+ * ascending, of h * W_down[n], h = g * (x[t] . W_up[n]) (gated) or g. */
+void oracle_ffn_rowell(int T, int D, int E, int dt, const void *x, const void *Wu,
+                       const void *Wd, const uint16_t *idx, const double *val,
+                       const int32_t *nnz, double *y) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double *yt = y + (size_t)t * D;
+    for (int d = 0; d < D; ++d) yt[d] = 0.0;
+    int m = nnz[t] < E ? nnz[t] : E;
+    for (int k = 0; k < m; ++k) {
+      int n = idx[(size_t)t * E + k];
+      double hh = val[(size_t)t * E + k];
+      if (Wu) hh *= dot(x, dt, (size_t)t * D, Wu, dt, (size_t)n * D, D);
+      for (int d = 0; d < D; ++d) yt[d] += hh * ld(Wd, dt, (size_t)n * D + d);
+    }
+  }
+}
+
 /* Backward of the FFN with the L1 term (section 2.B training):
  *   L = sum_t dy[t] . y[t] + lambda * sum_{t,n} |h[t][n]|
  *   dh  = dy[t] . Wd[n] + lambda * sign(h)
