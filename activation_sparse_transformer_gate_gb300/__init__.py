@@ -8,8 +8,10 @@ without it raises instead of falling back to anything else.
 
 Names follow the ABI: ``twell_workspace_size``, ``twell_pack_dense``,
 ``twell_pack``, ``twell_ffn_forward``, ``twell_ffn_backward``,
-``twell_get_status``.  ``TwellBuffers`` allocates the device buffers of a
-``twell_t`` with torch.
+``twell_get_status``, and the row-ELL comparison baseline
+``twell_rowell_pack_dense`` / ``twell_rowell_forward``.  ``TwellBuffers`` and
+``RowEllBuffers`` allocate the device buffers of a ``twell_t`` /
+``twell_rowell_t`` with torch.
 """
 from __future__ import annotations
 
@@ -31,7 +33,8 @@ TWELL_ERR = {
 TWELL_F32, TWELL_BF16 = 0, 1
 
 EXPORTS = ("twell_workspace_size", "twell_pack_dense", "twell_pack", "twell_ffn_forward",
-           "twell_ffn_backward", "twell_get_status", "twell_version")
+           "twell_ffn_backward", "twell_get_status", "twell_version", "twell_rowell_pack_dense",
+           "twell_rowell_forward")
 
 
 class TwellError(RuntimeError):
@@ -49,6 +52,15 @@ class twell_t(ctypes.Structure):
         ("g_fb", ctypes.c_void_p), ("u_val", ctypes.c_void_p), ("u_fb", ctypes.c_void_p),
         ("status", ctypes.c_void_p), ("dense_switch", ctypes.c_float),
         ("dense_density", ctypes.c_float),
+    ]
+
+
+class twell_rowell_t(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("F", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("idx", ctypes.c_void_p), ("val", ctypes.c_void_p), ("nnz", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
     ]
 
 
@@ -75,8 +87,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.twell_ffn_backward.argtypes = [P, P, P, P, TP, P, F32, I, P, P, P, P, P, P, S, P]
     lib.twell_get_status.argtypes = [TP, P, ctypes.POINTER(ctypes.c_int32)]
     lib.twell_version.restype = ctypes.c_char_p
+    RP = ctypes.POINTER(twell_rowell_t)
+    lib.twell_rowell_pack_dense.argtypes = [P, RP, P]
+    lib.twell_rowell_forward.argtypes = [P, P, P, I, RP, P, P]
     for name in ("twell_pack_dense", "twell_pack", "twell_ffn_forward", "twell_ffn_backward",
-                 "twell_get_status"):
+                 "twell_get_status", "twell_rowell_pack_dense", "twell_rowell_forward"):
         getattr(lib, name).restype = I
     if path is None:
         _lib = lib
@@ -139,6 +154,16 @@ def twell_ffn_backward(x, Wg, Wu, Wd, tw: twell_t, dy, lam: float, D: int, dx, d
                                      _stream(stream)), "twell_ffn_backward")
 
 
+def twell_rowell_pack_dense(H, re: twell_rowell_t, stream=None) -> None:
+    _check(load().twell_rowell_pack_dense(_ptr(H), ctypes.byref(re), _stream(stream)),
+           "twell_rowell_pack_dense")
+
+
+def twell_rowell_forward(x, Wu, Wd, D: int, re: twell_rowell_t, y, stream=None) -> None:
+    _check(load().twell_rowell_forward(_ptr(x), _ptr(Wu), _ptr(Wd), D, ctypes.byref(re), _ptr(y),
+                                       _stream(stream)), "twell_rowell_forward")
+
+
 def twell_get_status(tw: twell_t, stream=None):
     """Returns (status_code, n_ovf); synchronises the stream."""
     n = ctypes.c_int32(0)
@@ -171,6 +196,21 @@ class TwellBuffers:
                          ovf_cap=cap, g_fb=_ptr(self.g_fb), u_val=_ptr(self.u_val),
                          u_fb=_ptr(self.u_fb), status=_ptr(self.status),
                          dense_switch=float(dense_switch), dense_density=float(dense_density))
+
+
+class RowEllBuffers:
+    """Device buffers of one twell_rowell_t (row-ELL baseline), allocated with torch."""
+
+    def __init__(self, T: int, F: int, E: int, dtype: int, device="cuda"):
+        import torch
+        tdt = torch.bfloat16 if dtype == TWELL_BF16 else torch.float32
+        self.T, self.F, self.E, self.dtype = T, F, E, dtype
+        self.idx = torch.empty((T, E), dtype=torch.int16, device=device)
+        self.val = torch.empty((T, E), dtype=tdt, device=device)
+        self.nnz = torch.empty((T,), dtype=torch.int32, device=device)
+        self.status = torch.zeros((4,), dtype=torch.int32, device=device)
+        self.t = twell_rowell_t(T=T, F=F, E=E, dtype=dtype, idx=_ptr(self.idx),
+                                val=_ptr(self.val), nnz=_ptr(self.nnz), status=_ptr(self.status))
 
 
 def workspace(T: int, D: int, F: int, C: int, K: int, dtype: int, train: bool, device="cuda"):

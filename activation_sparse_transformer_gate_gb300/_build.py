@@ -20,6 +20,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtwell.so")
 
 SOURCES = ["twell_abi.cu", "pack.cu", "simt_gemm.cu", "updown.cu", "tc_gemm.cu", "backward.cu",
+           "rowell.cu",
            "static_split.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

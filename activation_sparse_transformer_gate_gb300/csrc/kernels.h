@@ -131,11 +131,20 @@ enum KernelId {
   KID_BWD_DENSE_DX = 15,
   KID_BWD_DENSE_DW = 16,
   KID_BWD_PREP = 17,
-  KID_COUNT = 18
+  KID_ROWELL_PACK = 18,
+  KID_ROWELL_UPDOWN = 19,
+  KID_COUNT = 20
 };
 // Record a timing event after `launches` kernel launches of component `id`
 // (no-op unless enabled).
 void prof_mark(int id, cudaStream_t s, int launches = 1);
+
+// rowell.cu (row-ELL comparison baseline)
+cudaError_t launch_rowell_pack_dense(const void *H, int T, int F, int E, int dtype, uint16_t *idx,
+                                     void *val, int32_t *nnz, int32_t *status, cudaStream_t s);
+cudaError_t launch_rowell_updown(const void *x, const void *Wu, const void *Wd, int T, int D,
+                                 int F, int E, int dtype, const uint16_t *idx, const void *val,
+                                 const int32_t *nnz, void *y, cudaStream_t s);
 
 // updown.cu
 cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);

@@ -62,7 +62,7 @@ static const char *kKernelNames[KID_COUNT] = {
     "dense_rows_gate_up",   "dense_rows_down",  "pack_dense",         "copy_fb_rows",
     "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
     "bwd_dense_dh_gemm",    "fill_u_slots",     "assemble_fb_rows",   "bwd_dense_dx_gemm",
-    "bwd_dense_dw_gemm",    "bwd_prep_rows"};
+    "bwd_dense_dw_gemm",    "bwd_prep_rows",    "rowell_pack_dense",  "rowell_updown"};
 
 Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
   Workspace w;
@@ -343,6 +343,47 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   a.dense_density = density_of(tw, D, gated, true);
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
   return cuda_status(launch_backward(a, (cudaStream_t)stream));
+}
+
+static twell_status check_rowell(const twell_rowell_t *re) {
+  if (!re) return TWELL_ERR_ARG;
+  if (re->dtype != TWELL_F32 && re->dtype != TWELL_BF16) return TWELL_ERR_DTYPE;
+  if (re->T < 1 || re->F < 32 || re->F % 32 != 0 || re->F > 65535 || re->E < 1)
+    return TWELL_ERR_ARG;
+  if ((double)re->T * (double)re->E >= 2147483647.0) return TWELL_ERR_ARG;
+  if (!re->idx || !re->val || !re->nnz || !re->status) return TWELL_ERR_ARG;
+  if (!aligned16(re->val)) return TWELL_ERR_ALIGN;
+  return TWELL_OK;
+}
+
+twell_status twell_rowell_pack_dense(const void *H, twell_rowell_t *re, void *stream) {
+  twell_status st = check_rowell(re);
+  if (st != TWELL_OK) return st;
+  if (!H) return TWELL_ERR_ARG;
+  if (!aligned16(H)) return TWELL_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  prof_mark(KID_START, s);
+  cudaError_t e = launch_rowell_pack_dense(H, re->T, re->F, re->E, re->dtype, re->idx, re->val,
+                                           re->nnz, re->status, s);
+  prof_mark(KID_ROWELL_PACK, s);
+  return cuda_status(e);
+}
+
+twell_status twell_rowell_forward(const void *x, const void *Wu, const void *Wd, int D,
+                                  const twell_rowell_t *re, void *y, void *stream) {
+  twell_status st = check_rowell(re);
+  if (st != TWELL_OK) return st;
+  if (!x || !Wd || !y) return TWELL_ERR_ARG;
+  const size_t es = re->dtype == TWELL_BF16 ? 2 : 4;
+  if (D < 8 || (D * es) % 16 != 0 || D * es > 16384) return D < 8 ? TWELL_ERR_ARG : TWELL_ERR_ALIGN;
+  if (!aligned16(x) || !aligned16(Wd) || !aligned16(y) || (Wu && !aligned16(Wu)))
+    return TWELL_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  prof_mark(KID_START, s);
+  cudaError_t e = launch_rowell_updown(x, Wu, Wd, re->T, D, re->F, re->E, re->dtype, re->idx,
+                                       re->val, re->nnz, y, s);
+  prof_mark(KID_ROWELL_UPDOWN, s);
+  return cuda_status(e);
 }
 
 int twell_profile_begin(void) {

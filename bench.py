@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-energy", action="store_true",
                     help="skip the saved-memory and energy-per-token leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--compare-formats", action="store_true",
+                    help="forward: TwELL against classic row-ELL and against an unfused pack "
+                         "(dense gate GEMM + standalone conversion), same inputs")
     ap.add_argument("--dense-density", type=float, default=0.0,
                     help="the dispatcher's density threshold (0: the library default; "
                          "< 0: off; a tiny value forces the all-dense path)")
@@ -280,6 +283,8 @@ def run_ours(args, rank, world, local_rank):
             roof["frac_of_l2_gather"] = round(roof["achieved"] / gceil, 4)
 
     dense = None if args.no_dense else dense_reference(torch, d, w, train, timed, args)
+    formats = (format_comparison(torch, lib, d, w, bufs, ws, nws, y, sh, timed, args)
+               if (args.compare_formats and not train and w.gated) else None)
     e2e = None if args.no_e2e else end_to_end(torch, d, step, y, dx, w, train, timed, args)
     mem = energy = None
     if not args.no_energy:
@@ -309,6 +314,8 @@ def run_ours(args, rank, world, local_rank):
         "memory": mem,
         "energy": energy,
     }
+    if formats:
+        line["format_comparison"] = formats
     if dense:
         line["dense_cublas"] = dense
         line["speedup_vs_dense"] = round(dense["ms_per_step"] / ms_step, 4)
@@ -589,6 +596,65 @@ def dense_reference(torch, d, w, train, timed, args):
     return {"ms_per_step": round(ms, 5), "tokens_per_s": round(w.T / (ms / 1e3), 1),
             "what": "torch bf16 matmul (cuBLAS) dense FFN" + (" fwd+bwd" if train else " fwd"),
             "steps": steps}
+
+
+def format_comparison(torch, lib, d, w, bufs, ws, nws, y, sh, timed, args):
+    """What the TwELL format and its fused pack buy, on the same inputs
+    (forward).  Times, with cold L2 before each step:
+      twell_fused_pack: twell_pack (gate GEMM with the ReLU + TwELL epilogue,
+        overflow list, backup rows);
+      twell_unfused_pack: the gate GEMM writing the dense activation matrix
+        H (cuBLAS through torch, bias, ReLU, bf16) + twell_pack_dense(H);
+      twell_forward: twell_ffn_forward (gate + pack + up/down);
+      rowell_forward: H as above + row-ELL pack (width E = the densest row)
+        + the row-ELL up/down projection.
+    and the bytes each format keeps (indices, values, counts)."""
+    import activation_sparse_transformer_gate_gb300 as tw
+    T, D, F = w.T, w.D, w.F
+    H = torch.empty((T, F), dtype=torch.bfloat16, device=d["x"].device)
+
+    bg16 = d["bg"].to(torch.bfloat16)
+
+    def gate_dense():  # cuBLAS GEMM with the bias (bf16 out), row bias + ReLU in one pass
+        z = torch.addmm(bg16, d["x"], d["Wg"].t())
+        if d["rb"] is not None:
+            z = z.float() + d["rb"][:, None]
+        H.copy_(torch.relu(z).to(torch.bfloat16))
+
+    # width of row-ELL: the densest row of this input
+    tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 0, bufs.t, y,
+                         ws, nws, sh)
+    gate_dense()
+    torch.cuda.synchronize()
+    E = int((H > 0).sum(dim=1).max().item())
+    re = tw.RowEllBuffers(T, F, E, tw.TWELL_BF16, device=d["x"].device)
+    y2 = torch.empty_like(y)
+
+    legs = {
+        "twell_fused_pack": lambda: tw.twell_pack(d["x"], d["Wg"], d["bg"], d["rb"], D, bufs.t,
+                                                  ws, nws, sh),
+        "twell_unfused_pack": lambda: (gate_dense(), tw.twell_pack_dense(H, bufs.t, sh)),
+        "twell_forward": lambda: tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"],
+                                                      d["Wd"], D, 0, bufs.t, y, ws, nws, sh),
+        "rowell_forward": lambda: (gate_dense(), tw.twell_rowell_pack_dense(H, re.t, sh),
+                                   tw.twell_rowell_forward(d["x"], d["Wu"], d["Wd"], D, re.t, y2,
+                                                           sh)),
+    }
+    out = {}
+    steps = max(10, min(args.steps, 100))
+    for k, fn in legs.items():
+        for _ in range(3):
+            fn()
+        out[k] = {"ms": round(timed(fn, steps) / steps, 5)}
+    code = int(re.status[0].item())
+    nt = F // w.C
+    out["bytes"] = {"twell_idx_val_nnz": nt * T * w.K * 3 + nt * T,
+                    "rowell_idx_val_nnz": T * E * 4 + T * 4, "rowell_width_E": E,
+                    "twell_K_per_tile": w.K, "dense_H": T * F * 2}
+    out["rowell_status"] = code
+    out["note"] = ("the unfused legs round z + bias to bf16 before the ReLU (a cuBLAS GEMM "
+                   "output), so their activations differ slightly from the fused epilogue's")
+    return out
 
 
 def end_to_end(torch, d, step, y, dx, w, train, timed, args):

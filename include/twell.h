@@ -181,6 +181,37 @@ twell_status twell_get_status(const twell_t *tw, void *stream, int32_t *n_ovf);
 #define TWELL_STATIC_SPLIT_MAX_T 262144
 twell_status twell_hybrid_split_static(twell_t *tw, void *stream);
 
+/* Comparison baseline (not on the TwELL path): classic row-ELL, the format
+ * the technical summary (section 2.A) contrasts TwELL with.  One list per
+ * row over the whole hidden axis, padded to a common width E:
+ *   idx [T][E]  uint16 global hidden column, ascending; pad 0xFFFF
+ *   val [T][E]  dtype, the activation value; pad +0
+ *   nnz [T]     int32, the row's TRUE number of positive values
+ * A row spans every N-tile of the gate matmul, so row-ELL cannot be written
+ * in its epilogue: it is packed from a dense activation matrix by a separate
+ * pass.  Rows with more than E positive values keep their first E (nnz stays
+ * true) and TWELL_ERR_CAPACITY goes to *status; a caller who wants no loss
+ * picks E = the densest row's count.  F <= 65535. */
+typedef struct {
+  int32_t T, F, E;        /* tokens, hidden width, entries per row          */
+  int32_t dtype;          /* twell_dtype of val                              */
+  uint16_t *idx;          /* [T][E]                                          */
+  void *val;              /* [T][E]                                          */
+  int32_t *nnz;           /* [T]                                             */
+  int32_t *status;        /* device int32 (first error wins)                 */
+} twell_rowell_t;
+
+/* Pack a dense activation matrix H [T][F] (dtype = re->dtype, entries >= 0;
+ * entries > 0 are active) into row-ELL. */
+twell_status twell_rowell_pack_dense(const void *H, twell_rowell_t *re, void *stream);
+
+/* y [T][D] = sum over each row's entries of h W_down[n], with h = g u,
+ * u = x . W_up[n] (gated), or h = g (Wu == NULL): the up + down projection
+ * of the FFN consuming row-ELL gate activations.  x, Wu, Wd, y as for
+ * twell_ffn_forward; D*elem_size <= 16384 bytes. */
+twell_status twell_rowell_forward(const void *x, const void *Wu, const void *Wd, int D,
+                                  const twell_rowell_t *re, void *y, void *stream);
+
 /* Optional per-launch timing, for benchmarks.  Between twell_profile_begin
  * and twell_profile_end every entry point records a CUDA event on its stream
  * before its first kernel and after each step of its launch sequence (a step
