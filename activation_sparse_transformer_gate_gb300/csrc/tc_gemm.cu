@@ -1025,12 +1025,14 @@ template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cudaStream_t s) {
   using CF = Cfg<BN, NB, B_MN, EPI, A_MN>;
   auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI, A_MN>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // once per instantiation and process (concurrent first calls from several
+  // host threads are safe)
+  static cudaError_t attr_err = cudaSuccess;
+  static std::once_flag attr_once;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   int grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
   TcParams q = p;

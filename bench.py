@@ -214,9 +214,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, total_ms, world, dev)
     clocks = sampler.stop() if sampler else None
     code, n_ovf = tw.twell_get_status(bufs.t, sh)
     if code != 0:
@@ -614,12 +612,13 @@ def format_comparison(torch, lib, d, w, bufs, ws, nws, y, sh, timed, args):
     H = torch.empty((T, F), dtype=torch.bfloat16, device=d["x"].device)
 
     bg16 = d["bg"].to(torch.bfloat16)
+    rb16 = None if d["rb"] is None else d["rb"].to(torch.bfloat16)[:, None]
 
-    def gate_dense():  # cuBLAS GEMM with the bias (bf16 out), row bias + ReLU in one pass
-        z = torch.addmm(bg16, d["x"], d["Wg"].t())
-        if d["rb"] is not None:
-            z = z.float() + d["rb"][:, None]
-        H.copy_(torch.relu(z).to(torch.bfloat16))
+    def gate_dense():  # cuBLAS GEMM with the bias into H (bf16), then row bias and ReLU in place
+        torch.addmm(bg16, d["x"], d["Wg"].t(), out=H)
+        if rb16 is not None:
+            H.add_(rb16)
+        H.relu_()
 
     # width of row-ELL: the densest row of this input
     tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 0, bufs.t, y,
@@ -713,6 +712,16 @@ def cpu_baseline(a, w, train, seconds):
             "sample": f"first {S} tokens of the workload, all {w.F} neurons, "
                       f"{'dense fwd+bwd' if train else 'dense fwd'} in fp64 C loops (OpenMP over "
                       f"tokens/neurons), {t:.1f} s"}
+
+
+def max_over_ranks(torch, value: float, world: int, device) -> float:
+    """The slowest rank's value (every rank contributes its own and receives
+    the maximum): the job takes as long as its slowest replica."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_reference(args, rank, world):

@@ -221,6 +221,22 @@ def test_bf16_dmodel_shapes(D):
     check_backward(a, w, g, 1e-3)
 
 
+@pytest.mark.parametrize("dt,D,dense", [("bf16", 8192, False), ("bf16", 8192, True),
+                                          ("f32", 4096, False)])
+def test_maximum_dmodel(dt, D, dense):
+    """The largest d_model the ABI accepts (16 KB rows), on the gather path
+    and (bf16) on the tensor-core path of every row, ragged token count."""
+    w = synth.Workload(f"bdmax{dt}", 70, D, 256, 64, 4, dt, True, -1.6, 49, hot_tokens=2,
+                       seq_len=35, hot_bias=1.5, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, dense_density=1e-6 if dense else -1.0, out=out)
+    assert g["code"] == 0 and g["n_ovf"] >= 2
+    if dense:
+        assert ctl_fields(out["ctl_bwd"])[:2] == (70, 1)
+    check_backward(a, w, g, 1e-3)
+
+
 def test_fp32_dmodel1024_exact_shapes():
     """fp32 d_model 1024: 256 vectors per row, the exact-shape dx and dW paths."""
     w = synth.Workload("bf32d1k", 96, 1024, 256, 64, 4, "f32", True, -1.7, 43, train=True)

@@ -175,6 +175,21 @@ def test_bf16_dmodel_shapes(D):
     check_forward(a, w, g)
 
 
+@pytest.mark.parametrize("dt,D", [("bf16", 8192), ("f32", 4096)])
+def test_maximum_dmodel(dt, D):
+    """The largest d_model the ABI accepts (16 KB rows: 1024 vectors), with
+    overflow rows (wide tiles) and a ragged token count; and the next size
+    up is rejected."""
+    w = synth.Workload(f"dmax{dt}", 70, D, 256, 64, 4, dt, True, -1.6, 48, hot_tokens=2,
+                       seq_len=35, hot_bias=1.5)
+    a = synth.generate(w)
+    g = run_forward(a, w)
+    assert g["code"] == 0 and g["n_ovf"] >= 2
+    check_forward(a, w, g)
+    dtype = tw.TWELL_BF16 if dt == "bf16" else tw.TWELL_F32
+    assert tw.twell_workspace_size(70, 2 * D, 256, 64, 4, dtype, 0) == 0
+
+
 def test_fp32_dmodel1024_exact_shapes():
     """fp32 d_model 1024: 256 vectors per row, the exact-shape fused path."""
     w = synth.Workload("f32d1k", 96, 1024, 256, 64, 4, "f32", True, -1.7, 33)
