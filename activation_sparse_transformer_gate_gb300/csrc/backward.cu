@@ -200,7 +200,12 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 constexpr int DH_WARPS = 8;
 constexpr int DH_CHUNK = 256;  // pairs whose partial dots are held before the finish
 
-template <int U>
+// WIDE (U even, W_down 32-byte aligned): lane q of a row group takes the
+// 32 contiguous bytes (vectors 2q, 2q + 1) of each pair of chunks in one
+// 256-bit load, so one load instruction covers 128 contiguous bytes of each
+// of its 8 rows -- half the L1 wavefronts of four lanes x 16 bytes -- and dy
+// is read at the same vectors.
+template <int U, bool WIDE>
 __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
     bwd_dh_mma_kernel(BParams p) {
   pdl_begin();
@@ -223,7 +228,8 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
   if (gemm_row(p, ps)) return;
   for (int v = tid; v < NV; v += blockDim.x) s_dy[v] = ((const uint4 *)p.dy)[(size_t)t * NV + v];
   const uint4 *Wd4 = (const uint4 *)p.Wd;
-  const uint4 *dyw = s_dy + 4 * w * CPW + q;  // this lane's dy vectors (read by lanes 0-3)
+  // this lane's dy vectors (read by lanes 0-3)
+  const uint4 *dyw = s_dy + 4 * w * CPW + (WIDE ? 2 * q : q);
   const bf16 *uval = (const bf16 *)p.u_val, *ufb = (const bf16 *)p.u_fb;
   const PairSource<bf16> src = bwd_source<bf16>(p, t, ps);
   int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
@@ -241,20 +247,30 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
       for (int pb = 0; pb < PC; pb += 16) {
         // rows g and g + 8 of the block (past the chunk: its first row, result unused)
         const int r0 = pb + gq < PC ? pb + gq : pb, r1 = pb + gq + 8 < PC ? pb + gq + 8 : pb;
-        const uint4 *w0 = Wd4 + (size_t)s_n[cb + r0] * NV + 4 * w * CPW + q;
-        const uint4 *w1 = Wd4 + (size_t)s_n[cb + r1] * NV + 4 * w * CPW + q;
+        const int lq = WIDE ? 2 * q : q;
+        const uint4 *w0 = Wd4 + (size_t)s_n[cb + r0] * NV + 4 * w * CPW + lq;
+        const uint4 *w1 = Wd4 + (size_t)s_n[cb + r1] * NV + 4 * w * CPW + lq;
         // two accumulator chains (even / odd half of each chunk)
         float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
         for (int c0 = 0; c0 < CPW; c0 += U) {
           uint4 A0[U], A1[U];
+          if (WIDE) {  // chunks (c0 + 2v, c0 + 2v + 1): vectors 8v + 2q, 8v + 2q + 1
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            A0[u] = ldg_stream(w0 + 4 * (c0 + u));
-            A1[u] = ldg_stream(w1 + 4 * (c0 + u));
+            for (int v = 0; v < U / 2; ++v) {
+              ldg_stream32(w0 + 4 * c0 + 8 * v, A0[2 * v], A0[2 * v + 1]);
+              ldg_stream32(w1 + 4 * c0 + 8 * v, A1[2 * v], A1[2 * v + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              A0[u] = ldg_stream(w0 + 4 * (c0 + u));
+              A1[u] = ldg_stream(w1 + 4 * (c0 + u));
+            }
           }
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const uint4 b = gq == 0 ? dyw[4 * (c0 + u)] : make_uint4(0, 0, 0, 0);
+            const int dv = WIDE ? 4 * c0 + 8 * (u >> 1) + (u & 1) : 4 * (c0 + u);
+            const uint4 b = gq == 0 ? dyw[dv] : make_uint4(0, 0, 0, 0);
             mma_bf16_16816(c, A0[u].x, A1[u].x, A0[u].y, A1[u].y, b.x, b.y);
             mma_bf16_16816(e, A0[u].z, A1[u].z, A0[u].w, A1[u].w, b.z, b.w);
           }
@@ -647,9 +663,14 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     // tensor-core dh SDDMM: chunks per warp = NV / 32; U of them per load
     // batch (4: three CTAs per SM, measured faster than 8 at two)
     const int cpw = NV / (4 * DH_WARPS);
-    if (cpw % 4 == 0) launch_k(bwd_dh_mma_kernel<4>, a.T, DH_WARPS * 32, 0, s, p);
-    else if (cpw % 2 == 0) launch_k(bwd_dh_mma_kernel<2>, a.T, DH_WARPS * 32, 0, s, p);
-    else launch_k(bwd_dh_mma_kernel<1>, a.T, DH_WARPS * 32, 0, s, p);
+    // 256-bit row loads need 32-byte aligned rows (the ABI promises 16)
+    const bool wide = ((uintptr_t)a.Wd & 31u) == 0 && (a.D * 2) % 32 == 0;
+    if (cpw % 4 == 0 && wide) launch_k(bwd_dh_mma_kernel<4, true>, a.T, DH_WARPS * 32, 0, s, p);
+    else if (cpw % 4 == 0) launch_k(bwd_dh_mma_kernel<4, false>, a.T, DH_WARPS * 32, 0, s, p);
+    else if (cpw % 2 == 0 && wide)
+      launch_k(bwd_dh_mma_kernel<2, true>, a.T, DH_WARPS * 32, 0, s, p);
+    else if (cpw % 2 == 0) launch_k(bwd_dh_mma_kernel<2, false>, a.T, DH_WARPS * 32, 0, s, p);
+    else launch_k(bwd_dh_mma_kernel<1, false>, a.T, DH_WARPS * 32, 0, s, p);
   } else if (bf) {
     TW_DH_T(bf16);
   } else {

@@ -64,6 +64,16 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return r;
 }
 
+// 32-byte read-only load (two 16-byte vectors; the address must be 32-byte
+// aligned): no L1 allocation, L2 policy POL.
+template <int POL = L2_NORMAL>
+__device__ __forceinline__ void ldg_stream32(const void *p, uint4 &a, uint4 &b) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p), "l"(gather_policy<POL>()));
+}
+
 // 16-byte store of a row that is not read again by the same kernel (y, dx,
 // dW rows): no L1 allocation, evict-first in L2, so the stream of outputs
 // does not displace the gathered weight rows.

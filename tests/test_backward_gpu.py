@@ -21,7 +21,16 @@ def _lib():
     tw.load()
 
 
-def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None):
+def shifted(t, elems):
+    """A copy of device tensor t whose data starts `elems` elements past an
+    allocation boundary (16-byte aligned but not 32-byte aligned for 8 bf16)."""
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    v = buf[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0):
     """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
     the density test of the dispatcher off, so that moderately dense test
     workloads still run the gather kernels; out (dict) receives the
@@ -31,6 +40,8 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None):
     dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     d = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
+    if wd_shift:
+        d["Wd"] = shifted(d["Wd"], wd_shift)
     bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density)
     ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
     y = torch.empty((T, D), dtype=tdt, device="cuda")
@@ -234,6 +245,19 @@ def test_maximum_dmodel(dt, D, dense):
     assert g["code"] == 0 and g["n_ovf"] >= 2
     if dense:
         assert ctl_fields(out["ctl_bwd"])[:2] == (70, 1)
+    check_backward(a, w, g, 1e-3)
+
+
+@pytest.mark.parametrize("shift", [0, 8])
+def test_dh_row_loads_aligned_and_16_byte_aligned(shift):
+    """The tensor-core dh SDDMM reads W_down rows with 256-bit loads when W_down
+    is 32-byte aligned and with 128-bit loads otherwise (the ABI promises 16
+    bytes): both give the oracle's gradients."""
+    w = synth.Workload(f"bal{shift}", 200, 1024, 512, 128, 8, "bf16", True, -1.9, 50,
+                       hot_tokens=2, seq_len=100, hot_bias=1.5, train=True)
+    a = synth.generate(w)
+    g = run_train(a, w, 1e-3, wd_shift=shift)
+    assert g["code"] == 0
     check_backward(a, w, g, 1e-3)
 
 
