@@ -318,7 +318,7 @@ struct Cfg {
   // EPI_PACK: per row idx (32 B) + bf16 val (64 B) slots, K <= 32, and a
   // 32-column bf16 staging row (64 B)
   static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64
-                                    : EPI == EPI_U  ? 128 * GZ_STRIDE * 2  // a 32-column bf16 g row
+                                    : EPI == EPI_U  ? 128 * GZ_STRIDE * 2 + 128 * 64  // g and u rows
                                     : EPI == EPI_DH ? 128 * GZ_STRIDE * 4  // g and u rows
                                                     : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
@@ -713,7 +713,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         // of the gate + up one.  The slots of the next TwELL tile are fetched
         // while the current one is processed; each 32-column block scatters
         // them branch-free (an entry outside the block goes to a spare
-        // element).  Stores as EPI_GU.
+        // element).  Stores h and the backup rows as EPI_GU; in all-dense
+        // training also u at the slots of the non-overflow rows.
         const int tok = tok_u;
         const int ps = row_ok ? (dense_all ? p.pos[tok] : m) : -1;
         const bool fb_ok = ps >= 0 && ps < p.cap;
@@ -769,11 +770,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
-          if (dense_all && p.train) {  // u at the slots of non-overflow rows
-            uint4 *ur = (uint4 *)(p.urows + (size_t)m * p.F + n0 + c0);
+          if (dense_all && p.train && ps < 0) {
+            // all-dense training: u at this row's slots in the block (staged
+            // in shared memory to be picked by slot column)
+            bf16 *uz = (bf16 *)s_slots + 128 * GZ_STRIDE + row * 32;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
-              ur[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+              ((uint4 *)uz)[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
+            const size_t s0 = ((size_t)((n0 + c0) / p.C) * p.Tn + tok) * K;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (k >= K) break;  // uniform
+              const int c = slot_col(iw, k) - cl;
+              if (k < nz && (unsigned)c < 32u) p.uval[s0 + k] = uz[c];
+            }
           }
           if (fb_ok) {
             uint4 *gd = (uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
@@ -1056,6 +1066,7 @@ TcParams base_params(const FwdArgs &a) {
   p.Tn = a.T; p.F = a.F; p.D = a.D; p.C = a.C; p.Kslots = a.K; p.cap = a.tw.ovf_cap;
   p.gated = a.gated; p.train = a.train; p.bg = a.bg; p.rb = a.rb; p.rows = a.ws.rows;
   p.pos = a.ws.pos; p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val;
+  p.uval = (bf16 *)a.tw.u_val;
   p.ovf_bits = a.ws.ovf_bits;
   p.slots = &a.ws.ctl->slots;
   p.wide = (bf16 *)a.ws.wide;

@@ -310,7 +310,9 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
     prof_mark(KID_UPDOWN, s);
   }
   if (e == cudaSuccess) e = run_dense_rows(a, true, s);
-  if (e == cudaSuccess && a.train && a.gated) {
+  // all-dense training: u at the slots of non-overflow rows (the tensor-core
+  // up GEMM writes them in its epilogue)
+  if (e == cudaSuccess && a.train && a.gated && !use_tc(a.dtype)) {
     e = launch_fill_u_slots(a, s);
     prof_mark(KID_FILL_U, s);
   }
