@@ -619,10 +619,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // 1. hybrid split of the saved activations into this workspace, with the
   // forward's dispatcher rules when the dense-path rows have GEMMs
   prof_mark(KID_START, s);
-  cudaError_t e = launch_flags_from_nnz(a.tw, a.ws, s);
+  cudaError_t e = launch_flags_from_nnz(a.tw, a.ws.ovf_bits, a.ws.slot_parts, s);
   if (e != cudaSuccess) return e;
   e = launch_overflow_compact(a.tw, &a.ws, gemm ? a.dense_switch : 2.0f, s, /*write_user=*/false,
-                              gemm ? a.dense_density : -1.f);
+                              gemm ? a.dense_density : -1.f, a.ws.slot_parts, flags_blocks(a.T));
   if (e != cudaSuccess) return e;
   prof_mark(KID_OVERFLOW_COMPACT, s, 2);
   // 1'. dense-path rows on the tensor cores (idle when there are none):

@@ -24,6 +24,7 @@ struct Workspace {
   void *urows;        // [Tp][F] dtype (training): u rows from the dense path
   void *dyg;          // [Tp][D] dtype (training): gathered dy rows of the dense path
   float *dbg_r;       // [F] fp32 (training): dbg of the dense-path rows
+  unsigned long long *slot_parts;  // [SLOT_PARTS_MAX] per-block slot counts (backward)
   // backward scratch
   float *dz;          // [F/C][T][K] fp32: dz at the slots
   float *du;          // [F/C][T][K] fp32: du at the slots
@@ -77,11 +78,20 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // list and count.
 // dense_density > 0: all-dense also when ctl->slots (zeroed before the gate,
 // summed by its epilogue) exceeds dense_density * T * F; <= 0 ignores slots.
+// slot_parts (n_parts entries, from launch_flags_from_nnz) replaces the gate
+// epilogue's count in ctl->slots.
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user = true,
-                                    float dense_density = -1.f);
-// Overflow-row bitmap from the nnz counts (clears the bitmap first).
-cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s);
+                                    float dense_density = -1.f,
+                                    const unsigned long long *slot_parts = nullptr,
+                                    int n_parts = 0);
+// Overflow-row bitmap from the nnz counts (every word written); with
+// slot_parts, per-block slot counts (flags_blocks(T) entries, at most
+// SLOT_PARTS_MAX).
+constexpr int SLOT_PARTS_MAX = 1024;
+int flags_blocks(int T);
+cudaError_t launch_flags_from_nnz(const twell_t &tw, uint32_t *bits,
+                                  unsigned long long *slot_parts, cudaStream_t s);
 // Dense backup rows of overflow rows that do not take the dense GEMM path.
 cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s);
 // All-dense training forward: u at the slots of the non-overflow rows.

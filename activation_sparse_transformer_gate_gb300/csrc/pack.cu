@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(1024)
 overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
                      int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf, int32_t *status,
                      Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
-                     int F, float dense_switch, float dense_density) {
+                     int F, float dense_switch, float dense_density,
+                     const unsigned long long *__restrict__ slot_parts, int n_parts) {
   pdl_begin();
   __shared__ int warp_off[32];
   __shared__ int word_off[1024];
@@ -205,6 +206,11 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
     __syncthreads();
   }
   if (tid == 0) {
+    if (slot_parts) {  // slot count from per-block partial sums (else the gate epilogue's)
+      unsigned long long sl = 0;
+      for (int i = 0; i < n_parts; ++i) sl += slot_parts[i];
+      ctl->slots = sl;
+    }
     if (n_ovf) *n_ovf = running;
     if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
     write_ctl(ctl, running, Tn, F, dense_switch, dense_density);
@@ -212,11 +218,12 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
 }
 
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
-                                    cudaStream_t s, bool write_user, float dense_density) {
+                                    cudaStream_t s, bool write_user, float dense_density,
+                                    const unsigned long long *slot_parts, int n_parts) {
   if (ws) {
     launch_k(overflow_scan_kernel, 1, 1024, 0, s, ws->ovf_bits, tw.T, tw.ovf_cap,
              write_user ? tw.ovf_rows : nullptr, write_user ? tw.n_ovf : nullptr, tw.status,
-             ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density);
+             ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density, slot_parts, n_parts);
     return cudaGetLastError();
   }
   launch_k(overflow_compact_kernel, 1, 1024, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,
@@ -224,36 +231,64 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
   return cudaGetLastError();
 }
 
-// Overflow-row bitmap from nnz (a thread per (tile, row)), and the number of
-// slots in use, sum of min(nnz, K), as the gate epilogue counts it.
-__global__ void flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, long total, int Tn, int K,
-                                      uint32_t *__restrict__ bits,
-                                      unsigned long long *__restrict__ slots) {
+// Overflow-row bitmap from nnz: a block per 32-row bitmap word at a time,
+// warp g taking tiles g, g + 8, ... of the word's rows (one row per lane,
+// reads coalesced across the warp); the warps' ballots are OR-ed and the word
+// written whole (no zeroing, no atomics).  With slot_parts: each block's
+// number of slots in use, sum of min(nnz, K) as the gate epilogue counts it.
+__global__ void __launch_bounds__(256)
+    flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, int Tn, int nt, int K,
+                          uint32_t *__restrict__ bits,
+                          unsigned long long *__restrict__ slot_parts) {
   pdl_begin();
+  __shared__ uint32_t s_mask[8];
+  __shared__ unsigned long long s_part[8];
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int words = (Tn + 31) / 32;
   unsigned long long mine = 0;
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long)gridDim.x * blockDim.x) {
-    const int c = nnz[i];
-    if (c > K) {
-      const int t = (int)(i % Tn);
-      atomicOr(&bits[t >> 5], 1u << (t & 31));
+  for (int wd = blockIdx.x; wd < words; wd += gridDim.x) {  // uniform per block
+    const int t = wd * 32 + lane;
+    bool over = false;
+    if (t < Tn) {
+      for (int j = g; j < nt; j += 8) {
+        const int c = nnz[(size_t)j * Tn + t];
+        over |= c > K;
+        mine += (unsigned long long)(c < K ? c : K);
+      }
     }
-    mine += (unsigned long long)(c < K ? c : K);
+    const unsigned m = __ballot_sync(0xffffffffu, over);
+    if (lane == 0) s_mask[g] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t wm = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wm |= s_mask[i];
+      bits[wd] = wm;
+    }
+    __syncthreads();  // s_mask is rewritten for the next word
   }
+  if (!slot_parts) return;  // uniform
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) mine += __shfl_down_sync(0xffffffffu, mine, o);
-  if ((threadIdx.x & 31) == 0 && mine) atomicAdd(slots, mine);
+  if (lane == 0) s_part[g] = mine;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long b = 0;
+    for (int i = 0; i < 8; ++i) b += s_part[i];
+    slot_parts[blockIdx.x] = b;
+  }
 }
 
-cudaError_t launch_flags_from_nnz(const twell_t &tw, const Workspace &ws, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(ws.ctl, 0, sizeof(Ctl), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws.ovf_bits, 0, 4 * (((size_t)tw.T + 31) / 32), s);
-  if (e != cudaSuccess) return e;
-  const long total = (long)tw.T * (tw.F / tw.C);
-  long blocks = (total + 255) / 256;
-  if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
-  launch_k(flags_from_nnz_kernel, (unsigned)blocks, 256, 0, s, tw.nnz, total, tw.T, tw.K,
-           ws.ovf_bits, &ws.ctl->slots);
+int flags_blocks(int T) {
+  const int words = (T + 31) / 32;
+  const int cap = 4 * num_sms() < SLOT_PARTS_MAX ? 4 * num_sms() : SLOT_PARTS_MAX;
+  return words < cap ? words : cap;
+}
+
+cudaError_t launch_flags_from_nnz(const twell_t &tw, uint32_t *bits,
+                                  unsigned long long *slot_parts, cudaStream_t s) {
+  launch_k(flags_from_nnz_kernel, flags_blocks(tw.T), 256, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K,
+           bits, slot_parts);
   return cudaGetLastError();
 }
 

@@ -86,8 +86,8 @@ extern "C" twell_status twell_hybrid_split_static(twell_t *tw, void *stream) {
   ws.rows = (int32_t *)(base + kCtlBytes + kBitsBytes);
   ws.pos = (int32_t *)(base + kCtlBytes + kBitsBytes + kRowsBytes);
   cudaStream_t s = (cudaStream_t)stream;
-  // clears the bitmap, then sets the bit of every row with a tile over K
-  cudaError_t e = launch_flags_from_nnz(*tw, ws, s);
+  // the bit of every row with a tile over K (every bitmap word written)
+  cudaError_t e = launch_flags_from_nnz(*tw, ws.ovf_bits, nullptr, s);
   if (e == cudaSuccess) e = launch_overflow_compact(*tw, &ws, 2.0f, s, /*write_user=*/true);
   return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

@@ -87,6 +87,7 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.urows = take(es * Tp * F);
     w.dyg = take(es * Tp * D);
     w.dbg_r = (float *)take(4 * (size_t)F);
+    w.slot_parts = (unsigned long long *)take(8 * (size_t)SLOT_PARTS_MAX);
     const size_t slots = nt * (size_t)T * (size_t)K;
     w.dz = (float *)take(4 * slots);
     w.du = (float *)take(4 * slots);
