@@ -1,10 +1,12 @@
 // tc_gemm.cu -- tcgen05 (5th-generation tensor core) GEMM engine for the bf16
 // path, with the epilogues of the TwELL FFN:
 //   EPI_PACK : z = x Wg^T + bg + rb -> ReLU -> TwELL slots + nnz     (gate)
-//   EPI_GU   : dual B (Wg, Wu): g = ReLU(z) rounded to bf16, u, h = g*u
-//              -> h rows (+ g_fb / u_fb rows of overflow rows)       (dense rows)
+//   EPI_GU   : g = ReLU(z) rounded to bf16 (B = Wg; with a second B = Wu
+//              also u and h = g*u) -> h rows (+ g_fb / u_fb rows of overflow
+//              rows); the plain FFN's dense rows                (dense rows)
 //   EPI_DOWN : y[tok] = h Wd, Wd read MN-major straight from [F][D]   (dense rows)
-//   EPI_U    : B = Wu only, g read back from the TwELL slots / wide tiles
+//   EPI_U    : the gated FFN's dense rows: B = Wu only, g read back from the
+//              TwELL slots / wide tiles, h = g*u (+ u at the slots)   (dense rows)
 //   EPI_DH   : dh = dy Wd^T + lambda sign(h) -> dz, du, h rows (bf16 hi +
 //              lo parts) and column sums of dz                    (bwd rows)
 //   EPI_DX   : dx[tok] = dz Wg + du Wu (K ranges over the hi and lo parts,
@@ -554,7 +556,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       const int tok_u = (SLOTS && row_ok) ? (dense_all ? m : p.rows[m]) : 0;
       const int ps_u = (EPI == EPI_DH && row_ok) ? p.pos[tok_u] : -1;
       int pf_nz = 0;
-      uint32_t pf_iw[8], pf_vw[16], pf_qw[16];
+      uint32_t pf_iw[8], pf_vw[16], pf_qw[16] = {};  // (pf_qw: plain FFN leaves it zero)
       if (SLOTS && row_ok && ps_u < 0) {
         fetch_slots(p, n0, tok_u, pf_nz, pf_iw, pf_vw);
         if (EPI == EPI_DH && p.gated)

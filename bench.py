@@ -187,18 +187,23 @@ def run_ours(args, rank, world, local_rank):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
 
-    def timed(fn, steps):
+    per_step = []
+
+    def timed(fn, steps, flush=True):
         """Sum of per-step device times (CUDA events on the launching stream),
-        with the L2 flushed by a large write before every step."""
+        with the L2 flushed by a large write before every step (flush=False:
+        back to back, warm L2); the per-step times are kept in per_step."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
         for e0, e1 in evs:
-            flush_buf.fill_(1)
+            if flush:
+                flush_buf.fill_(1)
             e0.record(stream)
             fn()
             e1.record(stream)
         torch.cuda.synchronize(dev)
-        return sum(e0.elapsed_time(e1) for e0, e1 in evs)
+        per_step[:] = [e0.elapsed_time(e1) for e0, e1 in evs]
+        return sum(per_step)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -212,6 +217,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     total_ms = timed(step, args.steps)
+    step_ms = sorted(per_step)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -224,6 +230,8 @@ def run_ours(args, rank, world, local_rank):
     value = T * world / (ms_step / 1e3)
     if rank != 0:
         return None
+    n_warm = max(10, min(args.steps, 100))
+    warm_ms = timed(step, n_warm, flush=False) / n_warm
 
     # ---- per-kernel times inside the step (events on the launch stream) ----
     prof_steps = max(5, min(50, args.steps))
@@ -296,6 +304,8 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "step_ms": {"median": round(step_ms[len(step_ms) // 2], 5), "min": round(step_ms[0], 5),
+                    "warm_l2_mean": round(warm_ms, 5)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; shapes and sparsity of the pages' FFN setting)",
         "config": {"workload": describe(w, train), "T": T, "d_model": D, "d_ff": F, "tile": w.C,

@@ -190,6 +190,20 @@ def test_dense_backward_all_rows_ragged(gated):
     check_backward(a, w, g, 0.05)
 
 
+def test_fp32_dense_forward_then_gather_backward():
+    """fp32 (no tensor-core path): a forward that the density test runs
+    densely on the CUDA-core GEMMs (u at the slots filled from its u rows),
+    then the gather backward over every row."""
+    w = synth.Workload("bf32dense", 96, 256, 512, 64, 8, "f32", True, -1.64, 52, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, dense_density=1e-6, out=out)
+    assert g["code"] == 0
+    assert ctl_fields(out["ctl"])[1] == 1       # the forward ran densely
+    assert ctl_fields(out["ctl_bwd"])[:2] == (0, 0)  # the backward gathered
+    check_backward(a, w, g, 1e-3)
+
+
 def test_dense_backward_l1_and_zero_down_weight():
     """All-dense backward with W_down = 0: dh is the L1 term alone, so
     dbg[n] = lambda * sum over active tokens of |u| (gated) exactly as on
