@@ -16,9 +16,9 @@
 //      SpMM).  Pairs come from the TwELL slots, or from the dense backup row
 //      of an overflow row.  Two passes keep each pass's working set (one or
 //      two weight matrices) small enough to stay in L2.
-//   3. a CTA per (tile, chunk of 1024 tokens), two passes: deterministic
-//      transpose of the slots into neuron-major lists ordered by token
-//      (sparse transpose)
+//   3. a CTA per (tile, chunk of 1024 tokens): deterministic transpose of
+//      the slots into neuron-major lists ordered by token (sparse
+//      transpose), from per-chunk column counts taken in step 2
 //   4. one CTA per neuron: dWg, dWu, dWd rows and dbg from gathered x / dy rows
 //      of its list, then the overflow rows' contributions (dense x hybrid)
 #include "common.cuh"
@@ -55,6 +55,22 @@ __device__ __forceinline__ bool gemm_row(const BParams &p, int ps) {
 }
 
 __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
+
+// Tokens per chunk of the sparse transpose (its per-(tile, chunk) column
+// counts are taken by the dh kernels, one per TwELL slot they finish).
+constexpr int TR_CHUNK = 1024;
+
+// The transpose's count of TwELL slot sl (a slot of token t, in the tile and
+// column it names): col_chunk[tile][t / TR_CHUNK][column] += 1 (zeroed by the
+// flags kernel at the start of the backward).  A malformed index is not
+// counted, as the transpose does not list it.
+__device__ __forceinline__ void count_slot(const BParams &p, int sl, int t) {
+  const int c = p.idx[sl];
+  if (c >= p.C) return;
+  const int j = sl / (p.Tn * p.K);
+  const int nch = (p.Tn + TR_CHUNK - 1) / TR_CHUNK;
+  atomicAdd(&p.col_chunk[((size_t)j * nch + t / TR_CHUNK) * p.C + c], 1);
+}
 
 // Four fp32 values (two pairs) as the bit pattern of one 16-byte store.
 __device__ __forceinline__ uint4 f4bits(const float2 &a, const float2 &b) {
@@ -116,6 +132,7 @@ __device__ __forceinline__ void dh_finish(const BParams &p, int ps, int sl, floa
     p.dz[sl] = dz;
     p.du[sl] = du;
     p.hs[sl] = h;
+    count_slot(p, sl, (sl / p.K) % p.Tn);
   } else {
     const size_t o = (size_t)ps * p.F + (-1 - sl);
     p.dzr[o] = dz;
@@ -297,6 +314,7 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
             p.dz[sl] = dz;
             p.du[sl] = du;
             p.hs[sl] = h;
+            count_slot(p, sl, t);
           } else {
             const size_t o = (size_t)ps * p.F + (-1 - sl);
             p.dzr[o] = dz;
@@ -397,36 +415,12 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
 // [j*T*K, (j+1)*T*K), ordered by token; each entry carries the token and the
 // pair's dz, du, h, so the weight-gradient pass reads one 16-byte record per
 // entry.  Overflow rows are not listed (their pairs live in the overflow-row
-// arrays).  Two passes over a (tile, chunk of 1024 tokens) grid:
-//   3a. count the entries of every column in the chunk;
-//   3b. the chunk's first entry per column = the column's start in the tile
-//       (prefix over columns of the totals) + the counts of earlier chunks;
-//       a token's rank among the chunk's tokens that use column c comes from
-//       per-warp lane masks (popc below the lane) plus per-warp offsets.
-constexpr int TR_CHUNK = 1024;
-
-template <int C>
-__global__ void __launch_bounds__(TR_CHUNK) twell_count_kernel(BParams p) {
-  pdl_begin();
-  __shared__ int cnt[C];
-  const int j = blockIdx.x, ch = blockIdx.y, tid = threadIdx.x;
-  const int K = p.K, Tn = p.Tn;
-  for (int c = tid; c < C; c += blockDim.x) cnt[c] = 0;
-  __syncthreads();
-  const int t = ch * TR_CHUNK + tid;
-  if (t < Tn && p.pos[t] < 0 && !(p.gemm_rows && p.ctl->dense)) {
-    const int n = p.nnz[(size_t)j * Tn + t];
-    const size_t s0 = ((size_t)j * Tn + t) * K;
-    for (int k = 0; k < n && k < K; ++k) {
-      const int c = p.idx[s0 + k];
-      if (c < C) atomicAdd(&cnt[c], 1);
-    }
-  }
-  __syncthreads();
-  for (int c = tid; c < C; c += blockDim.x)
-    p.col_chunk[((size_t)j * gridDim.y + ch) * C + c] = cnt[c];
-}
-
+// arrays).  The entries of every column in each chunk of 1024 tokens were
+// counted by the dh kernels (count_slot); one pass over a (tile, chunk) grid
+// then places them: the chunk's first entry per column = the column's start
+// in the tile (prefix over columns of the totals) + the counts of earlier
+// chunks; a token's rank among the chunk's tokens that use column c comes
+// from per-warp lane masks (popc below the lane) plus per-warp offsets.
 template <int C>
 __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
   pdl_begin();
@@ -619,7 +613,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // 1. hybrid split of the saved activations into this workspace, with the
   // forward's dispatcher rules when the dense-path rows have GEMMs
   prof_mark(KID_START, s);
-  cudaError_t e = launch_flags_from_nnz(a.tw, a.ws.ovf_bits, a.ws.slot_parts, s);
+  cudaError_t e = launch_flags_from_nnz(a.tw, a.ws.ovf_bits, a.ws.slot_parts, s, a.ws.col_chunk,
+                                        a.F * ((a.T + TR_CHUNK - 1) / TR_CHUNK));
   if (e != cudaSuccess) return e;
   e = launch_overflow_compact(a.tw, &a.ws, gemm ? a.dense_switch : 2.0f, s, /*write_user=*/false,
                               gemm ? a.dense_density : -1.f, a.ws.slot_parts, flags_blocks(a.T));
@@ -696,19 +691,13 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // 3. transpose
   const int nt = a.F / a.C;
   const dim3 tgrid(nt, (a.T + TR_CHUNK - 1) / TR_CHUNK);
-  if (a.C == 32) {
-    launch_k(twell_count_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
-    launch_k(twell_transpose_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
-  } else if (a.C == 64) {
-    launch_k(twell_count_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
-    launch_k(twell_transpose_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
-  } else {
-    launch_k(twell_count_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
-    launch_k(twell_transpose_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
-  }
+  // (the per-chunk column counts were taken by the dh kernels)
+  if (a.C == 32) launch_k(twell_transpose_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
+  else if (a.C == 64) launch_k(twell_transpose_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
+  else launch_k(twell_transpose_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prof_mark(KID_BWD_TRANSPOSE, s, 2);
+  prof_mark(KID_BWD_TRANSPOSE, s);
   // 4. weight gradients
   if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F);
   else TW_VPT(bwd_dw_kernel, float, a.F);

@@ -90,8 +90,10 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
 // SLOT_PARTS_MAX).
 constexpr int SLOT_PARTS_MAX = 1024;
 int flags_blocks(int T);
+// zero (zero_n int32, may be NULL) is cleared by the same launch.
 cudaError_t launch_flags_from_nnz(const twell_t &tw, uint32_t *bits,
-                                  unsigned long long *slot_parts, cudaStream_t s);
+                                  unsigned long long *slot_parts, cudaStream_t s,
+                                  int32_t *zero = nullptr, long zero_n = 0);
 // Dense backup rows of overflow rows that do not take the dense GEMM path.
 cudaError_t launch_assemble_fb_rows(const FwdArgs &a, cudaStream_t s);
 // All-dense training forward: u at the slots of the non-overflow rows.

@@ -239,8 +239,12 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
 __global__ void __launch_bounds__(256)
     flags_from_nnz_kernel(const uint8_t *__restrict__ nnz, int Tn, int nt, int K,
                           uint32_t *__restrict__ bits,
-                          unsigned long long *__restrict__ slot_parts) {
+                          unsigned long long *__restrict__ slot_parts,
+                          int32_t *__restrict__ zero, long zero_n) {
   pdl_begin();
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < zero_n;
+       i += (long)gridDim.x * blockDim.x)
+    zero[i] = 0;
   __shared__ uint32_t s_mask[8];
   __shared__ unsigned long long s_part[8];
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -286,9 +290,10 @@ int flags_blocks(int T) {
 }
 
 cudaError_t launch_flags_from_nnz(const twell_t &tw, uint32_t *bits,
-                                  unsigned long long *slot_parts, cudaStream_t s) {
+                                  unsigned long long *slot_parts, cudaStream_t s, int32_t *zero,
+                                  long zero_n) {
   launch_k(flags_from_nnz_kernel, flags_blocks(tw.T), 256, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K,
-           bits, slot_parts);
+           bits, slot_parts, zero, zero ? zero_n : 0L);
   return cudaGetLastError();
 }
 
