@@ -769,11 +769,21 @@ def cpu_baseline(a, w, train, seconds):
     t = oracle_sample(a, w, train, S, w.F)
     S = int(max(2, min(w.T, S * seconds / max(t, 1e-3))))
     t = oracle_sample(a, w, train, S, w.F)
-    return {"value": round(S / t, 3), "unit": "tokens/s", "cores": oracle.get_threads(),
+    cores = oracle.get_threads()
+    # the same oracle on one host core, on a smaller sample of the same rows
+    oracle.set_threads(1)
+    try:
+        S1 = max(1, S // max(cores, 1))
+        t1 = oracle_sample(a, w, train, S1, w.F)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(S / t, 3), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
             "sample": f"first {S} tokens of the workload, all {w.F} neurons, "
                       f"{'dense fwd+bwd' if train else 'dense fwd'} in fp64 C loops (OpenMP over "
-                      f"tokens/neurons), {t:.1f} s"}
+                      f"tokens/neurons), {t:.1f} s",
+            "single_thread": {"value": round(S1 / t1, 3), "unit": "tokens/s",
+                              "sample": f"first {S1} tokens, {t1:.1f} s on 1 core"}}
 
 
 def max_over_ranks(torch, value: float, world: int, device) -> float:
