@@ -21,7 +21,7 @@ struct Workspace {
   void *h;            // [Tp][F] dtype: h rows of the dense path
   void *xg;           // [Tp][D] dtype: gathered x rows of the dense path
   void *wide;         // [F/C][T][C] dtype: full ReLU(z) of overflowing (tile, row)s
-  void *urows;        // [Tp][F] dtype (training): u rows from the dense path
+  void *urows;        // [Tp][F] dtype (training, CUDA-core path): u rows of the dense path
   void *dyg;          // [Tp][D] dtype (training): gathered dy rows of the dense path
   float *dbg_r;       // [F] fp32 (training): dbg of the dense-path rows
   unsigned long long *slot_parts;  // [SLOT_PARTS_MAX] per-block slot counts (backward)

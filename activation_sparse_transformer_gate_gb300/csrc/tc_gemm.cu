@@ -274,7 +274,7 @@ struct TcParams {
   unsigned long long *slots;  // EPI_PACK: total slots written (the dispatcher's density)
   bf16 *val, *uval;         // uval: u at the slots (backward)
   bf16 *h, *g_fb, *u_fb, *y;
-  bf16 *wide, *urows;
+  bf16 *wide;
   float *out;              // EPI_F32, EPI_DW
   float lambda;            // EPI_DH: L1 coefficient
   bf16 *dz2, *du2, *h2;    // EPI_DH outputs, [2 Tp][F]: hi rows, then lo rows
@@ -688,12 +688,6 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
-          if (dense_all && p.train && p.gated) {  // u at the slots of non-overflow rows
-            uint4 *ur = (uint4 *)(p.urows + (size_t)m * p.F + n0 + c0);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              ur[v4] = make_uint4(uw[4 * v4], uw[4 * v4 + 1], uw[4 * v4 + 2], uw[4 * v4 + 3]);
-          }
           if (fb_ok) {
             uint4 *gd = (uint4 *)(p.g_fb + (size_t)ps * p.F + n0 + c0);
 #pragma unroll
@@ -1072,7 +1066,6 @@ TcParams base_params(const FwdArgs &a) {
   p.ovf_bits = a.ws.ovf_bits;
   p.slots = &a.ws.ctl->slots;
   p.wide = (bf16 *)a.ws.wide;
-  p.urows = (bf16 *)a.ws.urows;
   p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;
   p.status = a.tw.status;
   return p;

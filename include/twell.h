@@ -215,8 +215,8 @@ twell_status twell_rowell_forward(const void *x, const void *Wu, const void *Wd,
 /* Optional per-launch timing, for benchmarks.  Between twell_profile_begin
  * and twell_profile_end every entry point records a CUDA event on its stream
  * before its first kernel and after each step of its launch sequence (a step
- * is one kernel, or a few launches of one component: the two passes of the
- * sparse transpose, the three weight-gradient GEMMs).  twell_profile_end
+ * is one kernel, or a few launches of one component: the overflow-row flags
+ * and their scan, the backward's dense-path row gathers).  twell_profile_end
  * waits for those events and returns, in launch order, the step's identity
  * (see twell_kernel_name) and the milliseconds between the event before and
  * the event after it; *count receives the number of steps
