@@ -51,7 +51,7 @@ class twell_t(ctypes.Structure):
         ("ovf_rows", ctypes.c_void_p), ("n_ovf", ctypes.c_void_p), ("ovf_cap", ctypes.c_int32),
         ("g_fb", ctypes.c_void_p), ("u_val", ctypes.c_void_p), ("u_fb", ctypes.c_void_p),
         ("status", ctypes.c_void_p), ("dense_switch", ctypes.c_float),
-        ("dense_density", ctypes.c_float),
+        ("dense_density", ctypes.c_float), ("dh_density", ctypes.c_float),
     ]
 
 
@@ -176,7 +176,7 @@ class TwellBuffers:
 
     def __init__(self, T: int, F: int, C: int, K: int, dtype: int, ovf_cap: Optional[int] = None,
                  train: bool = False, device="cuda", dense_switch: float = 0.0,
-                 dense_density: float = 0.0):
+                 dense_density: float = 0.0, dh_density: float = 0.0):
         import torch
         tdt = torch.bfloat16 if dtype == TWELL_BF16 else torch.float32
         nt = F // C
@@ -195,7 +195,8 @@ class TwellBuffers:
                          nnz=_ptr(self.nnz), ovf_rows=_ptr(self.ovf_rows), n_ovf=_ptr(self.n_ovf),
                          ovf_cap=cap, g_fb=_ptr(self.g_fb), u_val=_ptr(self.u_val),
                          u_fb=_ptr(self.u_fb), status=_ptr(self.status),
-                         dense_switch=float(dense_switch), dense_density=float(dense_density))
+                         dense_switch=float(dense_switch), dense_density=float(dense_density),
+                         dh_density=float(dh_density))
 
 
 class RowEllBuffers:

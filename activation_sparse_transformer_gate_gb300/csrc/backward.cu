@@ -56,10 +56,6 @@ __device__ __forceinline__ bool gemm_row(const BParams &p, int ps) {
 
 __device__ __forceinline__ float sgnf(float v) { return v > 0.f ? 1.f : (v < 0.f ? -1.f : 0.f); }
 
-// Tokens per chunk of the sparse transpose (its per-(tile, chunk) column
-// counts are taken by the dh kernels, one per TwELL slot they finish).
-constexpr int TR_CHUNK = 1024;
-
 // The transpose's count of TwELL slot sl (a slot of token t, in the tile and
 // column it names): col_chunk[tile][t / TR_CHUNK][column] += 1 (zeroed by the
 // flags kernel at the start of the backward).  A malformed index is not
@@ -166,6 +162,7 @@ __global__ void __launch_bounds__(256, VL <= 8 ? 4 : 2) bwd_dh_kernel(BParams p)
   const int nw = blockDim.x >> 5;
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
+  if (p.ctl->dh_gemm) return;  // dh came from the tensor-core GEMM
   const int ps = p.pos[t];
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
   if (gemm_row(p, ps)) return;
@@ -240,6 +237,7 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
   const int nt = p.F / p.C;
   const int NV = p.D / 8;               // 16-byte vectors per row
   const int CPW = NV / (4 * DH_WARPS);  // 32-element chunks per warp (NV % 32 == 0)
+  if (p.ctl->dh_gemm) return;  // dh came from the tensor-core GEMM
   const int ps = p.pos[t];
   if (ps >= p.cap) return;  // overflow row without a dense backup row (capacity error)
   if (gemm_row(p, ps)) return;
@@ -617,7 +615,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
                                         a.F * ((a.T + TR_CHUNK - 1) / TR_CHUNK));
   if (e != cudaSuccess) return e;
   e = launch_overflow_compact(a.tw, &a.ws, gemm ? a.dense_switch : 2.0f, s, /*write_user=*/false,
-                              gemm ? a.dense_density : -1.f, a.ws.slot_parts, flags_blocks(a.T));
+                              gemm ? a.dense_density : -1.f, a.ws.slot_parts, flags_blocks(a.T),
+                              gemm ? a.dh_density : -1.f);
   if (e != cudaSuccess) return e;
   prof_mark(KID_OVERFLOW_COMPACT, s, 2);
   // 1'. dense-path rows on the tensor cores (idle when there are none):
@@ -633,7 +632,14 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     prof_mark(KID_BWD_DENSE_DX, s);
   }
-  // 2. per-token dh SDDMM (slots / overflow rows), then dx SpMM
+  // 2. dh of the rows the gathers own: one tensor-core GEMM read at the
+  // slots when the dispatcher chose it (its CTAs return at once otherwise),
+  // else the per-token SDDMM (whose CTAs then return at once); then dx SpMM
+  if (gemm) {
+    e = launch_tc_bwd_dh_sampled(a, s);
+    if (e != cudaSuccess) return e;
+    prof_mark(KID_BWD_DH_GEMM, s);
+  }
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
   // token / neuron CTAs: each thread owns two 16-byte vectors of a row (half

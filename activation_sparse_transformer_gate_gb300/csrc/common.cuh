@@ -141,7 +141,8 @@ struct Ctl {
   int32_t n_ovf;    // true number of overflow rows
   int32_t ovf_gemm; // 1: overflow rows run on the dense GEMM path
   unsigned long long slots;  // TwELL slots written by the gate epilogue (zeroed before it)
-  int32_t pad[10];
+  int32_t dh_gemm;  // backward: dh of the sparse rows from one dense GEMM read at the slots
+  int32_t pad[9];
 };
 
 }  // namespace twell

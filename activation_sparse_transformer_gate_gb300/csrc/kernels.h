@@ -63,7 +63,12 @@ struct BwdArgs {
   float *dWg, *dbg, *dWu, *dWd;
   Workspace ws;
   float dense_switch, dense_density;  // dispatcher of the dense-path rows (as the forward's)
+  float dh_density;  // dh from a dense GEMM above this slot density (<= 0: never)
 };
+
+// Tokens per chunk of the sparse transpose (its per-(tile, chunk) column
+// counts are taken where dh is finished, one per TwELL slot).
+constexpr int TR_CHUNK = 1024;
 
 // pack.cu
 // Streaming multiprocessors and L2 bytes of the current device (queried once).
@@ -79,12 +84,13 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // dense_density > 0: all-dense also when ctl->slots (zeroed before the gate,
 // summed by its epilogue) exceeds dense_density * T * F; <= 0 ignores slots.
 // slot_parts (n_parts entries, from launch_flags_from_nnz) replaces the gate
-// epilogue's count in ctl->slots.
+// epilogue's count in ctl->slots.  dh_density > 0 (backward): ctl->dh_gemm
+// when not all-dense and the slots exceed dh_density * T * F.
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user = true,
                                     float dense_density = -1.f,
                                     const unsigned long long *slot_parts = nullptr,
-                                    int n_parts = 0);
+                                    int n_parts = 0, float dh_density = -1.f);
 // Overflow-row bitmap from the nnz counts (every word written); with
 // slot_parts, per-block slot counts (flags_blocks(T) entries, at most
 // SLOT_PARTS_MAX).
@@ -119,6 +125,9 @@ cudaError_t launch_tc_gate_pack(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s);
+// dh of the rows that are not on the dense path, from dy W_down^T over all
+// rows, read at the TwELL slots (every CTA returns unless ctl->dh_gemm).
+cudaError_t launch_tc_bwd_dh_sampled(const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s);
 
@@ -145,7 +154,8 @@ enum KernelId {
   KID_BWD_PREP = 17,
   KID_ROWELL_PACK = 18,
   KID_ROWELL_UPDOWN = 19,
-  KID_COUNT = 20
+  KID_BWD_DH_GEMM = 20,
+  KID_COUNT = 21
 };
 // Record a timing event after `launches` kernel launches of component `id`
 // (no-op unless enabled).

@@ -79,16 +79,21 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s) 
 // All-dense when too many rows overflow, or when the slots the gate epilogue
 // wrote (active entries, at most K per row and tile, so overflow rows count
 // little) exceed dense_density * T * F: gathers then cost more than GEMMs.
+// Backward (dh_density > 0): dh of the rows left to the gathers comes from
+// one dense GEMM read at the slots when the slots exceed dh_density * T * F
+// (each active entry costs the SDDMM a d_model row; the GEMM costs the same
+// per entry of the whole T x F product).
 __device__ __forceinline__ void write_ctl(Ctl *ctl, int n_ovf, int Tn, int F, float dense_switch,
-                                          float dense_density) {
-  const bool too_dense =
-      dense_density > 0.f && (double)ctl->slots > (double)dense_density * (double)Tn * (double)F;
+                                          float dense_density, float dh_density) {
+  const double TF = (double)Tn * (double)F;
+  const bool too_dense = dense_density > 0.f && (double)ctl->slots > (double)dense_density * TF;
   const int dense = ((float)n_ovf > dense_switch * (float)Tn || too_dense) ? 1 : 0;
   const int og = (!dense && n_ovf >= OVF_GEMM_MIN) ? 1 : 0;
   ctl->n_ovf = n_ovf;
   ctl->dense = dense;
   ctl->ovf_gemm = og;
   ctl->n_rows = dense ? Tn : (og ? n_ovf : 0);
+  ctl->dh_gemm = (!dense && dh_density > 0.f && (double)ctl->slots > (double)dh_density * TF) ? 1 : 0;
 }
 
 // Hybrid split from nnz (one CTA of 1024 threads, no workspace): a row
@@ -149,7 +154,8 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
                      int32_t *__restrict__ ovf_rows, int32_t *__restrict__ n_ovf, int32_t *status,
                      Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
                      int F, float dense_switch, float dense_density,
-                     const unsigned long long *__restrict__ slot_parts, int n_parts) {
+                     const unsigned long long *__restrict__ slot_parts, int n_parts,
+                     float dh_density) {
   pdl_begin();
   __shared__ int warp_off[32];
   __shared__ int word_off[1024];
@@ -213,17 +219,19 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
     }
     if (n_ovf) *n_ovf = running;
     if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
-    write_ctl(ctl, running, Tn, F, dense_switch, dense_density);
+    write_ctl(ctl, running, Tn, F, dense_switch, dense_density, dh_density);
   }
 }
 
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user, float dense_density,
-                                    const unsigned long long *slot_parts, int n_parts) {
+                                    const unsigned long long *slot_parts, int n_parts,
+                                    float dh_density) {
   if (ws) {
     launch_k(overflow_scan_kernel, 1, 1024, 0, s, ws->ovf_bits, tw.T, tw.ovf_cap,
              write_user ? tw.ovf_rows : nullptr, write_user ? tw.n_ovf : nullptr, tw.status,
-             ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density, slot_parts, n_parts);
+             ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density, slot_parts, n_parts,
+             dh_density);
     return cudaGetLastError();
   }
   launch_k(overflow_compact_kernel, 1, 1024, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,

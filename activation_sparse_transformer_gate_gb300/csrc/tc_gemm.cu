@@ -9,6 +9,9 @@
 //              TwELL slots / wide tiles, h = g*u (+ u at the slots)   (dense rows)
 //   EPI_DH   : dh = dy Wd^T + lambda sign(h) -> dz, du, h rows (bf16 hi +
 //              lo parts) and column sums of dz                    (bwd rows)
+//   EPI_DHS  : the same dh for the rows left to the gathers, read only at the
+//              TwELL slots (and the overflow rows' backup-row columns) ->
+//              fp32 dz, du, h where the gather SDDMM puts them   (bwd, sparse)
 //   EPI_DX   : dx[tok] = dz Wg + du Wu (K ranges over the hi and lo parts,
 //              B MN-major)                                        (bwd rows)
 //   EPI_DW   : dW = A^T B with A, B both MN-major (token axis = K, hi and lo
@@ -53,7 +56,11 @@ constexpr int GZ_STRIDE = 40;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4, EPI_DH = 5, EPI_DX = 6,
-           EPI_DW = 7 };
+           EPI_DW = 7, EPI_DHS = 8 };
+// fp32 elements per row of the EPI_DHS accumulator staging (32 columns; the
+// 144-byte stride keeps the 16-byte stores of 8 consecutive rows on
+// distinct banks)
+constexpr int DHS_STRIDE = 36;
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -282,6 +289,9 @@ struct TcParams {
   float *dbg_out;          // EPI_DW: dbg (added from dbg_r with the W_gate problem)
   float *outq[3];          // EPI_DW: the fp32 output of each problem (dWg, [dWu,] dWd)
   int nq;                  // EPI_DW: problems in the launch
+  float *sdz, *sdu, *shs;  // EPI_DHS: dz, du, h at the slots, [F/C][T][K]
+  float *rdz, *rdu, *rhs;  // EPI_DHS: the same for overflow rows, [cap][F]
+  int32_t *col_chunk;      // EPI_DHS: the sparse transpose's column counts
   int32_t *status;
 };
 
@@ -322,6 +332,7 @@ struct Cfg {
   static constexpr int SLOT_BYTES = EPI == EPI_PACK ? 128 * 32 * 3 + 128 * 64
                                     : EPI == EPI_U  ? 128 * GZ_STRIDE * 2 + 128 * 64  // g and u rows
                                     : EPI == EPI_DH ? 128 * GZ_STRIDE * 4  // g and u rows
+                                    : EPI == EPI_DHS ? 128 * DHS_STRIDE * 4  // accumulator rows
                                                     : 0;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256 + BN * 4 + SLOT_BYTES;
   static_assert(STAGES >= 2, "too few stages");
@@ -380,6 +391,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
                      ? max(1, min(m_blocks, (32 << 20) / (BM * 2 * BK * max(KT, 1))))
                      : 1;
   if ((int)blockIdx.x >= num_tiles || KT == 0) return;  // uniform for the CTA
+  // EPI_DHS runs only when the dispatcher chose it (else the gather SDDMM)
+  if (EPI == EPI_DHS && (dense_all || !p.ctl->dh_gemm)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -552,14 +565,14 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       // while the accumulator is still being computed (they do not depend on
       // it); EPI_DH also fetches u at the slots, and rows with a dense backup
       // row (ps >= 0) read that instead
-      constexpr bool SLOTS = EPI == EPI_U || EPI == EPI_DH;
-      const int tok_u = (SLOTS && row_ok) ? (dense_all ? m : p.rows[m]) : 0;
-      const int ps_u = (EPI == EPI_DH && row_ok) ? p.pos[tok_u] : -1;
+      constexpr bool SLOTS = EPI == EPI_U || EPI == EPI_DH || EPI == EPI_DHS;
+      const int tok_u = (SLOTS && row_ok) ? ((dense_all || EPI == EPI_DHS) ? m : p.rows[m]) : 0;
+      const int ps_u = ((EPI == EPI_DH || EPI == EPI_DHS) && row_ok) ? p.pos[tok_u] : -1;
       int pf_nz = 0;
       uint32_t pf_iw[8], pf_vw[16], pf_qw[16] = {};  // (pf_qw: plain FFN leaves it zero)
       if (SLOTS && row_ok && ps_u < 0) {
         fetch_slots(p, n0, tok_u, pf_nz, pf_iw, pf_vw);
-        if (EPI == EPI_DH && p.gated)
+        if ((EPI == EPI_DH || EPI == EPI_DHS) && p.gated)
           load_vals(p.uval + ((size_t)(n0 / p.C) * p.Tn + tok_u) * p.Kslots, p.Kslots, pf_qw);
       }
       const bool ok = mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status);
@@ -893,6 +906,120 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           }
           atomicAdd(p.dbg_r + n0 + c0 + lane, dz[0]);
         }
+      } else if (EPI == EPI_DHS) {
+        // dh of the rows the gathers own (not the dense-path rows), from the
+        // full product dy W_down^T but read only where the forward kept an
+        // active entry: at the row's TwELL slots, or at every column of an
+        // overflow row with a dense backup row.  Per entry, as the gather
+        // SDDMM: dh = acc + lambda sign(h), h = g u, dz = [g > 0] dh u,
+        // du = [g > 0] dh g (plain FFN: u = 1), in fp32, stored at the slot
+        // (with the sparse transpose's count of its column) or in the
+        // overflow-row arrays.  A thread picks its slots' columns out of the
+        // accumulator through its own shared-memory row, 32 columns at a time.
+        const int tok = m;
+        const int ps = ps_u;
+        const bool skip = !row_ok || ps >= p.cap || (ps >= 0 && p.ctl->ovf_gemm);
+        const int K = p.Kslots;
+        float *st = (float *)s_slots + row * DHS_STRIDE;
+        const int nch = (p.Tn + TR_CHUNK - 1) / TR_CHUNK;
+        for (int jt = 0; jt < BN / p.C; ++jt) {
+          const int n1 = n0 + jt * p.C;
+          if (n1 >= p.N) break;  // uniform
+          if (jt > 0 && !skip && ps < 0) {  // the first tile's slots were prefetched
+            fetch_slots(p, n1, tok, pf_nz, pf_iw, pf_vw);
+            if (p.gated) load_vals(p.uval + ((size_t)(n1 / p.C) * p.Tn + tok) * K, K, pf_qw);
+          }
+          const int nz = min(pf_nz, K);
+          float dhv[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) dhv[k] = 0.f;
+          for (int cb = 0; cb < p.C; cb += 32) {
+            float v[32];
+            tmem_ld32(tacc + jt * p.C + cb, v);  // (warp-collective)
+            if (skip) continue;
+            if (ps >= 0) {  // overflow row: every column of the block
+              const size_t o = (size_t)ps * p.F + n1 + cb;
+              const uint4 *gr = (const uint4 *)(p.g_fb + o);
+              const uint4 *ur = (const uint4 *)(p.u_fb + o);
+              float4 *dz4 = (float4 *)(p.rdz + o), *du4 = (float4 *)(p.rdu + o);
+              float4 *h4 = (float4 *)(p.rhs + o);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const uint4 gv = gr[v4];
+                const uint4 uv = p.gated ? ur[v4] : make_uint4(0x3F803F80u, 0x3F803F80u,
+                                                               0x3F803F80u, 0x3F803F80u);
+                const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w}, ua[4] = {uv.x, uv.y, uv.z, uv.w};
+                float dz[8], du[8], hv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float g = (e & 1) ? bf_hi(ga[e / 2]) : bf_lo(ga[e / 2]);
+                  const float u = (e & 1) ? bf_hi(ua[e / 2]) : bf_lo(ua[e / 2]);
+                  const float h = p.gated ? g * u : g;
+                  const float dh = v[8 * v4 + e] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
+                  const bool act = g > 0.f;
+                  dz[e] = act ? (p.gated ? dh * u : dh) : 0.f;
+                  du[e] = act ? dh * g : 0.f;
+                  hv[e] = h;
+                }
+                dz4[2 * v4] = make_float4(dz[0], dz[1], dz[2], dz[3]);
+                dz4[2 * v4 + 1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
+                du4[2 * v4] = make_float4(du[0], du[1], du[2], du[3]);
+                du4[2 * v4 + 1] = make_float4(du[4], du[5], du[6], du[7]);
+                h4[2 * v4] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                h4[2 * v4 + 1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+              }
+            } else {  // slots: stage the block, pick the slots' columns
+              float4 *s4 = (float4 *)st;
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                s4[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                if (k >= K) break;  // uniform
+                const int c = slot_col(pf_iw, k) - cb;
+                if (k < nz && (unsigned)c < 32u) dhv[k] = st[c];
+              }
+            }
+          }
+          if (skip || ps >= 0) continue;
+          const int j = n1 / p.C;
+          const size_t s0 = ((size_t)j * p.Tn + tok) * K;
+#pragma unroll
+          for (int k0 = 0; k0 < 32; k0 += 4) {
+            if (k0 >= K) break;  // uniform
+            float dz[4], du[4], hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int k = k0 + i;
+              const bool live = k < nz;  // (pad slots store zeros)
+              const float g = live ? __uint_as_float((uint32_t)slot_val(pf_vw, k) << 16) : 0.f;
+              const float u = !p.gated ? 1.f
+                              : (live ? __uint_as_float((uint32_t)slot_val(pf_qw, k) << 16) : 0.f);
+              const float h = p.gated ? g * u : g;
+              const float dh = dhv[k] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
+              const bool act = g > 0.f;
+              dz[i] = act ? (p.gated ? dh * u : dh) : 0.f;
+              du[i] = act ? dh * g : 0.f;
+              hv[i] = h;
+              const int c = slot_col(pf_iw, k);
+              if (live && c < p.C)  // the transpose's count (a malformed index is not listed)
+                atomicAdd(&p.col_chunk[((size_t)j * nch + tok / TR_CHUNK) * p.C + c], 1);
+            }
+            if (K % 4 == 0) {
+              *(float4 *)(p.sdz + s0 + k0) = make_float4(dz[0], dz[1], dz[2], dz[3]);
+              *(float4 *)(p.sdu + s0 + k0) = make_float4(du[0], du[1], du[2], du[3]);
+              *(float4 *)(p.shs + s0 + k0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (k0 + i >= K) break;
+                p.sdz[s0 + k0 + i] = dz[i];
+                p.sdu[s0 + k0 + i] = du[i];
+                p.shs[s0 + k0 + i] = hv[i];
+              }
+            }
+          }
+        }
       } else if (EPI == EPI_DW) {
         // Weight-gradient rows (row m = neuron, fp32) of problem q: stored
         // in all-dense mode, added to the gather kernel's rows otherwise.
@@ -1175,6 +1302,25 @@ cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s) {
   p.Kdim = a.D;
   return launch_tc<256, 1, false, EPI_DH>(mdyg, mdy, mwd, mwd, p, (Tp / BM) * ((a.F + 255) / 256),
                                           s);
+}
+
+// dh of the rows the gathers own as one GEMM over every row, dy W_down^T
+// (both K-major, 128 x 256 tiles as the gate GEMM), read at the TwELL slots
+// by the epilogue: at ~1% active entries the tensor cores compute the whole
+// product sooner than the SDDMM gathers a d_model row of W_down per entry.
+cudaError_t launch_tc_bwd_dh_sampled(const BwdArgs &a, cudaStream_t s) {
+  CUtensorMap mdy, mwd;
+  if (!make_map(&mdy, a.dy, a.D, a.T, 64, BM) || !make_map(&mwd, a.Wd, a.D, a.F, 64, 256))
+    return cudaErrorInvalidValue;
+  TcParams p = bwd_params(a);
+  p.M_host = a.T;
+  p.N = a.F;
+  p.Kdim = a.D;
+  p.sdz = a.ws.dz; p.sdu = a.ws.du; p.shs = a.ws.hs;
+  p.rdz = a.ws.dzr; p.rdu = a.ws.dur; p.rhs = a.ws.hr;
+  p.col_chunk = a.ws.col_chunk;
+  const int tiles = ((a.T + BM - 1) / BM) * ((a.F + 255) / 256);
+  return launch_tc<256, 1, false, EPI_DHS>(mdy, mdy, mwd, mwd, p, tiles, s);
 }
 
 // dx[tok] = dz W_gate + du W_up over the dense-path rows (one accumulator,

@@ -62,7 +62,8 @@ static const char *kKernelNames[KID_COUNT] = {
     "dense_rows_gate_up",   "dense_rows_down",  "pack_dense",         "copy_fb_rows",
     "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
     "bwd_dense_dh_gemm",    "fill_u_slots",     "assemble_fb_rows",   "bwd_dense_dx_gemm",
-    "bwd_dense_dw_gemm",    "bwd_prep_rows",    "rowell_pack_dense",  "rowell_updown"};
+    "bwd_dense_dw_gemm",    "bwd_prep_rows",    "rowell_pack_dense",  "rowell_updown",
+    "bwd_dh_gemm_sampled"};
 
 Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
   Workspace w;
@@ -179,6 +180,23 @@ float density_of(const twell_t *tw, int D, int gated, bool backward) {
   double d = 0.013;
   if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
   if (backward) d *= 1.47;
+  return (float)d;
+}
+
+// Slot density above which the backward takes dh from one tensor-core GEMM
+// read at the slots.  Per active entry the SDDMM gathers a d_model row of
+// W_down (2 d_model bytes at ~9.6 TB/s from L2); the GEMM spends 2 d_model
+// flops per entry of the whole T x F product (~1.3 PFLOP/s with the
+// epilogue): crossover ~0.65% (measured 0.70% at d_model 2048 / d_ff 8192,
+// 0.61% at 4096 / 14336), lower when W_down does not fit in L2 and the
+// gathers slow down.
+float dh_density_of(const twell_t *tw, int D) {
+  if (tw->dh_density > 0.f) return tw->dh_density;
+  if (tw->dh_density < 0.f) return -1.f;
+  const double wbytes = (double)tw->F * (double)D * (tw->dtype == TWELL_BF16 ? 2.0 : 4.0);
+  const double l2 = (double)l2_size();
+  double d = 0.0065;
+  if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
   return (float)d;
 }
 
@@ -344,6 +362,7 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   a.lambda = lambda; a.dx = dx; a.dWg = dWg; a.dbg = dbg; a.dWu = dWu; a.dWd = dWd;
   a.dense_switch = switch_of(tw);
   a.dense_density = density_of(tw, D, gated, true);
+  a.dh_density = dh_density_of(tw, D);
   a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
   return cuda_status(launch_backward(a, (cudaStream_t)stream));
 }

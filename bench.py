@@ -63,6 +63,10 @@ def parse_args():
     ap.add_argument("--dense-density", type=float, default=0.0,
                     help="the dispatcher's density threshold (0: the library default; "
                          "< 0: off; a tiny value forces the all-dense path)")
+    ap.add_argument("--dh-density", type=float, default=0.0,
+                    help="backward: slot density above which dh comes from the tensor-core "
+                         "GEMM read at the slots (0: the library default; < 0: always the "
+                         "gather SDDMM; a tiny value: always the GEMM)")
     return ap.parse_args()
 
 
@@ -162,7 +166,7 @@ def run_ours(args, rank, world, local_rank):
     d = {k: upload(torch, dev, a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
     T, D, F = w.T, w.D, w.F
     bufs = tw.TwellBuffers(T, F, w.C, w.K, dtype, train=train, device=dev,
-                           dense_density=args.dense_density)
+                           dense_density=args.dense_density, dh_density=args.dh_density)
     ws, nws = tw.workspace(T, D, F, w.C, w.K, dtype, train, device=dev)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
     dx = dWg = dWu = dWd = dbg = None
@@ -263,12 +267,14 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     rows_f = int(ws[:4].view(torch.int32).item())
     rows_b = 0
+    dh_gemm = False
     if train:
         tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], w.lam, D, dx,
                               dWg, dbg, dWu, dWd, ws, nws, sh)
         torch.cuda.synchronize(dev)
         rows_b = int(ws[:4].view(torch.int32).item())
-    rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b)
+        dh_gemm = bool(ws[24:28].view(torch.int32).item())  # control block: dh_gemm
+    rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b, dh_gemm)
     dominant = max((k for k in kern if k in rl), key=lambda k: kern[k]["ms_per_step"], default=None)
     roof = None
     if dominant:
@@ -371,7 +377,7 @@ def gather_ceiling(torch, lib, dev, W, w, pairs, timed, sh):
     return pairs * row_bytes / (ms / 1e3) / 1e9
 
 
-def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0):
+def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
     """Achieved rate of each kernel from its algorithmic work per launch:
     bytes for the gather kernels (rows gathered + rows streamed + TwELL),
     flops for the gate GEMM and for the dense-path GEMMs (rows_f / rows_b
@@ -409,6 +415,9 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0):
         "bwd_dw_gather": ("hbm", pb * (2 * D * 2 + 16) + (3 * F * D * 4 + F * 4 if tb else 0)),
         "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
     }
+    if dh_gemm:  # dh from the full product dy W_down^T, read at the slots
+        del wrk["bwd_slots_sddmm"]
+        wrk["bwd_dh_gemm_sampled"] = ("tensor", 2.0 * T * D * F)
     wrk = {k: v for k, v in wrk.items() if v[1] > 0}
     ng = 3 if w.gated else 2  # dW problems (dWg, [dWu,] dWd)
     for k, rows, mult in (("dense_rows_gate_up", rows_f, 1), ("dense_rows_down", rows_f, 1),

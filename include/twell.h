@@ -112,6 +112,15 @@ typedef struct {
                              that in the backward; < 0 disables this test.
                              The backward applies the same rules to the
                              saved TwELL.                                    */
+  float dh_density;       /* backward, bf16 on the tensor-core path: when the
+                             rows are not all dense and the slots exceed
+                             dh_density * T * F, dh of the rows the gathers
+                             own comes from one dense GEMM dy W_down^T read
+                             at the slots instead of the per-entry SDDMM
+                             (same values up to fp32 summation order).  0
+                             selects the measured crossover: 0.0065, scaled
+                             by L2 / bytes of W_down when W_down does not fit
+                             in L2; < 0 always gathers.                      */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward

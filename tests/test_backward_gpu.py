@@ -30,10 +30,12 @@ def shifted(t, elems):
     return v
 
 
-def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0):
+def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0, dh_density=-1.0):
     """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
     the density test of the dispatcher off, so that moderately dense test
-    workloads still run the gather kernels; out (dict) receives the
+    workloads still run the gather kernels; dh_density < 0 keeps dh on the
+    gather SDDMM (> 0: on the tensor-core GEMM read at the slots above that
+    density; 0: the dispatcher's default); out (dict) receives the
     workspace's control block after the forward ("ctl") and after the
     backward ("ctl_bwd")."""
     T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
@@ -42,12 +44,13 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0)
     d = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
     if wd_shift:
         d["Wd"] = shifted(d["Wd"], wd_shift)
-    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density)
+    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density,
+                           dh_density=dh_density)
     ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
     y = torch.empty((T, D), dtype=tdt, device="cuda")
     tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 1, bufs.t, y, ws, nws)
     if out is not None:
-        out["ctl"] = ws[:24].cpu().numpy().copy()
+        out["ctl"] = ws[:32].cpu().numpy().copy()
     dx = torch.full((T, D), float("nan"), dtype=tdt, device="cuda")
     dWg = torch.full((F, D), float("nan"), dtype=torch.float32, device="cuda")
     dWu = torch.full_like(dWg, float("nan")) if d["Wu"] is not None else None
@@ -56,7 +59,7 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0)
     tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], lam, D, dx, dWg, dbg,
                           dWu, dWd, ws, nws)
     if out is not None:
-        out["ctl_bwd"] = ws[:24].cpu().numpy().copy()
+        out["ctl_bwd"] = ws[:32].cpu().numpy().copy()
     code, n_ovf = tw.twell_get_status(bufs.t)
     return dict(code=code, n_ovf=n_ovf, y=to_np64(y), dx=to_np64(dx), dWg=to_np64(dWg),
                 dbg=to_np64(dbg), dWu=None if dWu is None else to_np64(dWu), dWd=to_np64(dWd))
@@ -65,6 +68,11 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0)
 def ctl_fields(c):
     """(n_rows, dense, n_ovf, ovf_gemm) of a saved control block."""
     return tuple(int(v) for v in c[:16].view(np.int32))
+
+
+def dh_gemm_of(c):
+    """The backward's choice of the tensor-core dh GEMM in a saved control block."""
+    return int(c[24:28].view(np.int32)[0])
 
 
 def check_backward(a, w, g, lam, tok_sel=None, neu_sel=None):
@@ -299,6 +307,99 @@ def test_config5_full_size_sampled():
     g = run_train(a, w, w.lam)
     assert g["code"] == 0
     rng = np.random.default_rng(5)
+    ts = np.unique(np.concatenate([np.arange(8), rng.choice(w.T, 24, replace=False)]))
+    ns = np.unique(np.concatenate([np.arange(8), rng.choice(w.F, 24, replace=False)]))
+    check_backward(a, w, g, w.lam, tok_sel=ts, neu_sel=ns)
+    assert np.isfinite(g["dWg"]).all() and np.isfinite(g["dx"]).all()
+
+
+# ---- dh from the tensor-core GEMM read at the slots ------------------------
+# The same workloads as above with dh taken from dy W_down^T over every row
+# (dh_density tiny): the slots of ordinary rows, every column of overflow
+# rows with a backup row, overflow rows on the dense-row GEMMs skipped, the
+# sparse transpose's column counts, pad slots, ragged T and d_ff.
+DH_GEMM_CASES = {
+    "overflow_rows": (dict(T=300, D=256, F=1024, C=128, K=8, gated=True, bg=-2.33, seed=21,
+                           hot_tokens=3, seq_len=100, hot_bias=1.49), 1e-4),
+    "nongated_c64_k4": (dict(T=200, D=256, F=512, C=64, K=4, gated=False, bg=-2.2, seed=62,
+                             hot_tokens=2, seq_len=50, hot_bias=1.5), 0.05),
+    "many_overflow_rows": (dict(T=600, D=256, F=1024, C=128, K=8, gated=True, bg=-2.33, seed=63,
+                                hot_tokens=2, seq_len=7, hot_bias=1.6), 1e-3),
+    "c32_k2": (dict(T=192, D=128, F=512, C=32, K=2, gated=True, bg=-2.6, seed=64), 1e-2),
+    "c128_k32": (dict(T=96, D=128, F=512, C=128, K=32, gated=True, bg=-1.9, seed=65), 1e-2),
+    "dff_384_ragged": (dict(T=333, D=192, F=384, C=128, K=8, gated=True, bg=-1.8, seed=66,
+                            hot_tokens=2, seq_len=111, hot_bias=1.5), 1e-3),
+    "l1_dominant": (dict(T=160, D=256, F=512, C=64, K=8, gated=True, bg=-1.8, seed=67), 0.5),
+    "token_chunks": (dict(T=2500, D=256, F=512, C=128, K=8, gated=True, bg=-2.0, seed=68,
+                          hot_tokens=2, seq_len=500, hot_bias=1.5), 1e-3),
+}
+
+
+@pytest.mark.parametrize("case", sorted(DH_GEMM_CASES))
+def test_dh_gemm_read_at_slots(case):
+    kw, lam = DH_GEMM_CASES[case]
+    extra = {k: kw[k] for k in ("hot_tokens", "seq_len", "hot_bias") if k in kw}
+    w = synth.Workload(f"dhg_{case}", kw["T"], kw["D"], kw["F"], kw["C"], kw["K"], "bf16",
+                       kw["gated"], kw["bg"], kw["seed"], train=True, **extra)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, lam, out=out, dh_density=1e-9)
+    assert g["code"] == 0
+    n_rows, dense, n_ovf, ovf_gemm = ctl_fields(out["ctl_bwd"])
+    assert dense == 0 and dh_gemm_of(out["ctl_bwd"]) == 1
+    if case == "many_overflow_rows":
+        assert ovf_gemm == 1 and n_rows == n_ovf >= 128
+    elif "hot_tokens" in kw:
+        assert ovf_gemm == 0 and n_ovf >= 1
+    check_backward(a, w, g, lam)
+
+
+def test_dh_gemm_equals_gathers_on_the_same_inputs():
+    """The two dh paths give the same gradients up to fp32 summation order."""
+    kw, lam = DH_GEMM_CASES["overflow_rows"]
+    w = synth.Workload("dhg_eq", kw["T"], kw["D"], kw["F"], kw["C"], kw["K"], "bf16", True,
+                       kw["bg"], kw["seed"], hot_tokens=3, seq_len=100, hot_bias=1.49, train=True)
+    a = synth.generate(w)
+    o1, o2 = {}, {}
+    g1 = run_train(a, w, lam, out=o1, dh_density=-1.0)
+    g2 = run_train(a, w, lam, out=o2, dh_density=1e-9)
+    assert dh_gemm_of(o1["ctl_bwd"]) == 0 and dh_gemm_of(o2["ctl_bwd"]) == 1
+    for k in ("dx", "dWg", "dWu", "dWd", "dbg"):
+        ref = g1[k]
+        scale = max(float(np.sqrt(np.mean(ref ** 2))), 1e-30)
+        assert np.max(np.abs(g2[k] - ref)) <= 2e-2 * scale, k
+
+
+def test_dh_gemm_not_taken_when_all_dense():
+    """An all-dense backward keeps dh on the dense-row GEMM (hi + lo rows)."""
+    w = synth.Workload("dhg_dense", 160, 256, 1024, 128, 16, "bf16", True, -1.64, 69, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, dense_density=1e-6, out=out, dh_density=1e-9)
+    assert g["code"] == 0 and ctl_fields(out["ctl_bwd"])[:2] == (160, 1)
+    assert dh_gemm_of(out["ctl_bwd"]) == 0
+    check_backward(a, w, g, 1e-3)
+
+
+def test_dh_gemm_below_threshold_gathers():
+    """A dh_density above the slot density leaves dh on the gather SDDMM."""
+    w = synth.Workload("dhg_thr", 160, 256, 512, 128, 8, "bf16", True, -2.33, 70, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, out=out, dh_density=0.5)
+    assert g["code"] == 0 and dh_gemm_of(out["ctl_bwd"]) == 0
+    check_backward(a, w, g, 1e-3)
+
+
+def test_config5_full_size_default_dispatcher():
+    """The training-step workload at full size with the dispatcher's default
+    choice for dh (about 1% active: the tensor-core GEMM read at the slots)."""
+    w = synth.config5()
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, w.lam, out=out, dh_density=0.0)
+    assert g["code"] == 0 and dh_gemm_of(out["ctl_bwd"]) == 1
+    rng = np.random.default_rng(55)
     ts = np.unique(np.concatenate([np.arange(8), rng.choice(w.T, 24, replace=False)]))
     ns = np.unique(np.concatenate([np.arange(8), rng.choice(w.F, 24, replace=False)]))
     check_backward(a, w, g, w.lam, tok_sel=ts, neu_sel=ns)
