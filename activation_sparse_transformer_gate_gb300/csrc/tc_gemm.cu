@@ -317,6 +317,127 @@ __device__ __forceinline__ void fetch_slots(const TcParams &p, int col, int tok,
   load_slots(p.idx + jt * p.Kslots, p.val + jt * p.Kslots, p.Kslots, iw, vw);
 }
 
+// EPI_DHS: the gradients of one TwELL tile's slots (tile j, row tok) from dh
+// at the slots, as the gather SDDMM finishes an entry: h = g u, dh += lambda
+// sign(h), dz = [g > 0] dh u, du = [g > 0] dh g (plain FFN: u = 1), stored
+// at the live slots (groups of four from the first; pad slots past the last
+// group are not written, as no reader goes past nnz) with the sparse
+// transpose's count of each live slot's column.  iw / vw / qw: the slot
+// words of load_slots and of u at the slots; NK slots at most (K <= NK).
+template <int NK>
+__device__ __forceinline__ void dhs_store_slots(const TcParams &p, int j, int tok, int K, int nz,
+                                                const uint32_t (&iw)[NK / 4 > 0 ? NK / 4 : 1],
+                                                const uint32_t (&vw)[NK / 2],
+                                                const uint32_t (&qw)[NK / 2],
+                                                const float (&dh)[NK], int nch) {
+  const size_t s0 = ((size_t)j * p.Tn + tok) * K;
+#pragma unroll
+  for (int k0 = 0; k0 < NK; k0 += 4) {
+    if (k0 >= K) break;   // uniform
+    if (k0 >= nz) break;  // no live slot left
+    float dz[4], du[4], hv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = k0 + i;
+      const bool live = k < nz;  // (pad slots store zeros)
+      const uint32_t gb = (vw[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+      const uint32_t ub = (qw[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+      const float g = live ? __uint_as_float(gb << 16) : 0.f;
+      const float u = !p.gated ? 1.f : (live ? __uint_as_float(ub << 16) : 0.f);
+      const float h = p.gated ? g * u : g;
+      const float d = dh[k] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
+      const bool act = g > 0.f;
+      dz[i] = act ? (p.gated ? d * u : d) : 0.f;
+      du[i] = act ? d * g : 0.f;
+      hv[i] = h;
+      const int c = (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+      if (live && c < p.C)  // the transpose's count (a malformed index is not listed)
+        atomicAdd(&p.col_chunk[((size_t)j * nch + tok / TR_CHUNK) * p.C + c], 1);
+    }
+    if (K % 4 == 0) {
+      *(float4 *)(p.sdz + s0 + k0) = make_float4(dz[0], dz[1], dz[2], dz[3]);
+      *(float4 *)(p.sdu + s0 + k0) = make_float4(du[0], du[1], du[2], du[3]);
+      *(float4 *)(p.shs + s0 + k0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (k0 + i >= K) break;
+        p.sdz[s0 + k0 + i] = dz[i];
+        p.sdu[s0 + k0 + i] = du[i];
+        p.shs[s0 + k0 + i] = hv[i];
+      }
+    }
+  }
+}
+
+// EPI_DHS, an overflow row with a dense backup row (position ps): dz, du, h
+// of the 32 columns from column col on, written in full to the overflow-row
+// arrays (zeros where g = 0).
+__device__ __forceinline__ void dhs_store_row_block(const TcParams &p, int ps, int col,
+                                                    const float (&v)[32]) {
+  const size_t o = (size_t)ps * p.F + col;
+  const uint4 *gr = (const uint4 *)(p.g_fb + o);
+  const uint4 *ur = (const uint4 *)(p.u_fb + o);
+  float4 *dz4 = (float4 *)(p.rdz + o), *du4 = (float4 *)(p.rdu + o), *h4 = (float4 *)(p.rhs + o);
+#pragma unroll
+  for (int v4 = 0; v4 < 4; ++v4) {
+    const uint4 gv = gr[v4];
+    const uint4 uv = p.gated ? ur[v4] : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u,
+                                                   0x3F803F80u);  // u = 1
+    const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w}, ua[4] = {uv.x, uv.y, uv.z, uv.w};
+    float dz[8], du[8], hv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float g = (e & 1) ? bf_hi(ga[e / 2]) : bf_lo(ga[e / 2]);
+      const float u = (e & 1) ? bf_hi(ua[e / 2]) : bf_lo(ua[e / 2]);
+      const float h = p.gated ? g * u : g;
+      const float dh = v[8 * v4 + e] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
+      const bool act = g > 0.f;
+      dz[e] = act ? (p.gated ? dh * u : dh) : 0.f;
+      du[e] = act ? dh * g : 0.f;
+      hv[e] = h;
+    }
+    dz4[2 * v4] = make_float4(dz[0], dz[1], dz[2], dz[3]);
+    dz4[2 * v4 + 1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
+    du4[2 * v4] = make_float4(du[0], du[1], du[2], du[3]);
+    du4[2 * v4 + 1] = make_float4(du[4], du[5], du[6], du[7]);
+    h4[2 * v4] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    h4[2 * v4 + 1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+  }
+}
+
+// EPI_DHS: copy the accumulator block v into the thread's shared-memory row
+// st, then dh[k] = the value at slot k's column for the slots in the block
+// (local columns cl .. cl + 31 of the TwELL tile).
+template <int NK>
+__device__ __forceinline__ void dhs_pick(float *st, const float (&v)[32], int cl, int K, int nz,
+                                         const uint32_t (&iw)[NK / 4 > 0 ? NK / 4 : 1],
+                                         float (&dh)[NK]) {
+  float4 *s4 = (float4 *)st;
+#pragma unroll
+  for (int v4 = 0; v4 < 8; ++v4)
+    s4[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    if (k >= K) break;  // uniform
+    const int c = (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu) - cl;
+    if (k < nz && (unsigned)c < 32u) dh[k] = st[c];
+  }
+}
+
+// The 32-column blocks of a TwELL tile that hold one of the first nz slots.
+template <int NK>
+__device__ __forceinline__ uint32_t dhs_blocks(const uint32_t (&iw)[NK / 4 > 0 ? NK / 4 : 1],
+                                               int K, int nz) {
+  uint32_t blk = 0;
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    if (k >= K) break;  // uniform
+    if (k < nz) blk |= 1u << (((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu) >> 5);
+  }
+  return blk;
+}
+
 template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -574,6 +695,27 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         fetch_slots(p, n0, tok_u, pf_nz, pf_iw, pf_vw);
         if ((EPI == EPI_DH || EPI == EPI_DHS) && p.gated)
           load_vals(p.uval + ((size_t)(n0 / p.C) * p.Tn + tok_u) * p.Kslots, p.Kslots, pf_qw);
+      }
+      // EPI_DHS with two 128-column TwELL tiles per output tile and K <= 8:
+      // the second tile's slots are fetched here as well, into a compact set
+      // (two full sets would not fit the register budget)
+      const bool pf2 = EPI == EPI_DHS && BN == 256 && p.C == 128 && p.Kslots <= 8;
+      int pf2_nz = 0;
+      uint32_t pf2_i[2] = {0u, 0u}, pf2_v[4] = {0u, 0u, 0u, 0u}, pf2_q[4] = {0u, 0u, 0u, 0u};
+      if (pf2 && row_ok && ps_u < 0 && n0 + 128 < p.N) {
+        const size_t jt2 = (size_t)((n0 + 128) / 128) * p.Tn + tok_u;
+        uint32_t iw[8], vw[16];
+        pf2_nz = p.nnz[jt2];
+        load_idx(p.idx + jt2 * p.Kslots, p.Kslots, iw);
+        pf2_i[0] = iw[0]; pf2_i[1] = iw[1];
+        load_vals(p.val + jt2 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pf2_v[i] = vw[i];
+        if (p.gated) {
+          load_vals(p.uval + jt2 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pf2_q[i] = vw[i];
+        }
       }
       const bool ok = mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status);
       if (!ok) break;
@@ -909,19 +1051,55 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       } else if (EPI == EPI_DHS) {
         // dh of the rows the gathers own (not the dense-path rows), from the
         // full product dy W_down^T but read only where the forward kept an
-        // active entry: at the row's TwELL slots, or at every column of an
-        // overflow row with a dense backup row.  Per entry, as the gather
-        // SDDMM: dh = acc + lambda sign(h), h = g u, dz = [g > 0] dh u,
-        // du = [g > 0] dh g (plain FFN: u = 1), in fp32, stored at the slot
-        // (with the sparse transpose's count of its column) or in the
-        // overflow-row arrays.  A thread picks its slots' columns out of the
-        // accumulator through its own shared-memory row, 32 columns at a time.
+        // active entry: at the row's TwELL slots (through the thread's
+        // shared-memory row, 32 columns at a time, only for blocks that hold
+        // a slot), or at every column of an overflow row with a dense backup
+        // row; then the gradients of each entry as the gather SDDMM stores
+        // them.  With two 128-column TwELL tiles and K <= 8 the slots of
+        // both are prefetched before the accumulator wait, every accumulator
+        // column is read, and the TMEM buffer is released before the slot
+        // gradients are computed and stored.  (Measured on the d_model 2048 /
+        // d_ff 8192 step: the epilogue's global loads and stores each add
+        // about 11 us to the 78 us mainloop -- they share the L1 / shared-
+        // memory datapath with the MMA operands -- so only live slots are
+        // stored: 102.6 -> 99.0 us.)
         const int tok = m;
         const int ps = ps_u;
         const bool skip = !row_ok || ps >= p.cap || (ps >= 0 && p.ctl->ovf_gemm);
         const int K = p.Kslots;
         float *st = (float *)s_slots + row * DHS_STRIDE;
         const int nch = (p.Tn + TR_CHUNK - 1) / TR_CHUNK;
+        if (pf2) {
+          const bool two = n0 + 128 < p.N;  // uniform: the second TwELL tile exists
+          const uint32_t i0[2] = {pf_iw[0], pf_iw[1]};
+          const uint32_t v0[4] = {pf_vw[0], pf_vw[1], pf_vw[2], pf_vw[3]};
+          const uint32_t q0[4] = {pf_qw[0], pf_qw[1], pf_qw[2], pf_qw[3]};
+          const int nz0 = min(pf_nz, K), nz1 = min(pf2_nz, K);
+          const uint32_t blk = dhs_blocks<8>(i0, K, nz0) | (dhs_blocks<8>(pf2_i, K, nz1) << 4);
+          float d0[8], d1[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) d0[k] = d1[k] = 0.f;
+#pragma unroll 1
+          for (int cb = 0; cb < 256; cb += 32) {
+            if (cb >= 128 && !two) break;  // uniform
+            float v[32];
+            tmem_ld32(tacc + cb, v);  // (warp-collective)
+            if (skip) continue;
+            if (ps >= 0) dhs_store_row_block(p, ps, n0 + cb, v);
+            else if ((blk >> (cb >> 5)) & 1u) {
+              if (cb < 128) dhs_pick<8>(st, v, cb, K, nz0, i0, d0);
+              else dhs_pick<8>(st, v, cb - 128, K, nz1, pf2_i, d1);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+          if (!skip && ps < 0) {
+            dhs_store_slots<8>(p, n0 / 128, tok, K, nz0, i0, v0, q0, d0, nch);
+            if (two) dhs_store_slots<8>(p, n0 / 128 + 1, tok, K, nz1, pf2_i, pf2_v, pf2_q, d1, nch);
+          }
+          continue;  // the buffer is released
+        }
         for (int jt = 0; jt < BN / p.C; ++jt) {
           const int n1 = n0 + jt * p.C;
           if (n1 >= p.N) break;  // uniform
@@ -930,6 +1108,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             if (p.gated) load_vals(p.uval + ((size_t)(n1 / p.C) * p.Tn + tok) * K, K, pf_qw);
           }
           const int nz = min(pf_nz, K);
+          const uint32_t blk = dhs_blocks<32>(pf_iw, K, nz);
           float dhv[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) dhv[k] = 0.f;
@@ -937,88 +1116,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             float v[32];
             tmem_ld32(tacc + jt * p.C + cb, v);  // (warp-collective)
             if (skip) continue;
-            if (ps >= 0) {  // overflow row: every column of the block
-              const size_t o = (size_t)ps * p.F + n1 + cb;
-              const uint4 *gr = (const uint4 *)(p.g_fb + o);
-              const uint4 *ur = (const uint4 *)(p.u_fb + o);
-              float4 *dz4 = (float4 *)(p.rdz + o), *du4 = (float4 *)(p.rdu + o);
-              float4 *h4 = (float4 *)(p.rhs + o);
-#pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                const uint4 gv = gr[v4];
-                const uint4 uv = p.gated ? ur[v4] : make_uint4(0x3F803F80u, 0x3F803F80u,
-                                                               0x3F803F80u, 0x3F803F80u);
-                const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w}, ua[4] = {uv.x, uv.y, uv.z, uv.w};
-                float dz[8], du[8], hv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const float g = (e & 1) ? bf_hi(ga[e / 2]) : bf_lo(ga[e / 2]);
-                  const float u = (e & 1) ? bf_hi(ua[e / 2]) : bf_lo(ua[e / 2]);
-                  const float h = p.gated ? g * u : g;
-                  const float dh = v[8 * v4 + e] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
-                  const bool act = g > 0.f;
-                  dz[e] = act ? (p.gated ? dh * u : dh) : 0.f;
-                  du[e] = act ? dh * g : 0.f;
-                  hv[e] = h;
-                }
-                dz4[2 * v4] = make_float4(dz[0], dz[1], dz[2], dz[3]);
-                dz4[2 * v4 + 1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
-                du4[2 * v4] = make_float4(du[0], du[1], du[2], du[3]);
-                du4[2 * v4 + 1] = make_float4(du[4], du[5], du[6], du[7]);
-                h4[2 * v4] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-                h4[2 * v4 + 1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
-              }
-            } else {  // slots: stage the block, pick the slots' columns
-              float4 *s4 = (float4 *)st;
-#pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4)
-                s4[v4] = make_float4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                if (k >= K) break;  // uniform
-                const int c = slot_col(pf_iw, k) - cb;
-                if (k < nz && (unsigned)c < 32u) dhv[k] = st[c];
-              }
-            }
+            if (ps >= 0) dhs_store_row_block(p, ps, n1 + cb, v);
+            else if ((blk >> (cb >> 5)) & 1u) dhs_pick<32>(st, v, cb, K, nz, pf_iw, dhv);
           }
           if (skip || ps >= 0) continue;
-          const int j = n1 / p.C;
-          const size_t s0 = ((size_t)j * p.Tn + tok) * K;
-#pragma unroll
-          for (int k0 = 0; k0 < 32; k0 += 4) {
-            if (k0 >= K) break;  // uniform
-            float dz[4], du[4], hv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k = k0 + i;
-              const bool live = k < nz;  // (pad slots store zeros)
-              const float g = live ? __uint_as_float((uint32_t)slot_val(pf_vw, k) << 16) : 0.f;
-              const float u = !p.gated ? 1.f
-                              : (live ? __uint_as_float((uint32_t)slot_val(pf_qw, k) << 16) : 0.f);
-              const float h = p.gated ? g * u : g;
-              const float dh = dhv[k] + p.lambda * (h > 0.f ? 1.f : (h < 0.f ? -1.f : 0.f));
-              const bool act = g > 0.f;
-              dz[i] = act ? (p.gated ? dh * u : dh) : 0.f;
-              du[i] = act ? dh * g : 0.f;
-              hv[i] = h;
-              const int c = slot_col(pf_iw, k);
-              if (live && c < p.C)  // the transpose's count (a malformed index is not listed)
-                atomicAdd(&p.col_chunk[((size_t)j * nch + tok / TR_CHUNK) * p.C + c], 1);
-            }
-            if (K % 4 == 0) {
-              *(float4 *)(p.sdz + s0 + k0) = make_float4(dz[0], dz[1], dz[2], dz[3]);
-              *(float4 *)(p.sdu + s0 + k0) = make_float4(du[0], du[1], du[2], du[3]);
-              *(float4 *)(p.shs + s0 + k0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (k0 + i >= K) break;
-                p.sdz[s0 + k0 + i] = dz[i];
-                p.sdu[s0 + k0 + i] = du[i];
-                p.shs[s0 + k0 + i] = hv[i];
-              }
-            }
-          }
+          dhs_store_slots<32>(p, n1 / p.C, tok, K, nz, pf_iw, pf_vw, pf_qw, dhv, nch);
         }
       } else if (EPI == EPI_DW) {
         // Weight-gradient rows (row m = neuron, fp32) of problem q: stored
