@@ -8,19 +8,25 @@
 //   dx = sum_n dz Wg[n] + du Wu[n]
 //   dWg[n] = sum_t dz x_t, dbg[n] = sum_t dz, dWu[n] = sum_t du x_t,
 //   dWd[n] = sum_t h dy_t
-// Launch sequence (all on the caller's stream):
+// Launch sequence (on the caller's stream, except where noted):
 //   1. hybrid split of the saved TwELL (overflow rows, in this workspace)
-//   2. one CTA per token, two passes: dh at its active pairs from gathered
-//      W_down rows, then dz / du / h at those pairs (hybrid x dense SDDMM);
-//      then its dx row from gathered W_gate / W_up rows (dense x hybrid
-//      SpMM).  Pairs come from the TwELL slots, or from the dense backup row
-//      of an overflow row.  Two passes keep each pass's working set (one or
-//      two weight matrices) small enough to stay in L2.
+//   2. dh at the active pairs, then dz / du / h there: one CTA per token
+//      from gathered W_down rows (hybrid x dense SDDMM), or, above a slot
+//      density, one tensor-core GEMM dy W_down^T read at the slots; then a
+//      CTA per token builds its dx row from gathered W_gate / W_up rows
+//      (dense x hybrid SpMM).  Pairs come from the TwELL slots, or from the
+//      dense backup row of an overflow row.  Separate passes keep each
+//      pass's working set (one or two weight matrices) small enough to stay
+//      in L2.
 //   3. a CTA per (tile, chunk of 1024 tokens): deterministic transpose of
 //      the slots into neuron-major lists ordered by token (sparse
 //      transpose), from per-chunk column counts taken in step 2
 //   4. one CTA per neuron: dWg, dWu, dWd rows and dbg from gathered x / dy rows
 //      of its list, then the overflow rows' contributions (dense x hybrid)
+// Steps 3-4 depend on step 2 only, as does the dx SpMM: they run on a second
+// stream of the library, forked and joined with events, so the transpose and
+// the kernels' tails overlap the SpMM (one stream while per-launch timing is
+// on, so that each interval times one kernel).
 #include "common.cuh"
 #include "gather.cuh"
 #include "kernels.h"
@@ -591,6 +597,37 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 }
 
 // ---------------------------------------------------------------------------
+namespace {
+
+// The second stream and its fork / join events, one set per host thread and
+// device (created on first use, kept for the life of the process).
+struct AuxStream {
+  cudaStream_t s2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t aux_stream(AuxStream *&out) {
+  static thread_local AuxStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  AuxStream &a = per_dev[dev];
+  if (!a.s2) {
+    e = cudaStreamCreateWithFlags(&a.s2, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      a.s2 = nullptr;
+      return e;
+    }
+  }
+  out = &a;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   BParams p;
   p.x = a.x; p.Wg = a.Wg; p.Wu = a.Wu; p.Wd = a.Wd; p.dy = a.dy;
@@ -682,38 +719,66 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_mark(KID_BWD_SLOTS, s);
-#define TW_VPT(K, TT, G)                                                                       \
+#define TW_VPT(K, TT, G, SS)                                                                   \
   do {                                                                                         \
-    if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, s, p);                               \
-    else if (vpt == 2 && NV == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, s, p);               \
-    else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, s, p);                          \
-    else launch_k(K<TT, 4, 2, 0>, G, threads, 0, s, p);                                        \
+    if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, SS, p);                              \
+    else if (vpt == 2 && NV == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, SS, p);              \
+    else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, SS, p);                         \
+    else launch_k(K<TT, 4, 2, 0>, G, threads, 0, SS, p);                                       \
   } while (0)
-  if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T);
-  else TW_VPT(bwd_dx_kernel, float, a.T);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  prof_mark(KID_BWD_DX, s);
-  // 3. transpose
+  // Steps 3-4 on the second stream (the caller's while per-launch timing is
+  // on): forked here, after dh, and joined before returning.
+  const bool fork = !prof_enabled();
+  AuxStream *aux = nullptr;
+  cudaStream_t sw = s;
+  if (fork) {
+    e = aux_stream(aux);
+    if (e == cudaSuccess) e = cudaEventRecord(aux->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->s2, aux->fork, 0);
+    if (e != cudaSuccess) return e;
+    sw = aux->s2;
+  }
   const int nt = a.F / a.C;
   const dim3 tgrid(nt, (a.T + TR_CHUNK - 1) / TR_CHUNK);
-  // (the per-chunk column counts were taken by the dh kernels)
-  if (a.C == 32) launch_k(twell_transpose_kernel<32>, tgrid, TR_CHUNK, 0, s, p);
-  else if (a.C == 64) launch_k(twell_transpose_kernel<64>, tgrid, TR_CHUNK, 0, s, p);
-  else launch_k(twell_transpose_kernel<128>, tgrid, TR_CHUNK, 0, s, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  prof_mark(KID_BWD_TRANSPOSE, s);
-  // 4. weight gradients
-  if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F);
-  else TW_VPT(bwd_dw_kernel, float, a.F);
+  auto transpose = [&]() {  // 3. (the per-chunk column counts were taken with dh)
+    if (a.C == 32) launch_k(twell_transpose_kernel<32>, tgrid, TR_CHUNK, 0, sw, p);
+    else if (a.C == 64) launch_k(twell_transpose_kernel<64>, tgrid, TR_CHUNK, 0, sw, p);
+    else launch_k(twell_transpose_kernel<128>, tgrid, TR_CHUNK, 0, sw, p);
+    const cudaError_t r = cudaGetLastError();
+    prof_mark(KID_BWD_TRANSPOSE, sw);
+    return r;
+  };
+  auto dx_spmm = [&]() {
+    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s);
+    else TW_VPT(bwd_dx_kernel, float, a.T, s);
+    const cudaError_t r = cudaGetLastError();
+    prof_mark(KID_BWD_DX, s);
+    return r;
+  };
+  // the transpose first when forked: it is short and heads the longer chain
+  if (fork) {
+    e = transpose();
+    if (e == cudaSuccess) e = dx_spmm();
+  } else {
+    e = dx_spmm();
+    if (e == cudaSuccess) e = transpose();
+  }
+  if (e == cudaSuccess) {  // 4. weight gradients
+    if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw);
+    else TW_VPT(bwd_dw_kernel, float, a.F, sw);
+    e = cudaGetLastError();
+    prof_mark(KID_BWD_DW, sw);
+  }
 #undef TW_VPT
-  e = cudaGetLastError();
-  prof_mark(KID_BWD_DW, s);
   // 5. weight gradients of the dense-path rows (added to those of step 4)
   if (e == cudaSuccess && gemm) {
-    e = launch_tc_bwd_dw(a, s);
-    prof_mark(KID_BWD_DENSE_DW, s);
+    e = launch_tc_bwd_dw(a, sw);
+    prof_mark(KID_BWD_DENSE_DW, sw);
+  }
+  if (fork) {  // join (also after an error, so the caller's stream stays ordered)
+    const cudaError_t j1 = cudaEventRecord(aux->join, sw);
+    const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, aux->join, 0) : j1;
+    if (e == cudaSuccess) e = j2;
   }
   return e;
 }

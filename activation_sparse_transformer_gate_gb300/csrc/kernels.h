@@ -160,6 +160,8 @@ enum KernelId {
 // Record a timing event after `launches` kernel launches of component `id`
 // (no-op unless enabled).
 void prof_mark(int id, cudaStream_t s, int launches = 1);
+// True while per-launch timing is on (the backward then stays on one stream).
+bool prof_enabled();
 
 // rowell.cu (row-ELL comparison baseline)
 cudaError_t launch_rowell_pack_dense(const void *H, int T, int F, int E, int dtype, uint16_t *idx,

@@ -40,6 +40,8 @@ Profiler &profiler() {
 }
 }  // namespace
 
+bool prof_enabled() { return profiler().on; }
+
 void prof_mark(int kid, cudaStream_t s, int launches) {
   Profiler &p = profiler();
   if (!p.on) return;

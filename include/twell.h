@@ -160,7 +160,13 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
  *   dWg[n] = sum_t dz x_t, dbg[n] = sum_t dz, dWu[n] = sum_t du x_t,
  *   dWd[n] = sum_t h dy_t              (fp32, overwritten, not accumulated)
  * Plain FFN (Wu == NULL, dWu ignored): dz = [z>0] dh.  Only active (row,
- * neuron) pairs are visited; rows of never-active neurons are written 0. */
+ * neuron) pairs are visited; rows of never-active neurons are written 0.
+ * Ordering: the weight-gradient kernels run on a second stream of the
+ * library (one per host thread and device, created on first use), forked
+ * from `stream` after dh and joined back with events before the call
+ * returns, so all work is ordered with `stream` as if it ran there (also
+ * under stream capture).  While per-launch timing (twell_profile_begin) is
+ * on, everything runs on `stream`. */
 twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, const void *Wd,
                                 const twell_t *tw, const void *dy, float lambda, int D,
                                 void *dx, float *dWg, float *dbg, float *dWu, float *dWd,
