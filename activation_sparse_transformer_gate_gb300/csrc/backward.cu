@@ -597,15 +597,6 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 }
 
 // ---------------------------------------------------------------------------
-namespace {
-
-// The second stream and its fork / join events, one set per host thread and
-// device (created on first use, kept for the life of the process).
-struct AuxStream {
-  cudaStream_t s2 = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-
 cudaError_t aux_stream(AuxStream *&out) {
   static thread_local AuxStream per_dev[64];
   int dev = 0;
@@ -625,8 +616,6 @@ cudaError_t aux_stream(AuxStream *&out) {
   out = &a;
   return cudaSuccess;
 }
-
-}  // namespace
 
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   BParams p;

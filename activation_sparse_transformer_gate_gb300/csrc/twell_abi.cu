@@ -326,11 +326,31 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   a.dense_density = density_of(tw, D, gated, false);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = run_gate_and_split(a, s);
+  // The dense-path rows (tensor cores) and the gathers own disjoint rows:
+  // the dense-path kernels run on the library's second stream, launched
+  // first, beside the up/down gathers (one stream while per-launch timing
+  // is on).  With few dense-path rows their GEMMs fill a fraction of the
+  // GPU for a whole wave, which the gathers then use.
+  const bool fork = e == cudaSuccess && use_tc(a.dtype) && !prof_enabled();
+  AuxStream *aux = nullptr;
+  if (fork) {
+    e = aux_stream(aux);
+    if (e == cudaSuccess) e = cudaEventRecord(aux->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->s2, aux->fork, 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = run_dense_rows(a, true, aux->s2);
+  }
   if (e == cudaSuccess) {
     e = launch_updown_fused(a, s);
     prof_mark(KID_UPDOWN, s);
   }
-  if (e == cudaSuccess) e = run_dense_rows(a, true, s);
+  if (fork) {  // join (also after an error, so the caller's stream stays ordered)
+    const cudaError_t j1 = cudaEventRecord(aux->join, aux->s2);
+    const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, aux->join, 0) : j1;
+    if (e == cudaSuccess) e = j2;
+  } else if (e == cudaSuccess) {
+    e = run_dense_rows(a, true, s);
+  }
   // all-dense training: u at the slots of non-overflow rows (the tensor-core
   // up GEMM writes them in its epilogue)
   if (e == cudaSuccess && a.train && a.gated && !use_tc(a.dtype)) {

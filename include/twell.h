@@ -147,7 +147,10 @@ twell_status twell_pack(const void *x, const void *Wg, const float *bg, const fl
  * slots exceed dense_density * T * F).
  * Wu == NULL selects the plain FFN y = ReLU(z) Wd.  y [T][D] dtype.
  * train != 0 additionally stores u at the slots (tw->u_val) and the u rows of
- * the overflow rows (tw->u_fb) for twell_ffn_backward. */
+ * the overflow rows (tw->u_fb) for twell_ffn_backward.
+ * Ordering: on the bf16 tensor-core path the dense-row kernels run on the
+ * library's second stream (as in twell_ffn_backward), forked from `stream`
+ * after the overflow split and joined back before the call returns. */
 twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
                                const float *row_bias, const void *Wu, const void *Wd, int D,
                                int train, twell_t *tw, void *y, void *workspace,
