@@ -608,8 +608,12 @@ cudaError_t aux_stream(AuxStream *&out) {
     e = cudaStreamCreateWithFlags(&a.s2, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
-    if (e != cudaSuccess) {
+    if (e != cudaSuccess) {  // release what was made; the next call tries again
+      if (a.join) cudaEventDestroy(a.join);
+      if (a.fork) cudaEventDestroy(a.fork);
+      if (a.s2) cudaStreamDestroy(a.s2);
       a.s2 = nullptr;
+      a.fork = a.join = nullptr;
       return e;
     }
   }

@@ -176,13 +176,22 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);
 // backward.cu
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s);
 // The library's second stream and its fork / join events, one set per host
-// thread and device (created on first use, kept for the life of the
-// process): work forked onto it after a record of `fork` on the caller's
-// stream is joined back by a record of `join` and a wait on the caller's
-// stream.
+// thread and device (created on first use, released when the thread exits):
+// work forked onto it after a record of `fork` on the caller's stream is
+// joined back by a record of `join` and a wait on the caller's stream.
 struct AuxStream {
   cudaStream_t s2 = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  AuxStream() = default;
+  AuxStream(const AuxStream &) = delete;
+  AuxStream &operator=(const AuxStream &) = delete;
+  // (work still queued on s2 completes; errors at process teardown, when the
+  // runtime may already be unloaded, are ignored)
+  ~AuxStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s2) cudaStreamDestroy(s2);
+  }
 };
 cudaError_t aux_stream(AuxStream *&out);
 
