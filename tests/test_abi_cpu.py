@@ -118,3 +118,29 @@ def test_backward_rejects_bad_args(lib):
              None, good, good, P(1 << 42), need, None) == -1          # NULL dbg
     assert f(good, good, None, good, ctypes.byref(t), good, ctypes.c_float(0.0), 128, good, good,
              good, good, good, P(1 << 42), need - 1, None) == -8      # workspace
+
+
+def header_struct_fields(name):
+    """Field names, in order, of `typedef struct { ... } name;` in include/twell.h."""
+    src = open(os.path.join(ROOT, "include", "twell.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    m = re.search(r"typedef\s+struct\s*\{([^{}]*)\}\s*" + name + r"\s*;", src)
+    assert m, name
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        # "type a, *b, c" -> a, b, c
+        parts = decl.split(",")
+        first = re.findall(r"\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*$", parts[0])
+        fields += first + [re.sub(r"[\s\*]", "", p) for p in parts[1:]]
+    return fields
+
+
+@pytest.mark.parametrize("name", ["twell_t", "twell_rowell_t"])
+def test_binding_structs_match_the_header(name):
+    """The ctypes mirrors of the ABI structs list the header's fields in the
+    header's order (a field added on one side only would shift the others)."""
+    py = [f[0] for f in getattr(tw, name)._fields_]
+    assert py == header_struct_fields(name)
