@@ -326,6 +326,8 @@ DH_GEMM_CASES = {
     "many_overflow_rows": (dict(T=600, D=256, F=1024, C=128, K=8, gated=True, bg=-2.33, seed=63,
                                 hot_tokens=2, seq_len=7, hot_bias=1.6), 1e-3),
     "c32_k2": (dict(T=192, D=128, F=512, C=32, K=2, gated=True, bg=-2.6, seed=64), 1e-2),
+    "nongated_c128_k8": (dict(T=260, D=256, F=768, C=128, K=8, gated=False, bg=-2.2, seed=71,
+                              hot_tokens=2, seq_len=65, hot_bias=1.5), 0.05),
     "c128_k32": (dict(T=96, D=128, F=512, C=128, K=32, gated=True, bg=-1.9, seed=65), 1e-2),
     "dff_384_ragged": (dict(T=333, D=192, F=384, C=128, K=8, gated=True, bg=-1.8, seed=66,
                             hot_tokens=2, seq_len=111, hot_bias=1.5), 1e-3),
@@ -404,3 +406,19 @@ def test_config5_full_size_default_dispatcher():
     ns = np.unique(np.concatenate([np.arange(8), rng.choice(w.F, 24, replace=False)]))
     check_backward(a, w, g, w.lam, tok_sel=ts, neu_sel=ns)
     assert np.isfinite(g["dWg"]).all() and np.isfinite(g["dx"]).all()
+
+
+@pytest.mark.parametrize("dh_density", [1e-9, -1.0], ids=["dh_gemm", "dh_sddmm"])
+def test_dense_forward_then_sparse_backward_bf16(dh_density):
+    """~1.5% active with the dispatcher's default thresholds: the forward runs
+    every row densely (its up GEMM writes u at the slots) while the backward,
+    whose threshold is higher, gathers and reads that u."""
+    w = synth.Workload("dfsb", 256, 256, 1024, 128, 8, "bf16", True, -2.17, 72, train=True)
+    a = synth.generate(w)
+    out = {}
+    g = run_train(a, w, 1e-3, dense_density=0.0, out=out, dh_density=dh_density)
+    assert g["code"] == 0
+    assert ctl_fields(out["ctl"])[1] == 1       # the forward ran densely
+    assert ctl_fields(out["ctl_bwd"])[:2] == (0, 0)  # the backward gathered
+    assert dh_gemm_of(out["ctl_bwd"]) == (1 if dh_density > 0 else 0)
+    check_backward(a, w, g, 1e-3)
