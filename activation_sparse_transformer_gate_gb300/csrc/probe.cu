@@ -1,4 +1,5 @@
-// probe.cu -- measurement hook (exported, not part of the public ABI in
+// probe.cu -- measurement hook, compiled only into the test-hooks variant of
+// the library (not into libtwell.so; not part of the public ABI in
 // include/twell.h): the rate at which this GPU gathers rows of a matrix in
 // an arbitrary order, the access pattern of the sparse projections.  Warps
 // take consecutive entries of a row list; every lane loads its 16-byte
@@ -8,6 +9,7 @@
 // fits in L2), against which the gather kernels can be read.
 #include "common.cuh"
 #include "kernels.h"
+#include "test_hooks.h"
 
 namespace twell {
 

@@ -7,13 +7,15 @@
 // allocator.  For them this entry point keeps its scratch (the overflow-row
 // bitmap, the full row list, per-row positions and the control block that the
 // workspace-based split uses) in one file-scope device array of fixed size,
-// so a call needs nothing but the caller's TwELL buffers.
+// so a call needs nothing but the caller's TwELL buffers: it makes no
+// cudaMalloc or cudaFree call and uses no allocating library routine.
 //
 // The array lives in the library image: every GPU that loads the library
 // holds it (about 2 MiB) until the process exits.  All calls share it and it
 // keeps the previous call's contents; the bitmap is cleared at the start of
 // every call.  Calls that overlap on the GPU (different streams, or different
 // host threads on the same device without ordering) race on it.
+#include <cuda.h>
 #include <string.h>
 
 #include <mutex>
@@ -37,25 +39,69 @@ static_assert(kMaxT % 32 == 0 && kBitsBytes % 256 == 0 && kRowsBytes % 256 == 0,
 // on the host it is a stand-in, not a device address.
 static __device__ __align__(256) unsigned char g_split_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// The array's address belongs to a CUDA context: a device reset (or another
+// context on the same device) gives the array another address.  The address
+// is therefore looked up once per context, identified by the driver's
+// process-unique context id (a context handle may be reused after a reset;
+// its id is not), with that context current, and cached.
+constexpr int kMaxContexts = 64;
+struct CtxAddr {
+  unsigned long long ctx_id;
+  unsigned char *ptr;
+};
 std::mutex g_mu;
-unsigned char *g_ptr[kMaxDevices] = {};
+CtxAddr g_addr[kMaxContexts] = {};
+int g_n_addr = 0;
 
-// Device address of the array on the current device (looked up once per
-// device, with that device current).
-cudaError_t scratch_ptr(unsigned char **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> g(g_mu);
-  if (!g_ptr[dev]) {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <class Fn>
+Fn driver_fn(const char *name) {
+  void *f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return (Fn)f;
+}
+
+// Id of the current context.  The runtime creates its context lazily: when
+// none is current yet, the symbol lookup (which needs one) creates it first.
+cudaError_t current_ctx_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_cur || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (!ctx) {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_split_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_split_scratch);
     if (e != cudaSuccess) return e;
-    g_ptr[dev] = (unsigned char *)p;
+    if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorUnknown;
   }
-  *out = g_ptr[dev];
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Device address of the array in the current context (looked up with that
+// context current on the first call in it).
+cudaError_t scratch_ptr(unsigned char **out) {
+  unsigned long long id = 0;
+  cudaError_t e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(g_mu);
+  for (int i = 0; i < g_n_addr; ++i)
+    if (g_addr[i].ctx_id == id) {
+      *out = g_addr[i].ptr;
+      return cudaSuccess;
+    }
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_split_scratch);
+  if (e != cudaSuccess) return e;
+  // keep the most recent contexts (a process rarely has more than one per device)
+  const int slot = g_n_addr < kMaxContexts ? g_n_addr++ : (int)(id % kMaxContexts);
+  g_addr[slot] = {id, (unsigned char *)p};
+  *out = (unsigned char *)p;
   return cudaSuccess;
 }
 

@@ -32,9 +32,12 @@
 //   warps 2..5  epilogue: tcgen05.ld 32x32b (thread = accumulator row),
 //               fused element-wise work and stores.  Two TMEM accumulators
 //               alternate so the epilogue of tile i overlaps the MMAs of i+1.
-// Every mbarrier wait is bounded by a 2-second global-timer limit; on expiry
-// the CTA records TWELL_ERR_TIMEOUT in the status word, drains, frees its TMEM
-// and returns.
+// Every mbarrier wait of the pipeline is bounded by a global-timer limit
+// (TWELL_WAIT_LIMIT_NS, 2 s unless the build sets another); on expiry the CTA
+// records TWELL_ERR_TIMEOUT in the status word, waits (with a fixed 2 s limit
+// of its own) for the copies and MMAs it has in flight, frees its TMEM and
+// returns.  The four epilogue warps take the outcome of each wait together,
+// so they leave their loop at the same tile.
 #include <cuda.h>
 #include <stdio.h>
 #include <string.h>
@@ -43,7 +46,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "tc_test.h"
+#include "test_hooks.h"
 
 namespace twell {
 
@@ -53,7 +56,16 @@ constexpr int BM = 128, BK = 64, NTHREADS = 192;
 // bf16 elements per row of the EPI_U g staging: 32 columns, a spare element
 // for scattered slots outside the block, padding to 16 bytes
 constexpr int GZ_STRIDE = 40;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+// Limit of a pipeline wait (a build may shorten it to make the waits run out
+// on a sane input: the timeout path is then exercised without a fault).
+#ifndef TWELL_WAIT_LIMIT_NS
+#define TWELL_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t WAIT_LIMIT_NS = TWELL_WAIT_LIMIT_NS;
+// Limit of the waits for work already in flight before a CTA exits (TMA
+// copies into shared memory, MMAs writing TMEM): always long, since leaving
+// earlier would free memory that the hardware still writes.
+constexpr uint64_t DRAIN_LIMIT_NS = 2000000000ull;
 
 enum Epi { EPI_PACK = 0, EPI_GU = 1, EPI_DOWN = 2, EPI_F32 = 3, EPI_U = 4, EPI_DH = 5, EPI_DX = 6,
            EPI_DW = 7, EPI_DHS = 8 };
@@ -255,6 +267,21 @@ __device__ __forceinline__ void epi_bar() {  // named barrier of the 4 epilogue 
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// The same barrier with an AND of v over the 128 epilogue threads: every
+// thread gets the same answer, so a decision taken on it is uniform (the
+// warp-collective tcgen05.ld and the named barrier need all four warps on
+// the same path).
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 // --------------------------------------------------------------- params --
 // Operand tensor maps.  a[0] / b[0]: gathered rows (dense-path rows of the
 // hybrid), a[1] / b[1]: the operand in place (all-dense mode), or the second
@@ -353,6 +380,8 @@ __device__ __forceinline__ void dhs_store_slots(const TcParams &p, int j, int to
       const int c = (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu);
       if (live && c < p.C)  // the transpose's count (a malformed index is not listed)
         atomicAdd(&p.col_chunk[((size_t)j * nch + tok / TR_CHUNK) * p.C + c], 1);
+      else if (live)
+        set_status(p.status, TWELL_ERR_INDEX);
     }
     if (K % 4 == 0) {
       *(float4 *)(p.sdz + s0 + k0) = make_float4(dz[0], dz[1], dz[2], dz[3]);
@@ -425,15 +454,19 @@ __device__ __forceinline__ void dhs_pick(float *st, const float (&v)[32], int cl
   }
 }
 
-// The 32-column blocks of a TwELL tile that hold one of the first nz slots.
+// The 32-column blocks of a TwELL tile (C columns) that hold one of the
+// first nz slots.  A malformed index (>= C) names no block: it would
+// otherwise set a bit of a block past the tile (the next tile's, where two
+// tiles share an output tile).
 template <int NK>
 __device__ __forceinline__ uint32_t dhs_blocks(const uint32_t (&iw)[NK / 4 > 0 ? NK / 4 : 1],
-                                               int K, int nz) {
+                                               int K, int nz, int C) {
   uint32_t blk = 0;
 #pragma unroll
   for (int k = 0; k < NK; ++k) {
     if (k >= K) break;  // uniform
-    if (k < nz) blk |= 1u << (((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu) >> 5);
+    const int c = (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+    if (k < nz && c < C) blk |= 1u << (c >> 5);
   }
   return blk;
 }
@@ -604,7 +637,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           const long last = s + (long)S * ((issued - 1 - s) / S);
           const uint32_t par = (uint32_t)((last / S) & 1);
           const uint64_t t0 = global_timer();
-          while (!mbar_try(full0 + 8 * s, par) && global_timer() - t0 < WAIT_LIMIT_NS / 4) {
+          while (!mbar_try(full0 + 8 * s, par) && global_timer() - t0 < DRAIN_LIMIT_NS) {
           }
         }
       }
@@ -658,7 +691,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       // All MMAs issued by this thread are complete before TMEM is freed.
       mma_commit(mma_done);
       const uint64_t t0 = global_timer();
-      while (!mbar_try(mma_done, 0) && global_timer() - t0 < WAIT_LIMIT_NS) {
+      while (!mbar_try(mma_done, 0) && global_timer() - t0 < DRAIN_LIMIT_NS) {
       }
     }
   } else {
@@ -717,7 +750,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           for (int i = 0; i < 4; ++i) pf2_q[i] = vw[i];
         }
       }
-      const bool ok = mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status);
+      // Each epilogue thread waits (bounded) for the accumulator; the AND of
+      // the outcomes is taken at a barrier, so if any thread gave up (or
+      // another role aborted) all four warps leave here together.
+      const bool ok = epi_all(mbar_wait(tfull0 + 8 * buf, use & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NB * BN);
@@ -992,6 +1028,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
                   load_vals(p.uval + ((size_t)((n0 + c0) / p.C) * p.Tn + tok) * K, K, pf_qw);
               }
               const int nz = min(pf_nz, K);
+              if (cl == 0) {  // a malformed live slot (index >= C) lands in no block
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  if (k >= K) break;  // uniform
+                  if (k < nz && slot_col(pf_iw, k) >= p.C) set_status(p.status, TWELL_ERR_INDEX);
+                }
+              }
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4) {
                 ((uint4 *)gz)[v4] = make_uint4(0, 0, 0, 0);
@@ -1075,7 +1118,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           const uint32_t v0[4] = {pf_vw[0], pf_vw[1], pf_vw[2], pf_vw[3]};
           const uint32_t q0[4] = {pf_qw[0], pf_qw[1], pf_qw[2], pf_qw[3]};
           const int nz0 = min(pf_nz, K), nz1 = min(pf2_nz, K);
-          const uint32_t blk = dhs_blocks<8>(i0, K, nz0) | (dhs_blocks<8>(pf2_i, K, nz1) << 4);
+          const uint32_t blk =
+              dhs_blocks<8>(i0, K, nz0, 128) | (dhs_blocks<8>(pf2_i, K, nz1, 128) << 4);
           float d0[8], d1[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) d0[k] = d1[k] = 0.f;
@@ -1108,7 +1152,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             if (p.gated) load_vals(p.uval + ((size_t)(n1 / p.C) * p.Tn + tok) * K, K, pf_qw);
           }
           const int nz = min(pf_nz, K);
-          const uint32_t blk = dhs_blocks<32>(pf_iw, K, nz);
+          const uint32_t blk = dhs_blocks<32>(pf_iw, K, nz, p.C);
           float dhv[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) dhv[k] = 0.f;
@@ -1470,8 +1514,11 @@ cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s) {
   return launch_tc<256, 1, true, EPI_DW, true>(maps, p, tiles, s);
 }
 
-// Test hook: fp32 C[M][N] = op(A) op(B), bf16 operands.  layout bit 0: B is
-// [K][N] (MN-major), else [N][K]; bit 1: A is [K][M] (MN-major), else [M][K].
+#ifdef TWELL_TEST_HOOKS
+// Test hook (built only into the test-hooks library, never into
+// libtwell.so): fp32 C[M][N] = op(A) op(B), bf16 operands.  layout bit 0: B
+// is [K][N] (MN-major), else [N][K]; bit 1: A is [K][M] (MN-major), else
+// [M][K].
 cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N, int K, int layout,
                          int32_t *status, cudaStream_t s) {
   const bool b_mn = (layout & 1) != 0, a_mn = (layout & 2) != 0;
@@ -1496,8 +1543,11 @@ cudaError_t tc_test_gemm(const void *A, const void *B, float *Cout, int M, int N
   }
 }
 
+#endif  // TWELL_TEST_HOOKS
+
 }  // namespace twell
 
+#ifdef TWELL_TEST_HOOKS
 extern "C" int twell_test_tc_gemm(const void *A, const void *B, float *C, int M, int N, int K,
                                   int layout, int32_t *status, void *stream) {
   if (!twell::tc_available()) return TWELL_ERR_UNSUPPORTED;
@@ -1507,3 +1557,4 @@ extern "C" int twell_test_tc_gemm(const void *A, const void *B, float *C, int M,
   cudaError_t e = twell::tc_test_gemm(A, B, C, M, N, K, layout, status, (cudaStream_t)stream);
   return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
+#endif  // TWELL_TEST_HOOKS

@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-energy", action="store_true",
                     help="skip the saved-memory and energy-per-token leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the compact records of the other workloads' forward")
     ap.add_argument("--compare-formats", action="store_true",
                     help="forward: TwELL against classic row-ELL and against an unfused pack "
                          "(dense gate GEMM + standalone conversion), same inputs")
@@ -71,7 +73,9 @@ def parse_args():
 
 
 def workload_of(name: str, train: bool) -> synth.Workload:
-    if name == "c2":
+    if name == "c1":
+        w = synth.config1()
+    elif name == "c2":
         w = synth.config5() if train else synth.config2()
     elif name == "c3":
         w = synth.config3()
@@ -89,8 +93,9 @@ def describe(w: synth.Workload, train: bool) -> str:
     from scipy.stats import norm
     zero = 100.0 * norm.cdf(-w.bias) if w.bias < 0 else 100.0 * (1 - norm.cdf(w.bias))
     kind = f"training step (fwd+bwd, L1 lambda={w.lam})" if train else "inference forward"
-    s = (f"{kind} of the gated ReLU FFN, bf16, T={w.T} d_model={w.D} d_ff={w.F}, TwELL tile {w.C}"
-         f" K={w.K}, gate bias {w.bias} (~{zero:.1f}% zero)")
+    s = (f"{kind} of the {'gated' if w.gated else 'plain'} ReLU FFN, {w.dtype}, T={w.T} "
+         f"d_model={w.D} d_ff={w.F}, TwELL tile {w.C} K={w.K}, gate bias {w.bias} "
+         f"(~{zero:.1f}% zero)")
     if w.hot_tokens:
         s += f", first {w.hot_tokens} of every {w.seq_len} tokens at bias {w.bias + w.hot_bias:.2f}"
     return s
@@ -147,50 +152,68 @@ def upload(torch, dev, v):
     return torch.from_numpy(v).to(dev)
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-    import activation_sparse_transformer_gate_gb300 as tw
-    from activation_sparse_transformer_gate_gb300 import _build
+class Bench:
+    """Device state of one workload: inputs, TwELL buffers, workspace, outputs
+    and the step (forward, or forward + backward) through the C ABI."""
 
-    if rank == 0:
-        _build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    lib = tw.load()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    train = args.mode == "train"
-    w = workload_of(args.workload, train)
-    a = synth.generate(w)
-    dtype = tw.TWELL_BF16
-    d = {k: upload(torch, dev, a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
-    T, D, F = w.T, w.D, w.F
-    bufs = tw.TwellBuffers(T, F, w.C, w.K, dtype, train=train, device=dev,
-                           dense_density=args.dense_density, dh_density=args.dh_density)
-    ws, nws = tw.workspace(T, D, F, w.C, w.K, dtype, train, device=dev)
-    y = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
-    dx = dWg = dWu = dWd = dbg = None
-    if train:
-        dx = torch.empty_like(d["x"])
-        dWg = torch.empty((F, D), dtype=torch.float32, device=dev)
-        dWu, dWd = torch.empty_like(dWg), torch.empty_like(dWg)
-        dbg = torch.empty((F,), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-
-    def step(x=None, dy=None, y_out=None, dx_out=None):
-        xx = d["x"] if x is None else x
-        tw.twell_ffn_forward(xx, d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, int(train),
-                             bufs.t, y if y_out is None else y_out, ws, nws, sh)
+    def __init__(self, torch, tw, w, train, dev, args, a=None):
+        self.torch, self.tw, self.w, self.train, self.dev = torch, tw, w, train, dev
+        self.a = synth.generate(w) if a is None else a
+        self.dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.d = d = {k: upload(torch, dev, self.a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
+        T, D, F = w.T, w.D, w.F
+        self.bufs = tw.TwellBuffers(T, F, w.C, w.K, self.dtype, train=train, device=dev,
+                                    dense_density=args.dense_density,
+                                    dh_density=args.dh_density)
+        self.ws, self.nws = tw.workspace(T, D, F, w.C, w.K, self.dtype, train, device=dev)
+        self.y = torch.empty((T, D), dtype=tdt, device=dev)
+        self.dx = self.dWg = self.dWu = self.dWd = self.dbg = None
         if train:
-            tw.twell_ffn_backward(xx, d["Wg"], d["Wu"], d["Wd"], bufs.t,
-                                  d["dy"] if dy is None else dy, w.lam, D,
-                                  dx if dx_out is None else dx_out, dWg, dbg, dWu, dWd, ws, nws,
-                                  sh)
+            self.dx = torch.empty_like(d["x"])
+            self.dWg = torch.empty((F, D), dtype=torch.float32, device=dev)
+            self.dWu = torch.empty_like(self.dWg) if w.gated else None
+            self.dWd = torch.empty_like(self.dWg)
+            self.dbg = torch.empty((F,), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.sh = self.stream.cuda_stream
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
+    def step(self, x=None, dy=None, y_out=None, dx_out=None):
+        tw, d, w = self.tw, self.d, self.w
+        xx = d["x"] if x is None else x
+        tw.twell_ffn_forward(xx, d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], w.D, int(self.train),
+                             self.bufs.t, self.y if y_out is None else y_out, self.ws, self.nws,
+                             self.sh)
+        if self.train:
+            tw.twell_ffn_backward(xx, d["Wg"], d["Wu"], d["Wd"], self.bufs.t,
+                                  d["dy"] if dy is None else dy, w.lam, w.D,
+                                  self.dx if dx_out is None else dx_out, self.dWg, self.dbg,
+                                  self.dWu, self.dWd, self.ws, self.nws, self.sh)
 
+    def status(self):
+        return self.tw.twell_get_status(self.bufs.t, self.sh)
+
+    def dispatch(self):
+        """Rows the dispatcher sent to the dense path (control block n_rows) in
+        a lone forward and in the backward that follows it, and whether the
+        backward took dh from the tensor-core GEMM."""
+        torch, tw, d, w = self.torch, self.tw, self.d, self.w
+        tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], w.D,
+                             int(self.train), self.bufs.t, self.y, self.ws, self.nws, self.sh)
+        torch.cuda.synchronize(self.dev)
+        rows_f = int(self.ws[:4].view(torch.int32).item())
+        rows_b, dh_gemm = 0, False
+        if self.train:
+            tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], self.bufs.t, d["dy"], w.lam,
+                                  w.D, self.dx, self.dWg, self.dbg, self.dWu, self.dWd, self.ws,
+                                  self.nws, self.sh)
+            torch.cuda.synchronize(self.dev)
+            rows_b = int(self.ws[:4].view(torch.int32).item())
+            dh_gemm = bool(self.ws[24:28].view(torch.int32).item())  # control block: dh_gemm
+        return rows_f, rows_b, dh_gemm
+
+
+def make_timer(torch, dev, stream, flush_buf):
     per_step = []
 
     def timed(fn, steps, flush=True):
@@ -209,41 +232,17 @@ def run_ours(args, rank, world, local_rank):
         per_step[:] = [e0.elapsed_time(e1) for e0, e1 in evs]
         return sum(per_step)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    code, n_ovf = tw.twell_get_status(bufs.t, sh)
-    if code != 0:
-        raise SystemExit(f"device status {code} after warm-up")
-    sampler = None if (args.no_clocks or rank != 0) else ClockSampler(local_rank)
-    if sampler:
-        time.sleep(0.2)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    total_ms = timed(step, args.steps)
-    step_ms = sorted(per_step)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = max_over_ranks(torch, total_ms, world, dev)
-    clocks = sampler.stop() if sampler else None
-    code, n_ovf = tw.twell_get_status(bufs.t, sh)
-    if code != 0:
-        raise SystemExit(f"device status {code} after the timed region")
-    ms_step = total_ms / args.steps
-    value = T * world / (ms_step / 1e3)
-    if rank != 0:
-        return None
-    n_warm = max(10, min(args.steps, 100))
-    warm_ms = timed(step, n_warm, flush=False) / n_warm
+    return timed, per_step
 
-    # ---- per-kernel times inside the step (events on the launch stream) ----
-    prof_steps = max(5, min(50, args.steps))
+
+def kernel_profile(torch, lib, b, flush_buf, prof_steps):
+    """Per-kernel times inside the step: events the library records between
+    its own launches on the launch stream (one stream while this is on)."""
     lib.twell_profile_begin()
     for _ in range(prof_steps):
         flush_buf.fill_(1)
-        step()
-    torch.cuda.synchronize(dev)
+        b.step()
+    torch.cuda.synchronize(b.dev)
     cap = 64 * prof_steps
     ids = (ctypes.c_int * cap)()
     ms = (ctypes.c_float * cap)()
@@ -254,71 +253,187 @@ def run_ours(args, rank, world, local_rank):
     per = {}
     for i in range(min(cnt.value, cap)):
         per.setdefault(lib.twell_kernel_name(ids[i]).decode(), []).append(ms[i])
-    # kernel launches of the library per step (a profiled step may hold several)
     launches_per_step = sum(nl[i] for i in range(min(cnt.value, cap))) / prof_steps
     kern = {k: {"launches_per_step": len(v) / prof_steps, "avg_ms": float(np.mean(v)),
                 "ms_per_step": float(np.sum(v)) / prof_steps} for k, v in per.items()}
+    return kern, launches_per_step
 
-    nnz = bufs.nnz.cpu().numpy().astype(np.int64)
-    # rows the dispatcher sent to the dense path (control block: n_rows), of
-    # a lone forward and of the backward that follows it
-    tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, int(train),
-                         bufs.t, y, ws, nws, sh)
-    torch.cuda.synchronize(dev)
-    rows_f = int(ws[:4].view(torch.int32).item())
-    rows_b = 0
-    dh_gemm = False
-    if train:
-        tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], w.lam, D, dx,
-                              dWg, dbg, dWu, dWd, ws, nws, sh)
-        torch.cuda.synchronize(dev)
-        rows_b = int(ws[:4].view(torch.int32).item())
-        dh_gemm = bool(ws[24:28].view(torch.int32).item())  # control block: dh_gemm
-    rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b, dh_gemm)
-    dominant = max((k for k in kern if k in rl), key=lambda k: kern[k]["ms_per_step"], default=None)
-    roof = None
-    if dominant:
-        r = rl[dominant]
-        roof = {"kernel": dominant, "bound": r["bound"], "achieved": round(r["achieved"], 2),
+
+def dominant_roofline(kern, rl, workload, train, gceil):
+    """The contract's roofline object for the kernel with the largest time
+    per step.  A tensor-core kernel is read against the measured bf16 peak.
+    A gather kernel whose rows are served from L2 (the weight rows it
+    re-reads fit in L2; ncu DRAM bytes are a small fraction of its
+    algorithmic bytes) is read against the rate this GPU reaches on the same
+    random-row gather pattern, measured in the same run (bound "l2"); its
+    figures against the HBM copy peak are kept beside it, both on algorithmic
+    bytes and on the ncu DRAM bytes."""
+    dominant = max((k for k in kern if k in rl), key=lambda k: kern[k]["ms_per_step"],
+                   default=None)
+    if not dominant:
+        return None
+    r = rl[dominant]
+    traffic = traffic_for(dominant, workload, train)
+    if r["bound"] != "hbm" or not gceil:
+        return {"kernel": dominant, "bound": r["bound"], "achieved": round(r["achieved"], 2),
                 "peak": r["peak"], "unit": r["unit"], "frac": round(r["frac"], 4),
-                "traffic": traffic_for(dominant, args.workload, train),
-                "peak_source": r["peak_source"]}
+                "traffic": traffic, "peak_source": r["peak_source"]}
+    sec = kern[dominant]["avg_ms"] / 1e3
+    hbm = {"peak_gbs": r["peak"], "peak_source": r["peak_source"],
+           "frac_algorithmic_bytes": round(r["frac"], 4),
+           "frac_dram_bytes": (round(traffic / sec / 1e9 / r["peak"], 4) if traffic else None)}
+    return {"kernel": dominant, "bound": "l2", "achieved": round(r["achieved"], 2),
+            "peak": round(gceil, 1), "unit": "GB/s", "frac": round(r["achieved"] / gceil, 4),
+            "traffic": traffic,
+            "peak_source": "measured in this run: random-row gather probe on the same matrix "
+                           "and pair count (the memory level that serves these gathers)",
+            "hbm": hbm}
 
-    # the memory system's rate for the same gather pattern (probe kernel)
-    gceil = gather_ceiling(torch, lib, dev, d["Wu"] if w.gated else d["Wd"], w,
-                           rl["_counts"]["pairs_all"], timed, sh)
-    if gceil:
-        for k, r in rl.items():
-            if r.get("bound") == "hbm":
-                r["frac_of_l2_gather"] = r["achieved"] / gceil
-        if roof and roof["bound"] == "hbm":
-            roof["l2_gather_gbs"] = round(gceil, 1)
-            roof["frac_of_l2_gather"] = round(roof["achieved"] / gceil, 4)
 
-    dense = None if args.no_dense else dense_reference(torch, d, w, train, timed, args)
+def measure(torch, lib, b, timed, per_step, flush_buf, args, steps, w_key, full=True):
+    """Time one workload: the sparse step (cold L2), per-kernel times and
+    rooflines, the gather ceiling, and the two dense cuBLAS arms."""
+    w, train = b.w, b.train
+    for _ in range(3):
+        b.step()
+    code, n_ovf = b.status()
+    if code != 0:
+        raise SystemExit(f"device status {code} after warm-up ({w.name})")
+    ms = timed(b.step, steps) / steps
+    med = sorted(per_step)[len(per_step) // 2]
+    code, n_ovf = b.status()
+    if code != 0:
+        raise SystemExit(f"device status {code} after the timed steps ({w.name})")
+    kern, launches = kernel_profile(torch, lib, b, flush_buf, 5 if not full else max(5, min(50, steps)))
+    nnz = b.bufs.nnz.cpu().numpy().astype(np.int64)
+    rows_f, rows_b, dh_gemm = b.dispatch()
+    rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b, dh_gemm)
+    gceil = None
+    if any(r.get("bound") == "hbm" for k, r in rl.items() if not k.startswith("_")):
+        gceil = gather_ceiling(torch, b.dev, b.d["Wu"] if w.gated else b.d["Wd"], w,
+                               rl["_counts"]["pairs_all"], timed, b.sh)
+        if gceil:
+            for k, r in rl.items():
+                if r.get("bound") == "hbm":
+                    r["frac_of_l2_gather"] = r["achieved"] / gceil
+    dense = None if args.no_dense else dense_arms(torch, b.d, w, train, timed, args, steps)
+    row_ovf = (nnz > w.K).any(axis=0)
+    rec = {"ms_per_step": round(ms, 5), "median_ms": round(med, 5),
+           "tokens_per_s": round(w.T / (ms / 1e3), 1),
+           "roofline": dominant_roofline(kern, rl, w_key, train, gceil),
+           "path": {"forward_all_dense": bool(rows_f >= w.T), "forward_dense_rows": rows_f,
+                    "backward_dense_rows": rows_b if train else None,
+                    "backward_dh_gemm": dh_gemm if train else None},
+           "sparsity": {"active_frac": float(nnz.sum() / (w.T * w.F)), "n_ovf": int(row_ovf.sum())},
+           "l2_gather_gbs": round(gceil, 1) if gceil else None}
+    if dense:
+        rec["dense_cublas"] = dense["eager"]
+        rec["dense_gemm_only"] = dense["gemm_only"]
+        rec["speedup_vs_dense"] = round(dense["eager"]["ms_per_step"] / ms, 4)
+        rec["speedup_vs_dense_gemm_only"] = round(dense["gemm_only"]["ms_per_step"] / ms, 4)
+    return rec, kern, rl, launches, nnz
+
+
+SWEEP = ("c2", "c3", "c4:-1.28:8", "c4:-1.64:8", "c4:-2.33:8", "c4:-2.58:8", "c1")
+
+
+def sweep(torch, tw, lib, dev, args, timed, per_step, flush_buf):
+    """Compact records of the inference forward of the other workloads (the
+    pages' shapes), each with its own dominant-kernel roofline and the two
+    dense cuBLAS arms on the same inputs."""
+    out = {}
+    for key in SWEEP:
+        w = workload_of(key, False)
+        b = Bench(torch, tw, w, False, dev, args)
+        rec, _, _, _, _ = measure(torch, lib, b, timed, per_step, flush_buf, args, 30, key,
+                                  full=False)
+        rec = {"workload": describe(w, False), "dtype": w.dtype, **rec}
+        out[f"{key}:fwd"] = rec
+        del b
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import activation_sparse_transformer_gate_gb300 as tw
+    from activation_sparse_transformer_gate_gb300 import _build
+
+    if rank == 0:
+        _build.build(variants=("", "hooks"))
+    if world > 1:
+        torch.distributed.barrier()
+    lib = tw.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    torch.backends.cuda.matmul.allow_tf32 = False  # the fp32 dense arm stays fp32
+    train = args.mode == "train"
+    w = workload_of(args.workload, train)
+    b = Bench(torch, tw, w, train, dev, args)
+    T = w.T
+    stream = b.stream
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
+    timed, per_step = make_timer(torch, dev, stream, flush_buf)
+
+    for _ in range(max(args.warmup, 3)):
+        b.step()
+    code, n_ovf = b.status()
+    if code != 0:
+        raise SystemExit(f"device status {code} after warm-up")
+    sampler = None if (args.no_clocks or rank != 0) else ClockSampler(local_rank)
+    if sampler:
+        time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    total_ms = timed(b.step, args.steps)
+    step_ms = sorted(per_step)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(torch, total_ms, world, dev)
+    clocks = sampler.stop() if sampler else None
+    code, n_ovf = b.status()
+    if code != 0:
+        raise SystemExit(f"device status {code} after the timed region")
+    ms_step = total_ms / args.steps
+    value = T * world / (ms_step / 1e3)
+    if rank != 0:
+        return None
+    n_warm = max(10, min(args.steps, 100))
+    warm_ms = timed(b.step, n_warm, flush=False) / n_warm
+
+    rec, kern, rl, launches_per_step, nnz = measure(
+        torch, lib, b, timed, per_step, flush_buf, args, max(10, min(args.steps, 200)),
+        args.workload, full=True)
+    d, bufs, ws, nws, y, sh = b.d, b.bufs, b.ws, b.nws, b.y, b.sh
     formats = (format_comparison(torch, lib, d, w, bufs, ws, nws, y, sh, timed, args)
                if (args.compare_formats and not train and w.gated) else None)
-    e2e = None if args.no_e2e else end_to_end(torch, d, step, y, dx, w, train, timed, args,
+    e2e = None if args.no_e2e else end_to_end(torch, d, b.step, y, b.dx, w, train, timed, args,
                                               stream, flush_buf)
     mem = energy = None
     if not args.no_energy:
-        mem, energy = memory_and_energy(torch, dev, local_rank, d, w, train, step, bufs, nws,
+        mem, energy = memory_and_energy(torch, dev, local_rank, d, w, train, b.step, bufs, nws,
                                         int(row_ovf_count(bufs, w)))
-    cpu = None if (args.no_cpu or world > 1) else cpu_baseline(a, w, train, args.cpu_seconds)
+    cpu = None if (args.no_cpu or world > 1) else cpu_baseline(b.a, w, train, args.cpu_seconds)
+    del b, d, bufs, ws, y
+    torch.cuda.empty_cache()
+    sub = None if (args.no_sweep or world > 1) else sweep(torch, tw, lib, dev, args, timed,
+                                                          per_step, flush_buf)
 
-    row_ovf = (nnz > w.K).any(axis=0)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
         "step_ms": {"median": round(step_ms[len(step_ms) // 2], 5), "min": round(step_ms[0], 5),
                     "warm_l2_mean": round(warm_ms, 5)},
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded numpy PCG64; shapes and sparsity of the pages' FFN setting)",
-        "config": {"workload": describe(w, train), "T": T, "d_model": D, "d_ff": F, "tile": w.C,
-                   "K": w.K, "step": "fwd+bwd" if train else "fwd",
+        "config": {"workload": describe(w, train), "T": T, "d_model": w.D, "d_ff": w.F,
+                   "tile": w.C, "K": w.K, "step": "fwd+bwd" if train else "fwd",
                    "l2": f"flushed before every timed step ({flush_buf.numel() >> 20} MiB write)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roof,
+        "roofline": rec["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(round(launches_per_step * args.steps)),
@@ -326,15 +441,19 @@ def run_ours(args, rank, world, local_rank):
         "kernels": {k: {kk: round(vv, 5) for kk, vv in v.items()} for k, v in kern.items()},
         "kernel_roofline": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                                 for kk, vv in v.items()} for k, v in rl.items()},
-        "sparsity": {"active_frac": float(nnz.sum() / (T * F)), "n_ovf": int(row_ovf.sum())},
+        "sparsity": rec["sparsity"],
+        "path": rec["path"],
+        "l2_gather_gbs": rec["l2_gather_gbs"],
         "memory": mem,
         "energy": energy,
     }
     if formats:
         line["format_comparison"] = formats
-    if dense:
-        line["dense_cublas"] = dense
-        line["speedup_vs_dense"] = round(dense["ms_per_step"] / ms_step, 4)
+    for k in ("dense_cublas", "dense_gemm_only", "speedup_vs_dense", "speedup_vs_dense_gemm_only"):
+        if k in rec:
+            line[k] = rec[k]
+    if sub:
+        line["workloads"] = sub
     return line
 
 
@@ -349,7 +468,22 @@ def load_peaks():
             "source": "of fallback (no MEASURED_PEAKS.json)"}
 
 
-def gather_ceiling(torch, lib, dev, W, w, pairs, timed, sh):
+def tw_hooks():
+    """The test-hooks build of the library (the gather probe lives there, not
+    in libtwell.so)."""
+    import activation_sparse_transformer_gate_gb300 as tw
+    from activation_sparse_transformer_gate_gb300 import _build
+    _build.build(variants=("hooks",))
+    return tw.load(_build.lib_path("hooks"))
+
+
+def fp32_alu_tflops() -> float:
+    """fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flop x the
+    2.07 GHz maximum SM clock."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def gather_ceiling(torch, dev, W, w, pairs, timed, sh):
     """GB/s at which the GPU gathers `pairs` rows of W (F x d_model, bf16) in
     a uniform random order with plain 16-byte loads: the measured ceiling
     for the sparse kernels' row gathers (L2-served when W fits in L2), timed
@@ -360,10 +494,11 @@ def gather_ceiling(torch, lib, dev, W, w, pairs, timed, sh):
     rows = torch.from_numpy(rng.integers(0, w.F, size=pairs).astype(np.int32)).to(dev)
     blocks = 6 * torch.cuda.get_device_properties(dev).multi_processor_count
     out = torch.empty((blocks * 8,), dtype=torch.int32, device=dev)
-    f = lib.twell_test_gather_probe
+    hooks = tw_hooks()
+    f = hooks.twell_test_gather_probe
     f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                   ctypes.c_void_p, ctypes.c_void_p]
-    row_bytes = w.D * 2
+    row_bytes = w.D * (2 if w.dtype == "bf16" else 4)
 
     def run():
         rc = f(W.data_ptr(), row_bytes, rows.data_ptr(), pairs, blocks, out.data_ptr(), sh)
@@ -386,11 +521,13 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
     notes for the per-unit figures."""
     peaks = load_peaks()
     D, F, T, K = w.D, w.F, w.T, w.K
+    es = 2 if w.dtype == "bf16" else 4
     row_ovf = (nnz > K).any(axis=0)
     sparse_rows = int((~row_ovf).sum())
     pairs = int(np.minimum(nnz, K)[:, ~row_ovf].sum())          # pairs of TwELL rows
     pairs_all = int(nnz.sum())                                    # incl. overflow rows
-    twell = (F // w.C) * T * (3 * K + 1)
+    twell = (F // w.C) * T * ((1 + es) * K + 1)
+    nw = 2 if w.gated else 1  # weight rows gathered per pair in the forward
 
     def gathered(rows):
         """Pairs and tokens the gather kernels take when `rows` rows are on
@@ -403,23 +540,25 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
 
     pf, tf = gathered(rows_f)
     pb, tb = gathered(rows_b)
+    ng = 3 if w.gated else 2  # dW problems (dWg, [dWu,] dWd)
     wrk = {
-        # per pair: W_up + W_down rows; per token: x row in, y row out; TwELL read
-        "twell_updown_fused": ("hbm", (pf * 2 * D * 2 + tf * D * 2 * 2 + twell) if tf else 0),
+        # per pair: W_up (gated) + W_down rows; per token: x row in (gated), y
+        # row out; TwELL read
+        "twell_updown_fused": ("hbm", (pf * nw * D * es + tf * D * es * nw + twell) if tf else 0),
         # dh SDDMM: per pair a W_down row, u in and dz/du/h out; per token the dy row
-        "bwd_slots_sddmm": ("hbm", pb * (D * 2 + 14) + tb * D * 2),
-        # dx SpMM: per pair W_gate + W_up rows and dz/du in; per token the dx row out
-        "bwd_dx_spmm": ("hbm", pb * (2 * D * 2 + 8) + tb * D * 2),
+        "bwd_slots_sddmm": ("hbm", pb * (D * es + es + 12) + tb * D * es),
+        # dx SpMM: per pair W_gate (+ W_up) rows and dz/du in; per token the dx row out
+        "bwd_dx_spmm": ("hbm", pb * (nw * D * es + 8) + tb * D * es),
         # per pair: x + dy rows and its 16-byte list record {token, dz, du, h};
-        # 3 fp32 dW rows and dbg out
-        "bwd_dw_gather": ("hbm", pb * (2 * D * 2 + 16) + (3 * F * D * 4 + F * 4 if tb else 0)),
-        "gate_gemm_relu_twell": ("tensor", 2.0 * T * D * F),
+        # the fp32 dW rows and dbg out
+        "bwd_dw_gather": ("hbm", pb * (2 * D * es + 16) + (ng * F * D * 4 + F * 4 if tb else 0)),
+        # bf16: tcgen05 tensor cores; fp32: CUDA-core FFMA (no TF32)
+        "gate_gemm_relu_twell": ("tensor" if es == 2 else "alu", 2.0 * T * D * F),
     }
     if dh_gemm:  # dh from the full product dy W_down^T, read at the slots
         del wrk["bwd_slots_sddmm"]
         wrk["bwd_dh_gemm_sampled"] = ("tensor", 2.0 * T * D * F)
     wrk = {k: v for k, v in wrk.items() if v[1] > 0}
-    ng = 3 if w.gated else 2  # dW problems (dWg, [dWu,] dWd)
     for k, rows, mult in (("dense_rows_gate_up", rows_f, 1), ("dense_rows_down", rows_f, 1),
                           ("bwd_dense_dh_gemm", rows_b, 1),
                           ("bwd_dense_dx_gemm", rows_b, 4 if w.gated else 2),
@@ -431,12 +570,17 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
         if k not in kern:
             continue
         sec = kern[k]["avg_ms"] / 1e3
+        src = peaks["source"]
         if bound == "hbm":
             ach, peak, unit = work / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+        elif bound == "alu":  # fp32 FFMA on the CUDA cores
+            ach, peak, unit = work / sec / 1e12, fp32_alu_tflops(), "TFLOP/s"
+            src = ("derived: 152 SMs x 128 fp32 lanes x 2 flop per FFMA x 2.07 GHz maximum "
+                   "SM clock")
         else:  # timed inside back-to-back steps: the sustained (power-capped) peak
             ach, peak, unit = work / sec / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
         out[k] = dict(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak,
-                      algorithmic=work, peak_source=peaks["source"])
+                      algorithmic=work, peak_source=src)
     out.setdefault("_counts", {"bound": "-", "pairs_twell_rows": pairs, "pairs_all": pairs_all,
                                "sparse_rows": sparse_rows, "dense_path_rows_fwd": rows_f,
                                "dense_path_rows_bwd": rows_b})
@@ -477,14 +621,22 @@ def dense_step_fn(torch, d, w, train):
     fp32 accumulation): forward, and for training the backward with the L1
     term."""
     x, Wg, Wu, Wd, rb, dy = d["x"], d["Wg"], d["Wu"], d["Wd"], d["rb"], d["dy"]
-    bgb = d["bg"].to(torch.bfloat16)
+    bgb = d["bg"].to(x.dtype)
     lam = w.lam
 
     def step():
         z = torch.addmm(bgb, x, Wg.t())
         if rb is not None:
-            z = z + rb.to(torch.bfloat16)[:, None]
+            z = z + rb.to(x.dtype)[:, None]
         g = torch.relu(z)
+        if Wu is None:
+            h = g
+            y = h @ Wd
+            if not train:
+                return y
+            dh = dy @ Wd.t() + lam * torch.sign(h)
+            dz = torch.where(z > 0, dh, torch.zeros_like(dh))
+            return (dz @ Wg, dz.t() @ x, h.t() @ dy, dz.float().sum(0))
         u = x @ Wu.t()
         h = g * u
         y = h @ Wd
@@ -604,17 +756,60 @@ def memory_and_energy(torch, dev, index, d, w, train, ours_step, bufs, nws, n_ov
     return mem, energy
 
 
-def dense_reference(torch, d, w, train, timed, args):
-    """The same FFN with cuBLAS GEMMs through torch (bf16, fp32 accumulate)."""
-    step = dense_step_fn(torch, d, w, train)
+def dense_gemm_only_fn(torch, d, w, train):
+    """The dense FFN's GEMMs alone, with the same shapes and operand types as
+    the eager arm and preallocated outputs, no element-wise work: 3 GEMMs
+    forward (gate, up, down; 2 for the plain FFN) and 6 more for the
+    backward (dh, the two dx products, dW_gate, dW_up, dW_down).  A floor
+    for any dense implementation that runs these products on cuBLAS."""
+    x, Wg, Wu, Wd, dy = d["x"], d["Wg"], d["Wu"], d["Wd"], d["dy"]
+    T, F, D = w.T, w.F, w.D
+    z = torch.empty((T, F), dtype=x.dtype, device=x.device)
+    u = torch.empty_like(z) if Wu is not None else None
+    y = torch.empty((T, D), dtype=x.dtype, device=x.device)
+    if train:
+        dh = torch.empty_like(z)
+        dx = torch.empty_like(y)
+        dWg = torch.empty((F, D), dtype=x.dtype, device=x.device)
+        dWu = torch.empty_like(dWg) if Wu is not None else None
+        dWd = torch.empty_like(dWg)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    steps = max(10, min(args.steps, 200))
-    ms = timed(step, steps) / steps
-    return {"ms_per_step": round(ms, 5), "tokens_per_s": round(w.T / (ms / 1e3), 1),
-            "what": "torch bf16 matmul (cuBLAS) dense FFN" + (" fwd+bwd" if train else " fwd"),
-            "steps": steps}
+    def step():
+        torch.matmul(x, Wg.t(), out=z)
+        if u is not None:
+            torch.matmul(x, Wu.t(), out=u)
+        torch.matmul(z, Wd, out=y)            # (z stands in for h: same shape, same cost)
+        if not train:
+            return
+        torch.matmul(dy, Wd.t(), out=dh)
+        torch.matmul(dh, Wg, out=dx)
+        if u is not None:
+            dx.addmm_(u, Wu)                  # (u stands in for du)
+        torch.matmul(dh.t(), x, out=dWg)
+        if dWu is not None:
+            torch.matmul(z.t(), x, out=dWu)
+        torch.matmul(z.t(), dy, out=dWd)
+
+    return step
+
+
+def dense_arms(torch, d, w, train, timed, args, steps):
+    """The same FFN on cuBLAS through torch (bf16 operands with fp32
+    accumulation; fp32 with TF32 off for the fp32 workload), timed like the
+    sparse step: "eager" with torch's element-wise ops between the GEMMs,
+    "gemm_only" the GEMMs alone."""
+    out = {}
+    for name, fn in (("eager", dense_step_fn(torch, d, w, train)),
+                     ("gemm_only", dense_gemm_only_fn(torch, d, w, train))):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        ms = timed(fn, steps) / steps
+        what = ("torch %s matmul (cuBLAS) dense FFN%s%s" %
+                (w.dtype, " fwd+bwd" if train else " fwd",
+                 ": GEMMs only, no element-wise work" if name == "gemm_only" else ""))
+        out[name] = {"ms_per_step": round(ms, 5), "tokens_per_s": round(w.T / (ms / 1e3), 1),
+                     "what": what, "steps": steps}
+    return out
 
 
 def format_comparison(torch, lib, d, w, bufs, ws, nws, y, sh, timed, args):
@@ -753,7 +948,11 @@ def end_to_end(torch, d, step, y, dx, w, train, timed, args, stream, flush_buf):
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
             "ms_per_step": round(ms, 5), "steps": steps,
             "copies": "double-buffered on a second stream, overlapping the neighbouring steps",
-            "serial_ms_per_step": round(ms_serial, 5)}
+            "serial_ms_per_step": round(ms_serial, 5),
+            "serial_tokens_per_s": round(w.T / (ms_serial / 1e3), 1),
+            "outputs_copied": "y" + (" and dx; the fp32 weight gradients (dW_gate, dW_up, "
+                                     "dW_down, dbg) stay on the device for an optimizer step "
+                                     "there" if train else "")}
 
 
 def oracle_sample(a, w, train, S, Fs):

@@ -192,8 +192,9 @@ twell_status twell_get_status(const twell_t *tw, void *stream, int32_t *n_ovf);
  * until the process exits), so it allocates nothing.
  *   - T > TWELL_STATIC_SPLIT_MAX_T returns TWELL_ERR_STATIC_LIMIT before any
  *     launch.
- *   - The first call on each device looks the array's address up (with that
- *     device current); make that first call before any stream capture.
+ *   - The first call in each CUDA context (each device's primary context, and
+ *     again after a device reset) looks the array's address up with that
+ *     context current; make that first call before any stream capture.
  *   - All calls share the array: calls that overlap on the GPU race.  The
  *     array keeps the last call's contents; each call clears what it needs. */
 #define TWELL_STATIC_SPLIT_MAX_T 262144

@@ -1,4 +1,5 @@
-"""The tcgen05 GEMM engine through its test hook, on exact integer inputs
+"""The tcgen05 GEMM engine through its test hook (the test-hooks build of the
+library), on exact integer inputs
 (every fp32 accumulation order gives the same value), then on Gaussian
 inputs.  Runs first among the GPU tests: the TwELL kernels sit on this engine."""
 import ctypes
@@ -16,8 +17,8 @@ pytestmark = pytest.mark.gpu
 def hook():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
-    tw._build.build()
-    lib = tw.load()
+    tw._build.build(variants=("hooks",))
+    lib = tw.load(tw._build.lib_path("hooks"))
     f = lib.twell_test_tc_gemm
     P = ctypes.c_void_p
     f.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]

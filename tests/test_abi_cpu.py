@@ -43,6 +43,19 @@ def test_library_exports_every_declared_symbol(lib):
     assert "sm_103a" in tw.twell_version()
 
 
+def test_test_hooks_stay_out_of_the_product_library(lib):
+    """The measurement hooks (GEMM engine test entry, gather probe) are built
+    into the test-hooks variant only."""
+    for n in ("twell_test_tc_gemm", "twell_test_gather_probe"):
+        assert not hasattr(lib, n), f"libtwell.so exports the test hook {n}"
+    _build.build(variants=("hooks",))
+    hooks = tw.load(_build.lib_path("hooks"))
+    for n in ("twell_test_tc_gemm", "twell_test_gather_probe"):
+        assert hasattr(hooks, n), n
+    for n in header_functions():
+        assert hasattr(hooks, n), n
+
+
 def test_workspace_size(lib):
     a = tw.twell_workspace_size(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 0)
     b = tw.twell_workspace_size(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1)

@@ -8,7 +8,7 @@ import torch
 import activation_sparse_transformer_gate_gb300 as tw
 import oracle
 import synth
-from twell_testlib import assert_close_rms, to_np64, torch_dev, z_allowance
+from twell_testlib import check_backward, ctl_fields, dh_gemm_of, run_train
 
 pytestmark = pytest.mark.gpu
 
@@ -19,80 +19,6 @@ def _lib():
         pytest.skip("needs a CUDA GPU")
     tw._build.build()
     tw.load()
-
-
-def shifted(t, elems):
-    """A copy of device tensor t whose data starts `elems` elements past an
-    allocation boundary (16-byte aligned but not 32-byte aligned for 8 bf16)."""
-    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
-    v = buf[elems:].view(t.shape)
-    v.copy_(t)
-    return v
-
-
-def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0, dh_density=-1.0):
-    """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
-    the density test of the dispatcher off, so that moderately dense test
-    workloads still run the gather kernels; dh_density < 0 keeps dh on the
-    gather SDDMM (> 0: on the tensor-core GEMM read at the slots above that
-    density; 0: the dispatcher's default); out (dict) receives the
-    workspace's control block after the forward ("ctl") and after the
-    backward ("ctl_bwd")."""
-    T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
-    dtype = tw.TWELL_BF16 if w.dtype == "bf16" else tw.TWELL_F32
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    d = {k: torch_dev(a[k]) for k in ("x", "Wg", "Wu", "Wd", "bg", "rb", "dy")}
-    if wd_shift:
-        d["Wd"] = shifted(d["Wd"], wd_shift)
-    bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density,
-                           dh_density=dh_density)
-    ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
-    y = torch.empty((T, D), dtype=tdt, device="cuda")
-    tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 1, bufs.t, y, ws, nws)
-    if out is not None:
-        out["ctl"] = ws[:32].cpu().numpy().copy()
-    dx = torch.full((T, D), float("nan"), dtype=tdt, device="cuda")
-    dWg = torch.full((F, D), float("nan"), dtype=torch.float32, device="cuda")
-    dWu = torch.full_like(dWg, float("nan")) if d["Wu"] is not None else None
-    dWd = torch.full_like(dWg, float("nan"))
-    dbg = torch.full((F,), float("nan"), dtype=torch.float32, device="cuda")
-    tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], lam, D, dx, dWg, dbg,
-                          dWu, dWd, ws, nws)
-    if out is not None:
-        out["ctl_bwd"] = ws[:32].cpu().numpy().copy()
-    code, n_ovf = tw.twell_get_status(bufs.t)
-    return dict(code=code, n_ovf=n_ovf, y=to_np64(y), dx=to_np64(dx), dWg=to_np64(dWg),
-                dbg=to_np64(dbg), dWu=None if dWu is None else to_np64(dWu), dWd=to_np64(dWd))
-
-
-def ctl_fields(c):
-    """(n_rows, dense, n_ovf, ovf_gemm) of a saved control block."""
-    return tuple(int(v) for v in c[:16].view(np.int32))
-
-
-def dh_gemm_of(c):
-    """The backward's choice of the tensor-core dh GEMM in a saved control block."""
-    return int(c[24:28].view(np.int32)[0])
-
-
-def check_backward(a, w, g, lam, tok_sel=None, neu_sel=None):
-    dt = w.dtype
-    b = oracle.ffn_backward(a["x"], a["Wg"], a["bg"], a["rb"], a["Wu"], a["Wd"], a["dy"], lam, dt,
-                            dt, tok_sel=tok_sel, neu_sel=neu_sel)
-    ts = slice(None) if tok_sel is None else np.asarray(tok_sel)
-    ns = slice(None) if neu_sel is None else np.asarray(neu_sel)
-    al = z_allowance(a, dt, rows=None if tok_sel is None else ts, lam=lam) if dt == "f32" else {}
-    assert_close_rms(g["dx"][ts], b["dx"], dt, "dx", extra=al.get("dx"))
-    for k in ("dWg", "dWd", "dbg") + (("dWu",) if a["Wu"] is not None else ()):
-        ex = al.get(k)
-        assert_close_rms(g[k][ns], b[k], dt, k, out_dtype="f32",
-                         extra=None if ex is None else ex[ns])
-    # neurons that are never active have exactly zero gradient rows
-    dead = np.all(b["dWd"] == 0, axis=1)
-    if dead.any():
-        assert np.all(g["dWg"][ns][dead] == 0) and np.all(g["dWd"][ns][dead] == 0)
-        assert np.all(g["dbg"][ns][dead] == 0)
-    return b
 
 
 def test_bf16_gated_small_with_overflow_rows():

@@ -3,7 +3,8 @@ memory (code inside an allocator or pool it does not own, hosts that forbid
 allocation on their hot path).  twell_hybrid_split_static keeps its scratch in
 a fixed device array inside the library; its overflow-row list must equal the
 one the workspace-free packing entry point (twell_pack_dense) produces for
-the same activations, on consecutive calls that share that array.
+the same activations, and the oracle's list from the same activations, on
+consecutive calls that share that array.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test."""
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 import activation_sparse_transformer_gate_gb300 as tw
+import oracle
 import synth
 from twell_testlib import torch_dev
 
@@ -62,6 +64,12 @@ def split_static(lib, a, cap=None):
     return b, st, n
 
 
+def oracle_list(H, C, K):
+    """Overflow rows of H by the oracle's TwELL pack (active iff > 0)."""
+    ref = oracle.twell_pack(synth.to_f64(H, "bf16"), C, K, "bf16")
+    return ref["ovf_rows"]
+
+
 def test_matches_existing_entry_on_two_calls_in_a_row(lib):
     T, F, C, K = 3000, 1024, 128, 8
     for seed, hot in ((1, 37), (2, 5)):          # different overflow sets, same array
@@ -71,6 +79,9 @@ def test_matches_existing_entry_on_two_calls_in_a_row(lib):
         assert code_a == 0 and code_b == 0
         assert n_a > 0 and n_b == n_a
         assert torch.equal(b.ovf_rows[:n_b], a.ovf_rows[:n_a])
+        want = oracle_list(H, C, K)
+        assert n_b == len(want)
+        assert np.array_equal(b.ovf_rows[:n_b].cpu().numpy(), want)
 
 
 def test_capacity_and_static_limit(lib):
@@ -81,6 +92,7 @@ def test_capacity_and_static_limit(lib):
     assert n_b == n_a > 5
     assert st == -4                                 # TWELL_ERR_CAPACITY on the device
     assert torch.equal(b.ovf_rows[:5], a.ovf_rows[:5])
+    assert np.array_equal(b.ovf_rows[:5].cpu().numpy(), oracle_list(H, C, K)[:5])
     # more tokens than the fixed scratch holds: rejected before any launch
     big = tw.twell_t(T=262145, F=512, C=64, K=4, dtype=tw.TWELL_BF16, idx=1 << 40, val=1 << 40,
                      nnz=1 << 40, ovf_rows=1 << 40, n_ovf=1 << 40, ovf_cap=1, g_fb=1 << 40,
