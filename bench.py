@@ -57,6 +57,10 @@ def parse_args():
     ap.add_argument("--no-energy", action="store_true",
                     help="skip the saved-memory and energy-per-token leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--shard", choices=["replicas", "tokens"], default="replicas",
+                    help="N > 1: one replica of the workload per rank (weak scaling), or the "
+                         "batch's tokens split over the ranks with the weight gradients summed "
+                         "by an all-reduce in every step (strong scaling)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the compact records of the other workloads' forward")
     ap.add_argument("--compare-formats", action="store_true",
@@ -369,7 +373,27 @@ def run_ours(args, rank, world, local_rank):
     torch.backends.cuda.matmul.allow_tf32 = False  # the fp32 dense arm stays fp32
     train = args.mode == "train"
     w = workload_of(args.workload, train)
-    b = Bench(torch, tw, w, train, dev, args)
+    sharded = args.shard == "tokens" and world > 1
+    if sharded:
+        # token-sharded step: this rank's contiguous range of the batch; the
+        # weight gradients are summed over the ranks inside the step
+        from activation_sparse_transformer_gate_gb300 import shard
+        a = synth.generate(w)
+        t0, t1 = shard.token_range(w.T, rank, world)
+        if t1 <= t0:
+            raise SystemExit(f"rank {rank} has no tokens: T={w.T} over {world} ranks")
+        a = {k: (v[t0:t1] if k in ("x", "dy", "rb") and v is not None else v) for k, v in a.items()}
+        b = Bench(torch, tw, synth.scaled(w, T=t1 - t0), train, dev, args, a=a)
+        local_step = b.step
+
+        def sharded_step():
+            local_step()
+            if train:
+                shard.allreduce_weight_grads([b.dWg, b.dWu, b.dWd, b.dbg])
+
+        b.step = sharded_step
+    else:
+        b = Bench(torch, tw, w, train, dev, args)
     T = w.T
     stream = b.stream
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -398,9 +422,11 @@ def run_ours(args, rank, world, local_rank):
     if code != 0:
         raise SystemExit(f"device status {code} after the timed region")
     ms_step = total_ms / args.steps
-    value = T * world / (ms_step / 1e3)
+    value = (T if sharded else T * world) / (ms_step / 1e3)
     if rank != 0:
         return None
+    if sharded:
+        b.step = local_step  # the measurements below are of this rank's own work
     n_warm = max(10, min(args.steps, 100))
     warm_ms = timed(b.step, n_warm, flush=False) / n_warm
 
@@ -427,12 +453,14 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
         "step_ms": {"median": round(step_ms[len(step_ms) // 2], 5), "min": round(step_ms[0], 5),
                     "warm_l2_mean": round(warm_ms, 5)},
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "higher_is_better": True, "scaling": "strong" if sharded else "weak",
+        "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded numpy PCG64; shapes and sparsity of the pages' FFN setting)",
         "config": {"workload": describe(w, train), "T": T, "d_model": w.D, "d_ff": w.F,
                    "tile": w.C, "K": w.K, "step": "fwd+bwd" if train else "fwd",
                    "l2": f"flushed before every timed step ({flush_buf.numel() >> 20} MiB write)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": (f"token-sharded x{world} (dW all-reduce in the step)"
+                                   if sharded else f"replicas x{world}")},
         "roofline": rec["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -581,6 +609,12 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
             ach, peak, unit = work / sec / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
         out[k] = dict(bound=bound, achieved=ach, peak=peak, unit=unit, frac=ach / peak,
                       algorithmic=work, peak_source=src)
+        if k == "bwd_dh_gemm_sampled":
+            # the same values as the SDDMM it replaces, rated on that SDDMM's
+            # bytes (the method's own work) beside the dense product's flops
+            sb = pb * (D * es + es + 12) + tb * D * es
+            out[k]["sddmm_bytes"] = sb
+            out[k]["sddmm_equivalent_gbs"] = sb / sec / 1e9
     out.setdefault("_counts", {"bound": "-", "pairs_twell_rows": pairs, "pairs_all": pairs_all,
                                "sparse_rows": sparse_rows, "dense_path_rows_fwd": rows_f,
                                "dense_path_rows_bwd": rows_b})

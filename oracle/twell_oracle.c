@@ -332,8 +332,11 @@ void oracle_ffn_rowell(int T, int D, int E, int dt, const void *x, const void *W
  *   dx[t]  = sum_n dz Wg[n] + du Wu[n]
  *   dWg[n] = sum_t dz x[t],  dbg[n] = sum_t dz,  dWu[n] = sum_t du x[t],
  *   dWd[n] = sum_t h dy[t]
- * g is the stored (rounded) gate value; the rounding is treated as identity
- * for differentiation.  tok_sel / neu_sel (NULL = all) select which dx rows
+ * g and u are the values the training forward saves for the backward,
+ * rounded to the storage type q (the backward consumes the saved activations,
+ * section 2.A hybrid format / section 4 training memory); the rounding is
+ * treated as identity for differentiation.  tok_sel / neu_sel (NULL = all)
+ * select which dx rows
  * and which dW rows are produced; outputs are packed in selection order:
  * dx [n_tok][D], dWg/dWu/dWd [n_neu][D], dbg [n_neu].  dWu may be NULL for
  * the plain FFN.  Every selected output is computed from the definition. */
@@ -354,7 +357,8 @@ void oracle_ffn_backward(int T, int D, int F, int dt, int q, const void *x, cons
       if (rb) zz += (double)rb[t];
       if (!is_active(zz, q)) continue; /* dz = du = 0 exactly */
       double g = quant(zz, q);
-      double u = Wu ? dot(x, dt, (size_t)t * D, Wu, dt, (size_t)n * D, D) : 1.0;
+      /* u as the forward saved it: rounded to the storage type, like g */
+      double u = Wu ? quant(dot(x, dt, (size_t)t * D, Wu, dt, (size_t)n * D, D), q) : 1.0;
       double h = Wu ? g * u : g;
       double dh = dot(dy, dt, (size_t)t * D, Wd, dt, (size_t)n * D, D) + lambda * sgn(h);
       double dz = Wu ? dh * u : dh;
@@ -381,7 +385,7 @@ void oracle_ffn_backward(int T, int D, int F, int dt, int q, const void *x, cons
       if (rb) zz += (double)rb[t];
       if (!is_active(zz, q)) continue;
       double g = quant(zz, q);
-      double u = Wu ? dot(x, dt, (size_t)t * D, Wu, dt, (size_t)n * D, D) : 1.0;
+      double u = Wu ? quant(dot(x, dt, (size_t)t * D, Wu, dt, (size_t)n * D, D), q) : 1.0;
       double h = Wu ? g * u : g;
       double dh = dot(dy, dt, (size_t)t * D, Wd, dt, (size_t)n * D, D) + lambda * sgn(h);
       double dz = Wu ? dh * u : dh;

@@ -38,3 +38,45 @@ def test_dh_gemm_is_rated_on_flops_of_the_whole_product():
     assert r["algorithmic"] == 2.0 * w.T * w.D * w.F
     assert abs(r["achieved"] - 2.0 * w.T * w.D * w.F / 0.05e-3 / 1e12) < 1e-9
     assert "bwd_slots_sddmm" not in rl  # launched but idle: not rated
+
+
+def test_dh_gemm_also_rated_on_the_sddmm_bytes():
+    w, nnz = small_case()
+    rl = bench.kernel_rooflines(kern_times(["bwd_dh_gemm_sampled"], 0.05), w, nnz, True, 0, 0,
+                                dh_gemm=True)
+    r = rl["bwd_dh_gemm_sampled"]
+    a = int(nnz.sum())
+    assert r["sddmm_bytes"] == a * (w.D * 2 + 14) + w.T * w.D * 2
+    assert abs(r["sddmm_equivalent_gbs"] - r["sddmm_bytes"] / 0.05e-3 / 1e9) < 1e-6
+
+
+def test_gather_dominated_step_is_read_against_the_l2_gather_rate():
+    """An L2-served gather kernel: bound "l2" against the measured gather
+    rate (frac <= 1 when below it), with its HBM figures beside it."""
+    w, nnz = small_case()
+    kern = kern_times(["bwd_dw_gather", "gate_gemm_relu_twell"], 0.01)
+    kern["bwd_dw_gather"]["ms_per_step"] = 0.2
+    rl = bench.kernel_rooflines(kern, w, nnz, True, 0, 0)
+    alg = rl["bwd_dw_gather"]["achieved"]
+    r = bench.dominant_roofline(kern, rl, "c2", True, gceil=2 * alg)
+    assert r["kernel"] == "bwd_dw_gather" and r["bound"] == "l2"
+    assert abs(r["frac"] - 0.5) < 1e-3 and r["unit"] == "GB/s"
+    assert r["hbm"]["frac_algorithmic_bytes"] == round(rl["bwd_dw_gather"]["frac"], 4)
+    # without a measured gather rate the HBM reading is kept
+    r2 = bench.dominant_roofline(kern, rl, "c2", True, gceil=None)
+    assert r2["bound"] == "hbm"
+
+
+def test_fp32_gate_gemm_is_rated_on_the_alu_peak():
+    w = synth.scaled(synth.config1(), train=False)
+    nnz = np.zeros((w.F // w.C, w.T), dtype=np.int64)
+    nnz[0, :] = 1
+    rl = bench.kernel_rooflines(kern_times(["gate_gemm_relu_twell", "twell_updown_fused"]), w,
+                                nnz, False)
+    assert rl["gate_gemm_relu_twell"]["bound"] == "alu"
+    assert abs(rl["gate_gemm_relu_twell"]["peak"] - bench.fp32_alu_tflops()) < 1e-9
+    # fp32 rows: 4-byte elements, one gathered weight row per pair (plain FFN)
+    pairs = int(nnz.sum())
+    twell = (w.F // w.C) * w.T * (5 * w.K + 1)
+    want = pairs * w.D * 4 + w.T * w.D * 4 + twell
+    assert rl["twell_updown_fused"]["algorithmic"] == want

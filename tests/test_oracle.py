@@ -207,7 +207,7 @@ def _bwd_numpy(a, dt, q, lam):
     act = active_np(z, q)
     g = np.where(act, q_np(z, q), 0.0)
     if Wu is not None:
-        u = x @ Wu.T
+        u = q_np(x @ Wu.T, q)  # u as saved for the backward, in the storage type
         h = g * u
     else:
         u = np.ones_like(g)
@@ -297,7 +297,7 @@ def test_backward_closed_form_zero_down_weight():
     b = oracle.ffn_backward(a["x"], a["Wg"], a["bg"], None, a["Wu"], a["Wd"], a["dy"], lam, "f32", "f32")
     x, Wg, Wu = (f64(a[k], "f32") for k in ("x", "Wg", "Wu"))
     z = x @ Wg.T + a["bg"].astype(np.float64)
-    u = x @ Wu.T
+    u = (x @ Wu.T).astype(np.float32).astype(np.float64)  # u as saved (fp32 storage)
     want = lam * np.where(z.astype(np.float32) > 0, np.abs(u), 0.0).sum(0)
     np.testing.assert_allclose(b["dbg"], want, rtol=1e-12, atol=1e-14)
     assert np.abs(want).max() > 0

@@ -1,0 +1,62 @@
+"""Why the tensor-core backward feeds dz, du and h to its dx and weight-
+gradient GEMMs as bf16 hi + lo parts (CPU, numpy, no library code).
+
+The weight gradients are sums of a few products per element (dW_down[n] =
+sum over ~T*p active tokens of h * dy_t).  The bound the outputs must meet is
+max |d| <= 2e-2 * rms over the whole tensor; its max-norm meets the heavy
+tail of the row magnitudes (a neuron with a large h dominates its row, and
+the largest of d_model normal values is ~4.5 rms).  One bf16 rounding of the
+fp32 operand (relative error up to 2^-9) then costs up to ~2^-9 * 4.5 * the
+tail factor, which exceeds 2e-2 at these shapes; with hi + lo parts the
+operand carries ~2^-17 relative error and the bound holds with a wide
+margin.  This pins the measured reason for the extra GEMM work of the dense
+rows' backward.
+"""
+import numpy as np
+
+import synth
+
+
+def bf(a):
+    return synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(a.astype(np.float32))).astype(np.float64)
+
+
+def hi_lo(a):
+    a32 = a.astype(np.float32).astype(np.float64)
+    hi = bf(a32)
+    return hi + bf(a32 - hi)
+
+
+def grads(T, D, F, bias, lam, seed, round_op):
+    rng = np.random.default_rng(seed)
+    x = bf(rng.standard_normal((T, D)))
+    Wg = bf(rng.standard_normal((F, D)) / np.sqrt(D))
+    Wu = bf(rng.standard_normal((F, D)) / np.sqrt(D))
+    Wd = bf(rng.standard_normal((F, D)) / np.sqrt(F))
+    dy = bf(rng.standard_normal((T, D)))
+    z = x @ Wg.T + bias
+    act = z.astype(np.float32) > 0
+    g = bf(np.where(act, z, 0.0))           # stored gate values (bf16)
+    u = bf(x @ Wu.T)                        # stored up values (bf16)
+    h = g * u
+    dh = dy @ Wd.T + lam * np.sign(h)
+    dz = np.where(act, dh * u, 0.0)
+    du = np.where(act, dh * g, 0.0)
+    q = round_op
+    return {"dx": q(dz) @ Wg + q(du) @ Wu, "dWg": q(dz).T @ x, "dWu": q(du).T @ x,
+            "dWd": q(h).T @ dy}
+
+
+def whole_error(got, ref):
+    return float(np.abs(got - ref).max() / np.sqrt(np.mean(ref ** 2)))
+
+
+def test_single_bf16_operands_break_the_bound_hi_lo_parts_keep_it():
+    T, D, F, bias, lam = 512, 1024, 4096, -2.33, 1e-4
+    exact = grads(T, D, F, bias, lam, 11, lambda v: v)
+    single = grads(T, D, F, bias, lam, 11, bf)
+    split = grads(T, D, F, bias, lam, 11, hi_lo)
+    worst_single = max(whole_error(single[k], exact[k]) for k in ("dWg", "dWu", "dWd"))
+    worst_split = max(whole_error(split[k], exact[k]) for k in exact)
+    assert worst_single > 2e-2, worst_single
+    assert worst_split < 1e-3, worst_split
