@@ -413,134 +413,6 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   }
 }
 
-// 2b'. The dx SpMM with the gathered W_gate / W_up rows streamed through a
-// per-thread ring of shared memory by asynchronous copies (as the weight-
-// gradient kernel's async variant): S batches of NB pairs in flight per CTA.
-template <class T, int VPT, int NB, int S>
-__global__ void __launch_bounds__(128) bwd_dx_async_kernel(BParams p) {
-  pdl_begin();
-  constexpr int EV = Vec<T>::EV;
-  constexpr int NTH = 128;
-  constexpr int LIST = 1024;  // pairs per tile group (a smaller list leaves room for the ring)
-  __shared__ int s_n[LIST];
-  __shared__ float s_g[LIST];
-  __shared__ float s_z[LIST];
-  __shared__ float s_u[LIST];
-  __shared__ int s_slot[LIST];
-  __shared__ int s_wsum[32];
-  __shared__ int s_total;
-  extern __shared__ uint4 ring[];  // [S][NB][2][VPT][NTH]
-
-  const int t = blockIdx.x, tid = threadIdx.x;
-  const int nt = p.F / p.C;
-  const int NV = p.D / EV;
-  const int ps = p.pos[t];
-  if (ps >= p.cap || gemm_row(p, ps)) return;
-  float2 dxg[VPT][EV / 2], dxu[VPT][EV / 2];
-#pragma unroll
-  for (int v = 0; v < VPT; ++v)
-#pragma unroll
-    for (int e = 0; e < EV / 2; ++e) dxg[v][e] = dxu[v][e] = make_float2(0.f, 0.f);
-  const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu;
-  auto slot = [&](int st, int b, int mtx, int v) -> uint4 * {
-    return ring + (size_t)(((st * NB + b) * 2 + mtx) * VPT + v) * NTH + tid;
-  };
-  const PairSource<T> src = bwd_source<T>(p, t, ps);
-  int group = LIST / (ps >= 0 ? p.C : p.K);
-  if (group > (int)blockDim.x) group = blockDim.x;
-  for (int g0 = 0; g0 < nt; g0 += group) {
-    const int P = build_pairs(src, g0, group, nt, s_n, s_g, s_slot, s_wsum, &s_total, p.status);
-    for (int i = tid; i < P; i += blockDim.x) {
-      const int sl = s_slot[i];
-      if (sl == PAD_SLOT) {
-        s_z[i] = 0.f;
-        s_u[i] = 0.f;
-        continue;
-      }
-      const size_t o = (size_t)ps * p.F + (-1 - sl);
-      s_z[i] = sl >= 0 ? p.dz[sl] : p.dzr[o];
-      s_u[i] = sl >= 0 ? p.du[sl] : p.dur[o];
-    }
-    __syncthreads();
-    const int nbat = (P + NB - 1) / NB;
-    auto issue = [&](int i) {
-      const int st = i % S;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int e = i * NB + b;
-        if (e >= P) break;
-        const size_t row = (size_t)s_n[e] * NV + tid;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          if (tid + v * NTH < NV) {
-            cp_async16(slot(st, b, 0, v), Wg4 + row + v * NTH);
-            if (p.gated) cp_async16(slot(st, b, 1, v), Wu4 + row + v * NTH);
-          }
-        }
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < S; ++i) {
-      if (i < nbat) issue(i);
-      cp_async_commit();
-    }
-    for (int i = 0; i < nbat; ++i) {
-      cp_async_wait<S - 1>();
-      const int st = i % S;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int e = i * NB + b;
-        if (e >= P) break;
-        const float z = s_z[e], u = s_u[e];
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          if (tid + v * NTH < NV) {
-            axpy_vec<T>(dxg[v], z, *slot(st, b, 0, v));
-            if (p.gated) axpy_vec<T>(dxu[v], u, *slot(st, b, 1, v));
-          }
-        }
-      }
-      if (i + S < nbat) issue(i + S);
-      cp_async_commit();
-    }
-    cp_async_wait<0>();
-    __syncthreads();  // the list is rewritten by the next group
-  }
-  uint4 *dxrow = (uint4 *)p.dx + (size_t)t * NV;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    const int vi = tid + v * NTH;
-    float o[EV];
-#pragma unroll
-    for (int e = 0; e < EV / 2; ++e) {
-      o[2 * e] = dxg[v][e].x + dxu[v][e].x;
-      o[2 * e + 1] = dxg[v][e].y + dxu[v][e].y;
-    }
-    if (vi < NV) stg_stream(dxrow + vi, Vec<T>::pack(o));
-  }
-}
-
-static bool launch_dx_async(const BParams &p, int T, int NV, cudaStream_t s) {
-  static const int mode = [] {
-    const char *e = getenv("TWELL_DX_ASYNC");
-    return e ? atoi(e) : 0;
-  }();
-  if (mode == 0 || (NV != 256 && NV != 512)) return false;
-  auto go = [&](auto kern, int vpt, int nb, int st) {
-    const size_t smem = (size_t)st * nb * 2 * vpt * 128 * 16;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_k(kern, T, 128, smem, s, p);
-  };
-  if (NV == 256) {
-    if (mode == 1) go(bwd_dx_async_kernel<bf16, 2, 2, 3>, 2, 2, 3);
-    else if (mode == 2) go(bwd_dx_async_kernel<bf16, 2, 3, 4>, 2, 3, 4);
-    else go(bwd_dx_async_kernel<bf16, 2, 2, 5>, 2, 2, 5);
-  } else {
-    go(bwd_dx_async_kernel<bf16, 4, 2, 3>, 4, 2, 3);
-  }
-  return true;
-}
-
 // ---------------------------------------------------------------------------
 // 3. Sparse transpose of the slots into neuron-major lists.  The list of
 // neuron j*C + c occupies col_e[col_start .. + col_cnt) inside tile j's region
@@ -725,141 +597,6 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// 4'. The same weight-gradient rows with the gathered x / dy rows streamed
-// through a per-thread ring of shared memory by asynchronous copies
-// (cp.async): a thread copies its own 16-byte vectors of the next S batches'
-// rows and later reads back only those, so the ring needs no barrier, and the
-// rows in flight hold no registers.  Each CTA then keeps S batches of NB
-// entries (2 rows each) in flight instead of one, which is what the gathers
-// need: at ~1% activity a neuron's ~40 entries form a chain of dependent
-// round trips to L2 when each batch must land before the next is requested.
-template <class T, int VPT, int NB, int S>
-__global__ void __launch_bounds__(128) bwd_dw_async_kernel(BParams p) {
-  pdl_begin();
-  constexpr int EV = Vec<T>::EV;
-  constexpr int NTH = 128;
-  constexpr int LIST = 256;
-  __shared__ float4 s_e[LIST];
-  extern __shared__ uint4 ring[];  // [S][NB][2][VPT][NTH]
-  if (p.gemm_rows && p.ctl->dense) return;  // the GEMMs write every row
-  const int n = blockIdx.x, tid = threadIdx.x;
-  const int NV = p.D / EV;
-  const uint4 *x4 = (const uint4 *)p.x, *dy4 = (const uint4 *)p.dy;
-  float2 ag[VPT][EV / 2], au[VPT][EV / 2], ad[VPT][EV / 2];
-#pragma unroll
-  for (int v = 0; v < VPT; ++v)
-#pragma unroll
-    for (int e = 0; e < EV / 2; ++e) ag[v][e] = au[v][e] = ad[v][e] = make_float2(0.f, 0.f);
-  float sb = 0.f;
-  auto slot = [&](int st, int b, int mtx, int v) -> uint4 * {
-    return ring + (size_t)(((st * NB + b) * 2 + mtx) * VPT + v) * NTH + tid;
-  };
-  const int start = p.col_start[n], cnt = p.col_cnt[n];
-  for (int c0 = 0; c0 < cnt; c0 += LIST) {
-    const int m = cnt - c0 < LIST ? cnt - c0 : LIST;
-    if (c0) __syncthreads();  // the previous chunk of the list is consumed
-    for (int i = tid; i < m; i += NTH) s_e[i] = p.col_e[start + c0 + i];
-    __syncthreads();
-    const int nbat = (m + NB - 1) / NB;
-    auto issue = [&](int i) {  // batch i's rows into stage i % S (this thread's vectors)
-      const int st = i % S;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int e = i * NB + b;
-        if (e >= m) break;
-        const int t = __float_as_int(s_e[e].x);
-        const uint4 *xr = x4 + (size_t)t * NV + tid, *yr = dy4 + (size_t)t * NV + tid;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          if (tid + v * NTH < NV) {
-            cp_async16(slot(st, b, 0, v), xr + v * NTH);
-            cp_async16(slot(st, b, 1, v), yr + v * NTH);
-          }
-        }
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < S; ++i) {  // S batches in flight
-      if (i < nbat) issue(i);
-      cp_async_commit();
-    }
-    for (int i = 0; i < nbat; ++i) {
-      cp_async_wait<S - 1>();  // batch i has landed (this thread's vectors)
-      const int st = i % S;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int e = i * NB + b;
-        if (e >= m) break;
-        const float4 r = s_e[e];
-        sb += r.y;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-          if (tid + v * NTH < NV) axpy3<T>(ag[v], au[v], ad[v], r, *slot(st, b, 0, v), *slot(st, b, 1, v));
-      }
-      if (i + S < nbat) issue(i + S);  // refill the stage just consumed
-      cp_async_commit();
-    }
-    cp_async_wait<0>();
-  }
-  // overflow rows (dense backup), unless the GEMMs add them afterwards
-  const int n_rows = (p.gemm_rows && p.ctl->ovf_gemm) ? 0 : min(p.ctl->n_ovf, p.cap);
-  const T *gfb = (const T *)p.g_fb;
-  for (int i = 0; i < n_rows; ++i) {
-    if (!(to_f(gfb[(size_t)i * p.F + n]) > 0.f)) continue;
-    const int t = p.rows[i];
-    const float4 r = make_float4(0.f, p.dzr[(size_t)i * p.F + n], p.dur[(size_t)i * p.F + n],
-                                 p.hr[(size_t)i * p.F + n]);
-    sb += r.y;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int vi = tid + v * NTH;
-      if (vi >= NV) continue;
-      axpy3<T>(ag[v], au[v], ad[v], r, x4[(size_t)t * NV + vi], dy4[(size_t)t * NV + vi]);
-    }
-  }
-  float4 *og = (float4 *)(p.dWg + (size_t)n * p.D), *od = (float4 *)(p.dWd + (size_t)n * p.D);
-  float4 *ou = p.gated ? (float4 *)(p.dWu + (size_t)n * p.D) : nullptr;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    const int vi = tid + v * NTH;
-    if (vi >= NV) continue;
-#pragma unroll
-    for (int q = 0; q < EV / 4; ++q) {
-      stg_stream(og + vi * (EV / 4) + q, f4bits(ag[v][2 * q], ag[v][2 * q + 1]));
-      stg_stream(od + vi * (EV / 4) + q, f4bits(ad[v][2 * q], ad[v][2 * q + 1]));
-      if (ou) stg_stream(ou + vi * (EV / 4) + q, f4bits(au[v][2 * q], au[v][2 * q + 1]));
-    }
-  }
-  if (tid == 0) p.dbg[n] = sb;
-}
-
-// Launch of the async-ring dW kernel for bf16 rows of 256 or 512 vectors
-// (d_model 2048 / 4096); returns false (nothing launched) for other shapes.
-static bool launch_dw_async(const BParams &p, int F, int NV, cudaStream_t s) {
-  static const int mode = [] {
-    const char *e = getenv("TWELL_DW_ASYNC");
-    return e ? atoi(e) : 0;
-  }();
-  if (mode == 0) return false;
-  if (NV != 256 && NV != 512) return false;
-  auto go = [&](auto kern, int vpt, int nb, int st) {
-    const size_t smem = (size_t)st * nb * 2 * vpt * 128 * 16;
-    static bool attr_done = false;
-    (void)attr_done;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_k(kern, F, 128, smem, s, p);
-  };
-  if (NV == 256) {
-    if (mode == 1) go(bwd_dw_async_kernel<bf16, 2, 2, 3>, 2, 2, 3);
-    else if (mode == 2) go(bwd_dw_async_kernel<bf16, 2, 3, 4>, 2, 3, 4);
-    else go(bwd_dw_async_kernel<bf16, 2, 2, 5>, 2, 2, 5);
-  } else {
-    go(bwd_dw_async_kernel<bf16, 4, 2, 3>, 4, 2, 3);
-  }
-  return true;
-}
-
-// ---------------------------------------------------------------------------
 cudaError_t aux_stream(AuxStream *&out) {
   static thread_local AuxStream per_dev[64];
   int dev = 0;
@@ -1005,8 +742,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     return r;
   };
   auto dx_spmm = [&]() {
-    if (bf && launch_dx_async(p, a.T, NV, s)) {
-    } else if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s);
+    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s);
     else TW_VPT(bwd_dx_kernel, float, a.T, s);
     const cudaError_t r = cudaGetLastError();
     prof_mark(KID_BWD_DX, s);
@@ -1021,8 +757,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = transpose();
   }
   if (e == cudaSuccess) {  // 4. weight gradients
-    if (bf && launch_dw_async(p, a.F, NV, sw)) {
-    } else if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw);
+    if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw);
     else TW_VPT(bwd_dw_kernel, float, a.F, sw);
     e = cudaGetLastError();
     prof_mark(KID_BWD_DW, sw);

@@ -74,27 +74,6 @@ __device__ __forceinline__ void ldg_stream32(const void *p, uint4 &a, uint4 &b) 
       : "l"(p), "l"(gather_policy<POL>()));
 }
 
-// 16-byte asynchronous copy of a gathered row's vector from global into
-// shared memory (cp.async, no L1 allocation, L2 policy POL): the load holds no
-// register while it is in flight, so a thread can keep several rows in
-// flight in a shared-memory ring.  Completion is tracked per thread with
-// commit / wait groups.
-template <int POL = L2_NORMAL>
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *src) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-               ::"r"(d), "l"(src), "l"(gather_policy<POL>())
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Wait until at most N of this thread's committed groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // 16-byte store of a row that is not read again by the same kernel (y, dx,
 // dW rows): no L1 allocation, evict-first in L2, so the stream of outputs
 // does not displace the gathered weight rows.

@@ -18,7 +18,8 @@ struct Workspace {
   int32_t *rows;      // [T] rows of the dense path (hybrid: overflow rows)
   int32_t *pos;       // [T] overflow position of each row, -1 if none
   // (the row buffers hold Tp = T rounded up to 128 rows)
-  void *h;            // [Tp][F] dtype: h rows of the dense path
+  void *h;            // [2 Tp][F] dtype: h rows of the dense path (bf16 gated: hi rows,
+                      // then lo rows)
   void *xg;           // [Tp][D] dtype: gathered x rows of the dense path
   void *wide;         // [F/C][T][C] dtype: full ReLU(z) of overflowing (tile, row)s
   void *urows;        // [Tp][F] dtype (training, CUDA-core path): u rows of the dense path

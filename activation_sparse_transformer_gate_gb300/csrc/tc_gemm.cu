@@ -531,7 +531,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
   //   EPI_DW: A_hi B, A_lo B
   const int Kd = p.k_dev ? *p.k_dev : p.Kdim;
   const int KT1 = (Kd + BK - 1) / BK;
-  const int NR = EPI == EPI_DX ? (p.gated ? 4 : 2) : (EPI == EPI_DW ? 2 : 1);
+  //   EPI_DOWN (gated): h_hi Wd, h_lo Wd (h = g u formed in fp32; the plain
+  //   FFN's h = g is exact in bf16: one range)
+  const int NR = EPI == EPI_DX ? (p.gated ? 4 : 2)
+                               : (EPI == EPI_DW || (EPI == EPI_DOWN && p.gated) ? 2 : 1);
   const int KT = NR * KT1;
   // Tile order.  When B is larger than half of L2, groups of gm M-blocks,
   // and within a group all N-blocks with the M-blocks innermost: the CTAs in
@@ -939,7 +942,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
               gz[in ? c : 32] = __ushort_as_bfloat16(slot_val(vw, k));
             }
           }
-          uint32_t hw[16], uw[16];
+          uint32_t uw[16];
+          float hv[32];
           const uint4 *g4 = (const uint4 *)gz;
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
@@ -948,15 +952,18 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
               const int i = 8 * v4 + 2 * q2;
-              const float g0 = bf_lo(gp[q2]), g1 = bf_hi(gp[q2]);
-              hw[i / 2] = pack_bf2(g0 * zu[i], g1 * zu[i + 1]);
+              hv[i] = bf_lo(gp[q2]) * zu[i];
+              hv[i + 1] = bf_hi(gp[q2]) * zu[i + 1];
               uw[i / 2] = pack_bf2(zu[i], zu[i + 1]);
             }
           }
-          uint4 *hd = (uint4 *)(p.h + (size_t)m * p.F + n0 + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            hd[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+          // h = g u in fp32 as bf16 hi + lo rows (rows m and Tp + m): the
+          // down GEMM contracts over both, so h enters it to ~2^-17
+          // relative, as on the gather path (one bf16 rounding of h alone
+          // gives output errors of several percent of rms where a row's
+          // output is dominated by a few large activations)
+          store_hi_lo(p.h + (size_t)m * p.F + n0 + c0, p.h + ((size_t)p.Tp + m) * p.F + n0 + c0,
+                      hv);
           if (dense_all && p.train && ps < 0) {
             // all-dense training: u at this row's slots in the block (staged
             // in shared memory to be picked by slot column)
@@ -1341,6 +1348,7 @@ TcParams base_params(const FwdArgs &a) {
   p.wide = (bf16 *)a.ws.wide;
   p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;
   p.status = a.tw.status;
+  p.Tp = (a.T + BM - 1) / BM * BM;  // rows of the h hi part (the lo part follows)
   return p;
 }
 
@@ -1396,12 +1404,15 @@ cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
   return launch_tc<128, 1, false, EPI_GU>(mxg, mx, mg, mg, p, tiles, s);
 }
 
-// Down projection of the dense-path rows: A = h rows (dense-path order),
+// Down projection of the dense-path rows: A = h rows (dense-path order; the
+// gated FFN's h as hi rows then lo rows, contracted as two K ranges),
 // B = W_down read MN-major from its neuron-major [F][D] storage.
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   // 128 x 256 output tiles (as the gate GEMM): half the A re-reads of 128 x 128
+  const int Tp = (a.T + BM - 1) / BM * BM;
   CUtensorMap mh, md;
-  if (!make_map(&mh, a.ws.h, a.F, a.T, 64, BM) || !make_map(&md, a.Wd, a.D, a.F, 64, 64))
+  if (!make_map(&mh, a.ws.h, a.F, a.gated ? 2 * Tp : a.T, 64, BM) ||
+      !make_map(&md, a.Wd, a.D, a.F, 64, 64))
     return cudaErrorInvalidValue;
   TcParams p = base_params(a);
   p.m_dev = &a.ws.ctl->n_rows;

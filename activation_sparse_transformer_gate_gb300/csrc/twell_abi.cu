@@ -83,7 +83,7 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
   w.rows = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   w.pos = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   const size_t Tp = ((size_t)T + 127) / 128 * 128;  // rows of the GEMM row buffers
-  w.h = take(es * Tp * F);
+  w.h = take(es * 2 * Tp * F);  // gated bf16 dense path: h hi rows, then lo rows
   w.xg = take(es * Tp * D);
   w.wide = take(es * Tp * F);
   if (train) {
@@ -166,7 +166,9 @@ float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_s
 // dense_density when > 0, none when < 0, else the default crossover of the
 // measured costs.  Per active (token, neuron) the forward gathers a W_up and
 // a W_down row (4·d_model bytes at ~14 TB/s when those matrices sit in L2)
-// where the dense path does ~6·d_model flops at ~1.3 PFLOP/s: 1.3%.  When
+// where the dense path does ~6·d_model flops per (token, neuron) beyond the
+// shared gate GEMM (up, and down on h's bf16 hi and lo parts) at ~1.3
+// PFLOP/s: measured crossover ~1.3% at d_model 2048 / d_ff 8192.  When
 // the gathered matrices exceed L2 the gathers slow in about the proportion
 // of rows that miss it (d_model 4096 / d_ff 14336 bf16: 235 MB, ~9.5 TB/s
 // measured, crossover ~0.65%), so the default scales by L2 / their bytes.

@@ -8,7 +8,7 @@ import activation_sparse_transformer_gate_gb300 as tw
 import oracle
 import synth
 from twell_testlib import (TOL, assert_close_rms, compare_twell, row_ovf_from_nnz, to_np64,
-                           torch_dev, z_allowance, z_band)
+                           torch_dev, value_allowance, z_band)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,7 @@ def check_forward(a, w, g, exact=False, rows=None, max_ambiguous=8):
             assert np.all(np.abs(gr - rr) <= tol), f"g_fb row {t}"
     y_ref = oracle.ffn_dense(xs, a["Wg"], a["bg"], rbs, a["Wu"], a["Wd"], dt, dt)
     assert np.isfinite(g["y"][sel]).all()
-    extra = None if exact or dt == "bf16" else z_allowance(a, dt, rows=sel)["y"]
+    extra = None if exact else value_allowance(a, dt, rows=sel, want=("y",))["y"]
     assert_close_rms(g["y"][sel], y_ref, dt, "y", extra=extra)
     return ref, z
 

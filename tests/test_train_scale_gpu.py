@@ -28,7 +28,7 @@ import activation_sparse_transformer_gate_gb300 as tw
 import oracle
 import synth
 from twell_testlib import (activity_flips, assert_close_rms, check_backward, ctl_fields,
-                           dh_gemm_of, run_train)
+                           dh_gemm_of, run_train, value_allowance)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,13 +54,16 @@ def check_dbg_full(a, w, g, lam):
     """dbg over every neuron (every token's dz) against the oracle, leaving
     out neurons that hold an activity flip."""
     _, bad_n = activity_flips(a, w, g)
-    assert len(bad_n) <= 8, sorted(bad_n)
+    cand = activity_flips.candidates
+    assert len(bad_n) <= max(8, 2 * cand), (sorted(bad_n), cand)
     # (one token's dx comes along: the oracle takes explicit selections)
     b = oracle.ffn_backward(a["x"], a["Wg"], a["bg"], a["rb"], a["Wu"], a["Wd"], a["dy"], lam,
                             w.dtype, w.dtype, tok_sel=np.zeros(1, dtype=np.int32))
     keep = np.ones(w.F, dtype=bool)
     keep[sorted(bad_n)] = False
-    assert_close_rms(g["dbg"][keep], b["dbg"][keep], w.dtype, "dbg(all neurons)", out_dtype="f32")
+    al = value_allowance(a, w.dtype, lam=lam, rows=np.zeros(0, dtype=np.int64), want=("dbg",))
+    assert_close_rms(g["dbg"][keep], b["dbg"][keep], w.dtype, "dbg(all neurons)", out_dtype="f32",
+                     extra=al["dbg"][keep])
 
 
 def check_y(a, w, g, rows):
@@ -69,7 +72,8 @@ def check_y(a, w, g, rows):
     rb = None if a["rb"] is None else a["rb"][rows]
     y_ref = oracle.ffn_dense(a["x"][rows], a["Wg"], a["bg"], rb, a["Wu"], a["Wd"], w.dtype,
                              w.dtype)
-    assert_close_rms(g["y"][rows], y_ref, w.dtype, "y")
+    al = value_allowance(a, w.dtype, rows=rows, want=("y",))
+    assert_close_rms(g["y"][rows], y_ref, w.dtype, "y", extra=al["y"])
 
 
 REGIMES = {
