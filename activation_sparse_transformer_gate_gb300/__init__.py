@@ -32,9 +32,9 @@ TWELL_ERR = {
 }
 TWELL_F32, TWELL_BF16 = 0, 1
 
-EXPORTS = ("twell_workspace_size", "twell_pack_dense", "twell_pack", "twell_ffn_forward",
-           "twell_ffn_backward", "twell_get_status", "twell_version", "twell_rowell_pack_dense",
-           "twell_rowell_forward")
+EXPORTS = ("twell_workspace_size", "twell_workspace_size_rows", "twell_pack_dense", "twell_pack",
+           "twell_ffn_forward", "twell_ffn_backward", "twell_get_status", "twell_version",
+           "twell_rowell_pack_dense", "twell_rowell_forward")
 
 
 class TwellError(RuntimeError):
@@ -52,6 +52,7 @@ class twell_t(ctypes.Structure):
         ("g_fb", ctypes.c_void_p), ("u_val", ctypes.c_void_p), ("u_fb", ctypes.c_void_p),
         ("status", ctypes.c_void_p), ("dense_switch", ctypes.c_float),
         ("dense_density", ctypes.c_float), ("dh_density", ctypes.c_float),
+        ("dense_rows_cap", ctypes.c_int32),
     ]
 
 
@@ -81,6 +82,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     TP = ctypes.POINTER(twell_t)
     lib.twell_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.twell_workspace_size.restype = S
+    lib.twell_workspace_size_rows.argtypes = [I, I, I, I, I, I, I, I]
+    lib.twell_workspace_size_rows.restype = S
     lib.twell_pack_dense.argtypes = [P, TP, P]
     lib.twell_pack.argtypes = [P, P, P, P, I, TP, P, S, P]
     lib.twell_ffn_forward.argtypes = [P, P, P, P, P, P, I, I, TP, P, P, S, P]
@@ -126,6 +129,12 @@ def twell_version() -> str:
 
 def twell_workspace_size(T: int, D: int, F: int, C: int, K: int, dtype: int, train: int) -> int:
     return int(load().twell_workspace_size(T, D, F, C, K, dtype, int(train)))
+
+
+def twell_workspace_size_rows(T: int, D: int, F: int, C: int, K: int, dtype: int, train: int,
+                              dense_rows_cap: int) -> int:
+    return int(load().twell_workspace_size_rows(T, D, F, C, K, dtype, int(train),
+                                                int(dense_rows_cap)))
 
 
 def twell_pack_dense(H, tw: twell_t, stream=None) -> None:
@@ -176,7 +185,7 @@ class TwellBuffers:
 
     def __init__(self, T: int, F: int, C: int, K: int, dtype: int, ovf_cap: Optional[int] = None,
                  train: bool = False, device="cuda", dense_switch: float = 0.0,
-                 dense_density: float = 0.0, dh_density: float = 0.0):
+                 dense_density: float = 0.0, dh_density: float = 0.0, dense_rows_cap: int = 0):
         import torch
         tdt = torch.bfloat16 if dtype == TWELL_BF16 else torch.float32
         nt = F // C
@@ -196,7 +205,7 @@ class TwellBuffers:
                          ovf_cap=cap, g_fb=_ptr(self.g_fb), u_val=_ptr(self.u_val),
                          u_fb=_ptr(self.u_fb), status=_ptr(self.status),
                          dense_switch=float(dense_switch), dense_density=float(dense_density),
-                         dh_density=float(dh_density))
+                         dh_density=float(dh_density), dense_rows_cap=int(dense_rows_cap))
 
 
 class RowEllBuffers:
@@ -214,10 +223,12 @@ class RowEllBuffers:
                                 val=_ptr(self.val), nnz=_ptr(self.nnz), status=_ptr(self.status))
 
 
-def workspace(T: int, D: int, F: int, C: int, K: int, dtype: int, train: bool, device="cuda"):
-    """Allocate a workspace tensor of twell_workspace_size bytes (256-byte aligned by torch)."""
+def workspace(T: int, D: int, F: int, C: int, K: int, dtype: int, train: bool, device="cuda",
+              dense_rows_cap: int = 0):
+    """Allocate a workspace tensor of twell_workspace_size_rows bytes (256-byte
+    aligned by torch); dense_rows_cap must match the twell_t's."""
     import torch
-    n = twell_workspace_size(T, D, F, C, K, dtype, int(train))
+    n = twell_workspace_size_rows(T, D, F, C, K, dtype, int(train), int(dense_rows_cap))
     if n == 0:
         raise TwellError(-1, "twell_workspace_size")
     return torch.empty((n,), dtype=torch.uint8, device=device), n

@@ -606,14 +606,17 @@ cudaError_t aux_stream(AuxStream *&out) {
   AuxStream &a = per_dev[dev];
   if (!a.s2) {
     e = cudaStreamCreateWithFlags(&a.s2, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&a.s3, cudaStreamNonBlocking);
+    for (cudaEvent_t *ev : {&a.fork, &a.join, &a.fork3, &a.join3, &a.mid})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {  // release what was made; the next call tries again
-      if (a.join) cudaEventDestroy(a.join);
-      if (a.fork) cudaEventDestroy(a.fork);
+      for (cudaEvent_t *ev : {&a.mid, &a.join3, &a.fork3, &a.join, &a.fork}) {
+        if (*ev) cudaEventDestroy(*ev);
+        *ev = nullptr;
+      }
+      if (a.s3) cudaStreamDestroy(a.s3);
       if (a.s2) cudaStreamDestroy(a.s2);
-      a.s2 = nullptr;
-      a.fork = a.join = nullptr;
+      a.s2 = a.s3 = nullptr;
       return e;
     }
   }
@@ -649,25 +652,55 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
                               gemm ? a.dh_density : -1.f);
   if (e != cudaSuccess) return e;
   prof_mark(KID_OVERFLOW_COMPACT, s, 2);
-  // 1'. dense-path rows on the tensor cores (idle when there are none):
-  // gathered dy / x rows, dh -> dz / du / h, dx
-  if (gemm) {
-    e = launch_bwd_prep_rows(a, s);
+  // Side streams (the caller's stream alone while per-launch timing is on,
+  // so that each interval times one kernel): s3 runs the dense-path rows'
+  // chain, s2 the sparse transpose and the weight-gradient gathers.
+  const bool fork = !prof_enabled();
+  AuxStream *aux = nullptr;
+  cudaStream_t sd = s, sw = s;
+  if (fork) {
+    e = aux_stream(aux);
     if (e != cudaSuccess) return e;
-    prof_mark(KID_BWD_PREP, s);
-    e = launch_tc_bwd_dh(a, s);
-    if (e != cudaSuccess) return e;
-    prof_mark(KID_BWD_DENSE, s);
-    e = launch_tc_bwd_dx(a, s);
-    if (e != cudaSuccess) return e;
-    prof_mark(KID_BWD_DENSE_DX, s);
+    sd = aux->s3;
+    sw = aux->s2;
   }
+  // 1'. dense-path rows on the tensor cores (idle when there are none):
+  // gathered dy / x rows, dh -> dz / du / h, dx.  They own other rows (and
+  // other buffers) than the gather path, so they run beside it on s3.
+  bool forked3 = false;
+  if (gemm) {
+    if (fork) {
+      e = cudaEventRecord(aux->fork3, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, aux->fork3, 0);
+      if (e != cudaSuccess) return e;
+      forked3 = true;
+    }
+    e = launch_bwd_prep_rows(a, sd);
+    if (e == cudaSuccess) {
+      prof_mark(KID_BWD_PREP, sd);
+      e = launch_tc_bwd_dh(a, sd);
+    }
+    if (e == cudaSuccess) {
+      prof_mark(KID_BWD_DENSE, sd);
+      e = launch_tc_bwd_dx(a, sd);
+    }
+    if (e == cudaSuccess) prof_mark(KID_BWD_DENSE_DX, sd);
+    if (e == cudaSuccess && fork) e = cudaEventRecord(aux->mid, sd);  // dense rows' dh done
+  }
+  // joins s3 back into the caller's stream (also after an error)
+  auto join3 = [&](cudaError_t err) {
+    if (!forked3) return err;
+    const cudaError_t j1 = cudaEventRecord(aux->join3, sd);
+    const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, aux->join3, 0) : j1;
+    return err == cudaSuccess ? j2 : err;
+  };
+  if (e != cudaSuccess) return join3(e);
   // 2. dh of the rows the gathers own: one tensor-core GEMM read at the
   // slots when the dispatcher chose it (its CTAs return at once otherwise),
   // else the per-token SDDMM (whose CTAs then return at once); then dx SpMM
   if (gemm) {
     e = launch_tc_bwd_dh_sampled(a, s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return join3(e);
     prof_mark(KID_BWD_DH_GEMM, s);
   }
   const int EV = bf ? 8 : 4;
@@ -710,7 +743,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
 #undef TW_DH_T
 #undef TW_DH
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) return join3(e);
   prof_mark(KID_BWD_SLOTS, s);
 #define TW_VPT(K, TT, G, SS)                                                                   \
   do {                                                                                         \
@@ -719,17 +752,11 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, SS, p);                         \
     else launch_k(K<TT, 4, 2, 0>, G, threads, 0, SS, p);                                       \
   } while (0)
-  // Steps 3-4 on the second stream (the caller's while per-launch timing is
-  // on): forked here, after dh, and joined before returning.
-  const bool fork = !prof_enabled();
-  AuxStream *aux = nullptr;
-  cudaStream_t sw = s;
+  // Steps 3-4 on s2: forked here, after dh, and joined before returning.
   if (fork) {
-    e = aux_stream(aux);
-    if (e == cudaSuccess) e = cudaEventRecord(aux->fork, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->s2, aux->fork, 0);
-    if (e != cudaSuccess) return e;
-    sw = aux->s2;
+    e = cudaEventRecord(aux->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sw, aux->fork, 0);
+    if (e != cudaSuccess) return join3(e);
   }
   const int nt = a.F / a.C;
   const dim3 tgrid(nt, (a.T + TR_CHUNK - 1) / TR_CHUNK);
@@ -763,9 +790,11 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     prof_mark(KID_BWD_DW, sw);
   }
 #undef TW_VPT
-  // 5. weight gradients of the dense-path rows (added to those of step 4)
+  // 5. weight gradients of the dense-path rows (added to those of step 4;
+  // after the dense rows' dh on s3)
   if (e == cudaSuccess && gemm) {
-    e = launch_tc_bwd_dw(a, sw);
+    if (fork) e = cudaStreamWaitEvent(sw, aux->mid, 0);
+    if (e == cudaSuccess) e = launch_tc_bwd_dw(a, sw);
     prof_mark(KID_BWD_DENSE_DW, sw);
   }
   if (fork) {  // join (also after an error, so the caller's stream stays ordered)
@@ -773,7 +802,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, aux->join, 0) : j1;
     if (e == cudaSuccess) e = j2;
   }
-  return e;
+  return join3(e);
 }
 
 }  // namespace twell

@@ -17,7 +17,8 @@ struct Workspace {
   uint32_t *ovf_bits; // [ceil(T/32)] overflow-row bitmap (set by the gate epilogue)
   int32_t *rows;      // [T] rows of the dense path (hybrid: overflow rows)
   int32_t *pos;       // [T] overflow position of each row, -1 if none
-  // (the row buffers hold Tp = T rounded up to 128 rows)
+  // (the row buffers hold rp rows: T, or the caller's dense-row cap, rounded
+  // up to 128)
   void *h;            // [2 Tp][F] dtype: h rows of the dense path (bf16 gated: hi rows,
                       // then lo rows)
   void *xg;           // [Tp][D] dtype: gathered x rows of the dense path
@@ -38,11 +39,15 @@ struct Workspace {
                       // [2 Tp][F] bf16: dz hi rows then lo rows (tensor-core rows)
   float *dur;         // the same for du
   float *hr;          // the same for h
+  int rp;             // rows of the dense-path row buffers (a multiple of 128): T
+                      // rounded up, or the caller's dense-row cap rounded up
   size_t bytes;       // total bytes needed
 };
 
-// Lay out (or size, when base == nullptr) the workspace.
-Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train);
+// Lay out (or size, when base == nullptr) the workspace; rows_cap (<= 0: T)
+// bounds the rows of the dense-path buffers.
+Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train,
+                          int rows_cap);
 
 struct FwdArgs {
   int T, D, F, C, K, dtype, gated, train;
@@ -87,6 +92,7 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // slot_parts (n_parts entries, from launch_flags_from_nnz) replaces the gate
 // epilogue's count in ctl->slots.  dh_density > 0 (backward): ctl->dh_gemm
 // when not all-dense and the slots exceed dh_density * T * F.
+// The dense path takes at most ws->rp rows (no all-dense mode when rp < T).
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user = true,
                                     float dense_density = -1.f,
@@ -176,21 +182,23 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);
 
 // backward.cu
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s);
-// The library's second stream and its fork / join events, one set per host
+// The library's side streams and their fork / join events, one set per host
 // thread and device (created on first use, released when the thread exits):
-// work forked onto it after a record of `fork` on the caller's stream is
-// joined back by a record of `join` and a wait on the caller's stream.
+// work forked onto s2 (or s3) after a record of `fork` (`fork3`) on the
+// caller's stream is joined back by a record of `join` (`join3`) and a wait
+// on the caller's stream.  `mid` orders work between the two side streams.
 struct AuxStream {
-  cudaStream_t s2 = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t s2 = nullptr, s3 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, fork3 = nullptr, join3 = nullptr, mid = nullptr;
   AuxStream() = default;
   AuxStream(const AuxStream &) = delete;
   AuxStream &operator=(const AuxStream &) = delete;
-  // (work still queued on s2 completes; errors at process teardown, when the
-  // runtime may already be unloaded, are ignored)
+  // (work still queued on the side streams completes; errors at process
+  // teardown, when the runtime may already be unloaded, are ignored)
   ~AuxStream() {
-    if (join) cudaEventDestroy(join);
-    if (fork) cudaEventDestroy(fork);
+    for (cudaEvent_t e : {mid, join3, fork3, join, fork})
+      if (e) cudaEventDestroy(e);
+    if (s3) cudaStreamDestroy(s3);
     if (s2) cudaStreamDestroy(s2);
   }
 };

@@ -83,12 +83,16 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s) 
 // one dense GEMM read at the slots when the slots exceed dh_density * T * F
 // (each active entry costs the SDDMM a d_model row; the GEMM costs the same
 // per entry of the whole T x F product).
+// The dense path takes at most rows_cap rows (the workspace's dense-row
+// buffers): no all-dense mode when rows_cap < Tn, and overflow rows beyond it
+// stay on the gathers.
 __device__ __forceinline__ void write_ctl(Ctl *ctl, int n_ovf, int Tn, int F, float dense_switch,
-                                          float dense_density, float dh_density) {
+                                          float dense_density, float dh_density, int rows_cap) {
   const double TF = (double)Tn * (double)F;
   const bool too_dense = dense_density > 0.f && (double)ctl->slots > (double)dense_density * TF;
-  const int dense = ((float)n_ovf > dense_switch * (float)Tn || too_dense) ? 1 : 0;
-  const int og = (!dense && n_ovf >= OVF_GEMM_MIN) ? 1 : 0;
+  const int dense =
+      (((float)n_ovf > dense_switch * (float)Tn || too_dense) && Tn <= rows_cap) ? 1 : 0;
+  const int og = (!dense && n_ovf >= OVF_GEMM_MIN && n_ovf <= rows_cap) ? 1 : 0;
   ctl->n_ovf = n_ovf;
   ctl->dense = dense;
   ctl->ovf_gemm = og;
@@ -155,7 +159,7 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
                      Ctl *ctl, int32_t *__restrict__ rows, int32_t *__restrict__ pos,
                      int F, float dense_switch, float dense_density,
                      const unsigned long long *__restrict__ slot_parts, int n_parts,
-                     float dh_density) {
+                     float dh_density, int rows_cap) {
   pdl_begin();
   __shared__ int warp_off[32];
   __shared__ int word_off[1024];
@@ -219,7 +223,7 @@ overflow_scan_kernel(const uint32_t *__restrict__ bits, int Tn, int cap,
     }
     if (n_ovf) *n_ovf = running;
     if (running > cap) set_status(status, TWELL_ERR_CAPACITY);
-    write_ctl(ctl, running, Tn, F, dense_switch, dense_density, dh_density);
+    write_ctl(ctl, running, Tn, F, dense_switch, dense_density, dh_density, rows_cap);
   }
 }
 
@@ -231,7 +235,7 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
     launch_k(overflow_scan_kernel, 1, 1024, 0, s, ws->ovf_bits, tw.T, tw.ovf_cap,
              write_user ? tw.ovf_rows : nullptr, write_user ? tw.n_ovf : nullptr, tw.status,
              ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density, slot_parts, n_parts,
-             dh_density);
+             dh_density, ws->rp > 0 ? ws->rp : tw.T);
     return cudaGetLastError();
   }
   launch_k(overflow_compact_kernel, 1, 1024, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,

@@ -299,7 +299,7 @@ struct TcParams {
   const Ctl *ctl;          // dense-path control (EPI_GU / EPI_DOWN), else null
   int N, Kdim;             // output columns, contraction length
   int Tn, F, D, C, Kslots, cap, gated, train;
-  int Tp;                  // backward: rows of a hi part (T rounded up to 128)
+  int Tp;                  // rows of a hi part (the dense-path row buffers' rows)
   long long l2_bytes;      // L2 size of the device (tile order)
   const float *bg, *rb;
   const int32_t *rows, *pos;
@@ -1348,7 +1348,7 @@ TcParams base_params(const FwdArgs &a) {
   p.wide = (bf16 *)a.ws.wide;
   p.h = (bf16 *)a.ws.h; p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb; p.y = (bf16 *)a.y;
   p.status = a.tw.status;
-  p.Tp = (a.T + BM - 1) / BM * BM;  // rows of the h hi part (the lo part follows)
+  p.Tp = a.ws.rp;  // rows of the h hi part (the lo part follows)
   return p;
 }
 
@@ -1409,9 +1409,9 @@ cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
 // B = W_down read MN-major from its neuron-major [F][D] storage.
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   // 128 x 256 output tiles (as the gate GEMM): half the A re-reads of 128 x 128
-  const int Tp = (a.T + BM - 1) / BM * BM;
+  const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   CUtensorMap mh, md;
-  if (!make_map(&mh, a.ws.h, a.F, a.gated ? 2 * Tp : a.T, 64, BM) ||
+  if (!make_map(&mh, a.ws.h, a.F, a.gated ? 2 * Tp : Tp, 64, BM) ||
       !make_map(&md, a.Wd, a.D, a.F, 64, 64))
     return cudaErrorInvalidValue;
   TcParams p = base_params(a);
@@ -1426,9 +1426,10 @@ cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 // Backward of the dense-path rows: every row in all-dense mode, else the
 // overflow rows when there are at least OVF_GEMM_MIN of them (the kernels
-// return at once when there are none).  Row buffers (Tp = T rounded up to
-// 128 rows): ws.dzr / ws.dur / ws.hr = dz / du / h as bf16 hi rows then lo
-// rows ([2 Tp][F]); ws.dyg / ws.xg = gathered dy / x rows ([Tp][D]).
+// return at once when there are none).  Row buffers (Tp = ws.rp rows: T, or
+// the caller's dense-row cap, rounded up to 128): ws.dzr / ws.dur / ws.hr =
+// dz / du / h as bf16 hi rows then lo rows ([2 Tp][F]); ws.dyg / ws.xg =
+// gathered dy / x rows ([Tp][D]).
 namespace {
 
 TcParams bwd_params(const BwdArgs &a) {
@@ -1439,7 +1440,7 @@ TcParams bwd_params(const BwdArgs &a) {
   p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val; p.uval = (bf16 *)a.tw.u_val;
   p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb;
   p.dz2 = (bf16 *)a.ws.dzr; p.du2 = (bf16 *)a.ws.dur; p.h2 = (bf16 *)a.ws.hr;
-  p.Tp = (a.T + BM - 1) / BM * BM;
+  p.Tp = a.ws.rp;
   p.y = (bf16 *)a.dx; p.lambda = a.lambda; p.dbg_r = a.ws.dbg_r; p.status = a.tw.status;
   return p;
 }
@@ -1448,7 +1449,7 @@ TcParams bwd_params(const BwdArgs &a) {
 
 // dh = dy W_down^T over the dense-path rows, then the L1 term and dz / du / h.
 cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s) {
-  const int Tp = (a.T + BM - 1) / BM * BM;
+  const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   CUtensorMap mdyg, mdy, mwd;
   if (!make_map(&mdyg, a.ws.dyg, a.D, Tp, 64, BM) || !make_map(&mdy, a.dy, a.D, a.T, 64, BM) ||
       !make_map(&mwd, a.Wd, a.D, a.F, 64, 256))
@@ -1484,7 +1485,7 @@ cudaError_t launch_tc_bwd_dh_sampled(const BwdArgs &a, cudaStream_t s) {
 // four K ranges: the hi and lo parts of dz and du; W read MN-major from
 // [F][D]).
 cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s) {
-  const int Tp = (a.T + BM - 1) / BM * BM;
+  const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   CUtensorMap mz, mu, mwg, mwu;
   if (!make_map(&mz, a.ws.dzr, a.F, 2 * Tp, 64, BM) ||
       !make_map(&mu, a.ws.dur, a.F, 2 * Tp, 64, BM) || !make_map(&mwg, a.Wg, a.D, a.F, 64, 64) ||
@@ -1502,7 +1503,7 @@ cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s) {
 // of dz / du / h as two K ranges).  Stored in all-dense mode, added to the
 // gather kernel's rows otherwise.
 cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s) {
-  const int Tp = (a.T + BM - 1) / BM * BM;
+  const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   // problems: dWg (A = dz, B = x), [dWu (du, x),] dWd (h, dy)
   TcMaps maps;
   const void *A[3] = {a.ws.dzr, a.gated ? (const void *)a.ws.dur : a.ws.hr, a.ws.hr};

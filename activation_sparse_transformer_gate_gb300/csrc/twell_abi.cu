@@ -67,7 +67,8 @@ static const char *kKernelNames[KID_COUNT] = {
     "bwd_dense_dw_gemm",    "bwd_prep_rows",    "rowell_pack_dense",  "rowell_updown",
     "bwd_dh_gemm_sampled"};
 
-Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train) {
+Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train,
+                          int rows_cap) {
   Workspace w;
   memset(&w, 0, sizeof(w));
   const size_t es = dtype == TWELL_BF16 ? 2 : 4;
@@ -82,13 +83,17 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
   w.ovf_bits = (uint32_t *)take(4 * (((size_t)T + 31) / 32));
   w.rows = (int32_t *)take(sizeof(int32_t) * (size_t)T);
   w.pos = (int32_t *)take(sizeof(int32_t) * (size_t)T);
-  const size_t Tp = ((size_t)T + 127) / 128 * 128;  // rows of the GEMM row buffers
-  w.h = take(es * 2 * Tp * F);  // gated bf16 dense path: h hi rows, then lo rows
-  w.xg = take(es * Tp * D);
-  w.wide = take(es * Tp * F);
+  const size_t Tp = ((size_t)T + 127) / 128 * 128;
+  // rows of the dense-path row buffers (a GEMM tile never leaves them)
+  const int cap = (rows_cap <= 0 || rows_cap >= T) ? T : rows_cap;
+  const size_t Rp = ((size_t)cap + 127) / 128 * 128;
+  w.rp = (int)Rp;
+  w.h = take(es * 2 * Rp * F);  // gated bf16 dense path: h hi rows, then lo rows
+  w.xg = take(es * Rp * D);
+  w.wide = take(es * Tp * F);   // indexed by token (written for overflowing tiles)
   if (train) {
-    w.urows = take(es * Tp * F);
-    w.dyg = take(es * Tp * D);
+    w.urows = take(es * Rp * F);
+    w.dyg = take(es * Rp * D);
     w.dbg_r = (float *)take(4 * (size_t)F);
     w.slot_parts = (unsigned long long *)take(8 * (size_t)SLOT_PARTS_MAX);
     const size_t slots = nt * (size_t)T * (size_t)K;
@@ -99,11 +104,11 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_e = (float4 *)take(16 * slots);
     w.col_chunk = (int32_t *)take(4 * (size_t)F * (((size_t)T + 1023) / 1024));
-    // fp32 [T][F] rows of the gather path, or bf16 hi + lo rows [2 Tp][F]
-    // of the tensor-core backward (never both in one call)
-    w.dzr = (float *)take(4 * Tp * F);
-    w.dur = (float *)take(4 * Tp * F);
-    w.hr = (float *)take(4 * Tp * F);
+    // fp32 [rp][F] rows of the gather path's overflow rows, or bf16 hi + lo
+    // rows [2 rp][F] of the tensor-core backward (never both in one call)
+    w.dzr = (float *)take(4 * Rp * F);
+    w.dur = (float *)take(4 * Rp * F);
+    w.hr = (float *)take(4 * Rp * F);
   }
   w.bytes = off;
   return w;
@@ -137,7 +142,7 @@ twell_status check_tw(const twell_t *tw, int train) {
   twell_status s = check_shape(tw->T, 16, tw->F, tw->C, tw->K, tw->dtype);
   if (s != TWELL_OK) return s;
   if (!tw->idx || !tw->val || !tw->nnz || !tw->n_ovf || !tw->status) return TWELL_ERR_ARG;
-  if (tw->ovf_cap < 0) return TWELL_ERR_ARG;
+  if (tw->ovf_cap < 0 || tw->dense_rows_cap < 0) return TWELL_ERR_ARG;
   if (tw->ovf_cap > 0 && (!tw->ovf_rows || !tw->g_fb)) return TWELL_ERR_ARG;
   if (!aligned16(tw->idx) || !aligned16(tw->val) || !aligned16(tw->nnz)) return TWELL_ERR_ALIGN;
   if (tw->ovf_cap > 0 && !aligned16(tw->g_fb)) return TWELL_ERR_ALIGN;
@@ -253,8 +258,13 @@ extern "C" {
 const char *twell_version(void) { return "twell-gb300 0.1 (sm_103a)"; }
 
 size_t twell_workspace_size(int T, int D, int F, int C, int K, int dtype, int train) {
+  return twell_workspace_size_rows(T, D, F, C, K, dtype, train, 0);
+}
+
+size_t twell_workspace_size_rows(int T, int D, int F, int C, int K, int dtype, int train,
+                                 int dense_rows_cap) {
   if (check_shape(T, D, F, C, K, dtype) != TWELL_OK) return 0;
-  return carve_workspace(nullptr, T, D, F, C, K, dtype, train).bytes;
+  return carve_workspace(nullptr, T, D, F, C, K, dtype, train, dense_rows_cap).bytes;
 }
 
 twell_status twell_pack_dense(const void *H, twell_t *tw, void *stream) {
@@ -282,14 +292,14 @@ twell_status twell_pack(const void *x, const void *Wg, const float *bg, const fl
   if (st != TWELL_OK) return st;
   if (!x || !Wg || !bg) return TWELL_ERR_ARG;
   if (!aligned16(x) || !aligned16(Wg)) return TWELL_ERR_ALIGN;
-  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 0);
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 0, tw->dense_rows_cap);
   st = check_ws(workspace, workspace_bytes, need);
   if (st != TWELL_OK) return st;
   FwdArgs a;
   memset(&a, 0, sizeof(a));
   a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
   a.gated = 0; a.train = 0; a.x = x; a.Wg = Wg; a.bg = bg; a.rb = row_bias; a.tw = *tw;
-  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 0);
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 0, tw->dense_rows_cap);
   a.dense_switch = 2.0f;  // the pack never switches to all-dense mode
   a.dense_density = -1.f;
   cudaStream_t s = (cudaStream_t)stream;
@@ -315,7 +325,7 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wd) || !aligned16(y) ||
       (Wu && !aligned16(Wu)))
     return TWELL_ERR_ALIGN;
-  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, train);
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, train, tw->dense_rows_cap);
   st = check_ws(workspace, workspace_bytes, need);
   if (st != TWELL_OK) return st;
   FwdArgs a;
@@ -323,7 +333,7 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   a.T = tw->T; a.D = D; a.F = tw->F; a.C = tw->C; a.K = tw->K; a.dtype = tw->dtype;
   a.gated = gated; a.train = train ? 1 : 0;
   a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd; a.bg = bg; a.rb = row_bias; a.tw = *tw; a.y = y;
-  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, train);
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, train, tw->dense_rows_cap);
   a.dense_switch = switch_of(tw);
   a.dense_density = density_of(tw, D, gated, false);
   cudaStream_t s = (cudaStream_t)stream;
@@ -376,7 +386,7 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wd) || !aligned16(dy) || !aligned16(dx) ||
       !aligned16(dWg) || !aligned16(dWd) || (gated && (!aligned16(Wu) || !aligned16(dWu))))
     return TWELL_ERR_ALIGN;
-  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 1);
+  Workspace need = carve_workspace(nullptr, tw->T, D, tw->F, tw->C, tw->K, tw->dtype, 1, tw->dense_rows_cap);
   st = check_ws(workspace, workspace_bytes, need);
   if (st != TWELL_OK) return st;
   BwdArgs a;
@@ -387,7 +397,10 @@ twell_status twell_ffn_backward(const void *x, const void *Wg, const void *Wu, c
   a.dense_switch = switch_of(tw);
   a.dense_density = density_of(tw, D, gated, true);
   a.dh_density = dh_density_of(tw, D);
-  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1);
+  a.ws = carve_workspace(workspace, a.T, D, a.F, a.C, a.K, a.dtype, 1, tw->dense_rows_cap);
+  // the backward keeps the gradients of an overflow row on the gather path in
+  // the workspace's row buffers: at most rp of them
+  if (a.tw.ovf_cap > a.ws.rp) a.tw.ovf_cap = a.ws.rp;
   return cuda_status(launch_backward(a, (cudaStream_t)stream));
 }
 

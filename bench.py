@@ -442,6 +442,12 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_energy:
         mem, energy = memory_and_energy(torch, dev, local_rank, d, w, train, b.step, bufs, nws,
                                         int(row_ovf_count(bufs, w)))
+        if w.dtype == "bf16":
+            cm = capped_memory(torch, tw, b, timed)
+            mem["capped_step"] = cm
+            mem["capped_vs_dense_peak"] = round(
+                cm["measured_peak_extra_bytes"] /
+                max(mem["dense_step_peak_beyond_outputs_bytes"], 1), 4)
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(b.a, w, train, args.cpu_seconds)
     del b, d, bufs, ws, y
     torch.cuda.empty_cache()
@@ -717,6 +723,45 @@ class PowerSampler:
         return samples
 
 
+def capped_memory(torch, tw, b, timed, cap=256):
+    """The same step with buffers and a workspace sized for at most `cap`
+    overflow rows and `cap` dense-path rows (twell_t.dense_rows_cap): the
+    device memory it needs beyond its inputs and outputs, measured as the
+    high-water mark of the allocator around the allocation and a step (the
+    library allocates nothing itself), and its time."""
+    w, dev, train = b.w, b.dev, b.train
+    T, D, F = w.T, w.D, w.F
+    torch.cuda.synchronize(dev)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    bufs = tw.TwellBuffers(T, F, w.C, w.K, b.dtype, ovf_cap=cap, train=train, device=dev,
+                           dense_rows_cap=cap)
+    ws, nws = tw.workspace(T, D, F, w.C, w.K, b.dtype, train, device=dev, dense_rows_cap=cap)
+    d = b.d
+
+    def step():
+        tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, int(train),
+                             bufs.t, b.y, ws, nws, b.sh)
+        if train:
+            tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], w.lam, D,
+                                  b.dx, b.dWg, b.dbg, b.dWu, b.dWd, ws, nws, b.sh)
+
+    for _ in range(3):
+        step()
+    code, n_ovf = tw.twell_get_status(bufs.t, b.sh)
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    ms = timed(step, 20) / 20
+    buf_bytes = sum(t.numel() * t.element_size() for t in
+                    (bufs.idx, bufs.val, bufs.nnz, bufs.ovf_rows, bufs.g_fb, bufs.u_val, bufs.u_fb,
+                     bufs.n_ovf, bufs.status) if t is not None)
+    out = {"dense_rows_cap": cap, "ovf_cap": cap, "status": code, "n_ovf": n_ovf,
+           "buffers_bytes": int(buf_bytes), "workspace_bytes": int(nws),
+           "measured_peak_extra_bytes": int(peak), "ms_per_step": round(ms, 5)}
+    del bufs, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def memory_and_energy(torch, dev, index, d, w, train, ours_step, bufs, nws, n_ovf, seconds=2.5):
     """Saved-activation bytes (forward -> backward) and device memory of the
     sparse path against the dense one, and energy per token of each measured
@@ -743,6 +788,11 @@ def memory_and_energy(torch, dev, index, d, w, train, ours_step, bufs, nws, n_ov
         "note_saved": "sparse: TwELL idx/val/nnz (+u at the slots) and the used overflow rows; "
                       "dense: z, u, h [T][F] bf16 kept for the backward",
         "dense_step_peak_extra_bytes": int(dense_peak),
+        # the dense step's outputs (y, and for training dx, the three weight
+        # gradients in bf16 and dbg) are part of its peak; the sparse path's
+        # outputs are the caller's preallocated tensors
+        "dense_step_peak_beyond_outputs_bytes": int(dense_peak - (
+            T * w.D * es + ((T * w.D * es + 3 * F * w.D * es + 4 * F) if train else 0))),
         "sparse_buffers_allocated_bytes": int(buf_bytes),
         "sparse_workspace_bytes": int(nws),
         "note_alloc": "buffers sized for ovf_cap = T overflow rows and a workspace sized for the "

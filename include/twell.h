@@ -121,12 +121,29 @@ typedef struct {
                              selects the measured crossover: 0.0065, scaled
                              by L2 / bytes of W_down when W_down does not fit
                              in L2; < 0 always gathers.                      */
+  int32_t dense_rows_cap; /* rows the workspace's dense-path buffers hold
+                             (0: T).  With a cap R < T the workspace is sized
+                             by twell_workspace_size_rows(..., R): the
+                             dispatcher then never runs more than R rows on
+                             the dense path (no all-dense mode; overflow rows
+                             beyond R stay on the gathers), and the backward
+                             keeps the gradients of at most min(ovf_cap, R)
+                             overflow rows (more: TWELL_ERR_CAPACITY).  The
+                             same value must be used for the workspace size
+                             and every call.                                 */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward
  * need for these sizes (train != 0: forward with saved activations and the
  * backward).  Returns 0 for invalid sizes. */
 size_t twell_workspace_size(int T, int D, int F, int C, int K, int dtype, int train);
+
+/* The same with the dense-path row buffers sized for dense_rows_cap rows
+ * (<= 0 or >= T: T rows, as twell_workspace_size).  A cap trades the
+ * all-dense fallback for memory: the dense-path buffers are the bulk of the
+ * workspace (with training, ~13 bytes x d_ff per row, plus the d_model rows). */
+size_t twell_workspace_size_rows(int T, int D, int F, int C, int K, int dtype, int train,
+                                 int dense_rows_cap);
 
 /* Pack a dense post-ReLU activation matrix H [T][F] (dtype = tw->dtype, all
  * entries >= 0) into TwELL + hybrid (section 2.A).  Fills idx, val, nnz,

@@ -157,3 +157,20 @@ def test_binding_structs_match_the_header(name):
     header's order (a field added on one side only would shift the others)."""
     py = [f[0] for f in getattr(tw, name)._fields_]
     assert py == header_struct_fields(name)
+
+
+def test_workspace_size_with_a_dense_row_cap(lib):
+    """A cap on the dense-path rows sizes those row buffers for the cap:
+    at the training-step shape, 256 rows instead of 4096."""
+    full = tw.twell_workspace_size(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1)
+    assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 0) == full
+    assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 4096) == full
+    assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 9999) == full
+    capped = tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 256)
+    # per dense row: h hi + lo (2 x 2F), u rows (2F), dz/du/h rows (3 x 4F) bytes, x and dy rows
+    per_row = 2 * 2 * 8192 + 2 * 8192 + 3 * 4 * 8192 + 2 * 2 * 2048
+    assert full - capped == (4096 - 256) * per_row
+    assert capped < full / 3
+    # rounded up to whole 128-row tiles
+    assert (tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 200) ==
+            capped)
