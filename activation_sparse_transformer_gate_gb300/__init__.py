@@ -28,7 +28,7 @@ TWELL_ERR = {
     -1: "TWELL_ERR_ARG", -2: "TWELL_ERR_ALIGN", -3: "TWELL_ERR_DTYPE",
     -4: "TWELL_ERR_CAPACITY", -5: "TWELL_ERR_INDEX", -6: "TWELL_ERR_TIMEOUT",
     -7: "TWELL_ERR_CUDA", -8: "TWELL_ERR_WORKSPACE", -9: "TWELL_ERR_UNSUPPORTED",
-    -10: "TWELL_ERR_STATIC_LIMIT",
+    -10: "TWELL_ERR_STATIC_LIMIT", -11: "TWELL_ERR_RANGE",
 }
 TWELL_F32, TWELL_BF16 = 0, 1
 

@@ -638,7 +638,9 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   p.dx = a.dx; p.dWg = a.dWg; p.dbg = a.dbg; p.dWu = a.dWu; p.dWd = a.dWd;
   p.status = a.tw.status;
   const bool bf = a.dtype == TWELL_BF16;
-  const bool gemm = bf && tc_available();
+  const bool tc = bf && tc_available();
+  // the dense-path rows' tensor-core GEMMs (when the workspace has their buffers)
+  const bool gemm = tc && a.ws.dense_bufs;
   p.gemm_rows = gemm ? 1 : 0;
 
   // 1. hybrid split of the saved activations into this workspace, with the
@@ -649,7 +651,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = launch_overflow_compact(a.tw, &a.ws, gemm ? a.dense_switch : 2.0f, s, /*write_user=*/false,
                               gemm ? a.dense_density : -1.f, a.ws.slot_parts, flags_blocks(a.T),
-                              gemm ? a.dh_density : -1.f);
+                              tc ? a.dh_density : -1.f);
   if (e != cudaSuccess) return e;
   prof_mark(KID_OVERFLOW_COMPACT, s, 2);
   // Side streams (the caller's stream alone while per-launch timing is on,
@@ -676,8 +678,14 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
       forked3 = true;
     }
     e = launch_bwd_prep_rows(a, sd);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess) {  // the fp16 operand copies of the weights
       prof_mark(KID_BWD_PREP, sd);
+      const void *src[3] = {a.Wd, a.Wg, a.gated ? a.Wu : nullptr};
+      void *const dst[3] = {a.ws.wd16, a.ws.wg16, a.gated ? a.ws.wu16 : nullptr};
+      e = launch_to_f16(src, dst, (size_t)a.F * (size_t)a.D, a.ws.ctl, a.tw.status, sd);
+    }
+    if (e == cudaSuccess) {
+      prof_mark(KID_TO_F16, sd);
       e = launch_tc_bwd_dh(a, sd);
     }
     if (e == cudaSuccess) {
@@ -698,7 +706,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // 2. dh of the rows the gathers own: one tensor-core GEMM read at the
   // slots when the dispatcher chose it (its CTAs return at once otherwise),
   // else the per-token SDDMM (whose CTAs then return at once); then dx SpMM
-  if (gemm) {
+  if (tc) {
     e = launch_tc_bwd_dh_sampled(a, s);
     if (e != cudaSuccess) return join3(e);
     prof_mark(KID_BWD_DH_GEMM, s);

@@ -19,12 +19,14 @@ struct Workspace {
   int32_t *pos;       // [T] overflow position of each row, -1 if none
   // (the row buffers hold rp rows: T, or the caller's dense-row cap, rounded
   // up to 128)
-  void *h;            // [2 Tp][F] dtype: h rows of the dense path (bf16 gated: hi rows,
-                      // then lo rows)
-  void *xg;           // [Tp][D] dtype: gathered x rows of the dense path
+  void *h;            // [rp][F]: h rows of the dense path (bf16 gated FFN: fp16)
+  void *xg;           // [rp][D] dtype: gathered x rows of the dense path (the
+                      // backward's tensor-core path: fp16)
   void *wide;         // [F/C][T][C] dtype: full ReLU(z) of overflowing (tile, row)s
   void *urows;        // [Tp][F] dtype (training, CUDA-core path): u rows of the dense path
-  void *dyg;          // [Tp][D] dtype (training): gathered dy rows of the dense path
+  void *dyg;          // [rp][D] (training, tensor-core path): dense-path dy rows, fp16
+  void *wd16, *wg16, *wu16;  // [F][D] fp16 copies of W_down (and, training, W_gate,
+                      // W_up): operands of the dense-path GEMMs (bf16 only)
   float *dbg_r;       // [F] fp32 (training): dbg of the dense-path rows
   unsigned long long *slot_parts;  // [SLOT_PARTS_MAX] per-block slot counts (backward)
   // backward scratch
@@ -35,12 +37,14 @@ struct Workspace {
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
   float4 *col_e;      // [T*(F/C)*K] transposed entries {token (int bits), dz, du, h}
   int32_t *col_chunk; // [(F/C) * ceil(T/1024) * C] per-(tile, token chunk) column counts
-  float *dzr;         // [T][F] fp32: dz rows of the overflow rows (gather path), or
-                      // [2 Tp][F] bf16: dz hi rows then lo rows (tensor-core rows)
+  float *dzr;         // [rp][F] fp32: dz rows of the overflow rows (gather path), or
+                      // [rp][F] fp16: dz rows of the tensor-core dense-path rows
   float *dur;         // the same for du
   float *hr;          // the same for h
   int rp;             // rows of the dense-path row buffers (a multiple of 128): T
                       // rounded up, or the caller's dense-row cap rounded up
+  bool dense_bufs;    // the dense-path GEMM buffers exist (the cap allows a
+                      // dense-path row: cap >= T, or cap >= one 128-row tile)
   size_t bytes;       // total bytes needed
 };
 
@@ -92,7 +96,8 @@ cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // slot_parts (n_parts entries, from launch_flags_from_nnz) replaces the gate
 // epilogue's count in ctl->slots.  dh_density > 0 (backward): ctl->dh_gemm
 // when not all-dense and the slots exceed dh_density * T * F.
-// The dense path takes at most ws->rp rows (no all-dense mode when rp < T).
+// The dense path takes at most ws->rp rows (no all-dense mode when rp < T),
+// none when the workspace has no dense-path buffers.
 cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, float dense_switch,
                                     cudaStream_t s, bool write_user = true,
                                     float dense_density = -1.f,
@@ -117,9 +122,16 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
 // of 128 (dst holds T rounded up to 128 rows).
 cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
                                int dtype, cudaStream_t s);
-// Backward, dense-path rows (bf16): zeroes ws.dbg_r and, for overflow rows on
-// the GEMMs, gathers their dy and x rows into ws.dyg / ws.xg.
+// Backward, dense-path rows (bf16): zeroes ws.dbg_r and copies the dy and x
+// rows of the dense-path rows (every row in all-dense mode) into ws.dyg /
+// ws.xg as fp16.
 cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s);
+// fp16 copies of up to three bf16 [F][D] matrices (src[i] -> dst[i], null
+// entries skipped), done only when the dispatcher sent rows to the dense
+// path (ctl->n_rows > 0); a value beyond the fp16 range records
+// TWELL_ERR_RANGE.
+cudaError_t launch_to_f16(const void *const src[3], void *const dst[3], size_t elems,
+                          const Ctl *ctl, int32_t *status, cudaStream_t s);
 
 // simt_gemm.cu (fp32 path)
 cudaError_t launch_simt_gate_pack(const FwdArgs &a, cudaStream_t s);
@@ -162,7 +174,8 @@ enum KernelId {
   KID_ROWELL_PACK = 18,
   KID_ROWELL_UPDOWN = 19,
   KID_BWD_DH_GEMM = 20,
-  KID_COUNT = 21
+  KID_TO_F16 = 21,
+  KID_COUNT = 22
 };
 // Record a timing event after `launches` kernel launches of component `id`
 // (no-op unless enabled).

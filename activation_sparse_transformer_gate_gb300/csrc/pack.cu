@@ -6,6 +6,8 @@
 // section 2.A: TwELL keeps K (index, value) slots per (row, tile of C
 // columns); section 2.A hybrid format: rows that overflow their slots go to a
 // dense backup matrix; section 2.B: conversion from TwELL to the hybrid form.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -235,7 +237,7 @@ cudaError_t launch_overflow_compact(const twell_t &tw, const Workspace *ws, floa
     launch_k(overflow_scan_kernel, 1, 1024, 0, s, ws->ovf_bits, tw.T, tw.ovf_cap,
              write_user ? tw.ovf_rows : nullptr, write_user ? tw.n_ovf : nullptr, tw.status,
              ws->ctl, ws->rows, ws->pos, tw.F, dense_switch, dense_density, slot_parts, n_parts,
-             dh_density, ws->rp > 0 ? ws->rp : tw.T);
+             dh_density, ws->dense_bufs ? ws->rp : 0);
     return cudaGetLastError();
   }
   launch_k(overflow_compact_kernel, 1, 1024, 0, s, tw.nnz, tw.T, tw.F / tw.C, tw.K, tw.ovf_cap,
@@ -450,39 +452,88 @@ cudaError_t launch_fill_u_slots(const FwdArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Eight bf16 values (one 16-byte vector) as fp16; sets *big when one of them
+// lies beyond the fp16 range (the conversion is exact inside it, down to
+// 2^-14, and keeps fp16's subnormal spacing below).
+__device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 &v, bool &big) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf_lo(w[i]), b = bf_hi(w[i]);
+    big |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;
+    __half2 h = __floats2half2_rn(a, b);
+    o[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Backward, dense-path rows (all rows in all-dense mode, else the overflow
-// rows when they take the GEMMs): zero the dbg partial sums, and in the
-// overflow-row case gather the dy and x rows (zero rows up to the next
-// multiple of 128).  One launch, idle when there are no such rows.
+// rows when they take the GEMMs): zero the dbg partial sums, and copy the
+// rows' dy and x as fp16 (the operands of the fp16 tensor-core GEMMs; in
+// all-dense mode row m is token m), zero rows up to the next multiple of 128.
+// One launch, idle when there are no such rows.
 __global__ void bwd_prep_rows_kernel(const Ctl *__restrict__ ctl, const int32_t *__restrict__ rows,
                                      const uint4 *__restrict__ dy, const uint4 *__restrict__ x,
                                      uint4 *__restrict__ dyg, uint4 *__restrict__ xg,
-                                     float *__restrict__ dbg_r, int row_vecs, int F) {
+                                     float *__restrict__ dbg_r, int row_vecs, int F,
+                                     int32_t *status) {
   pdl_begin();
   const int n = ctl->n_rows;
   if (n == 0) return;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < F; i += gridDim.x * blockDim.x)
     dbg_r[i] = 0.f;
-  if (ctl->dense) return;  // the GEMMs read dy and x in place
+  const bool dense = ctl->dense != 0;
   const int npad = (n + 127) / 128 * 128;
+  bool big = false;
   for (int m = blockIdx.x; m < npad; m += gridDim.x) {
     uint4 *a = dyg + (size_t)m * row_vecs, *b = xg + (size_t)m * row_vecs;
     if (m < n) {
-      const uint4 *sa = dy + (size_t)rows[m] * row_vecs, *sb = x + (size_t)rows[m] * row_vecs;
+      const int t = dense ? m : rows[m];
+      const uint4 *sa = dy + (size_t)t * row_vecs, *sb = x + (size_t)t * row_vecs;
       for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
-        a[v] = sa[v];
-        b[v] = sb[v];
+        a[v] = bf16x8_to_f16(sa[v], big);
+        b[v] = bf16x8_to_f16(sb[v], big);
       }
     } else {
       for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) a[v] = b[v] = make_uint4(0, 0, 0, 0);
     }
   }
+  if (big) set_status(status, TWELL_ERR_RANGE);
+}
+
+// fp16 copies of up to three bf16 matrices of `vecs` 16-byte vectors each,
+// when the dense path has rows (else every CTA returns at once).
+__global__ void to_f16_kernel(const uint4 *__restrict__ s0, uint4 *__restrict__ d0,
+                              const uint4 *__restrict__ s1, uint4 *__restrict__ d1,
+                              const uint4 *__restrict__ s2, uint4 *__restrict__ d2, size_t vecs,
+                              const Ctl *__restrict__ ctl, int32_t *status) {
+  pdl_begin();
+  if (ctl->n_rows == 0) return;
+  bool big = false;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += stride) {
+    d0[i] = bf16x8_to_f16(s0[i], big);
+    if (s1) d1[i] = bf16x8_to_f16(s1[i], big);
+    if (s2) d2[i] = bf16x8_to_f16(s2[i], big);
+  }
+  if (big) set_status(status, TWELL_ERR_RANGE);
+}
+
+cudaError_t launch_to_f16(const void *const src[3], void *const dst[3], size_t elems,
+                          const Ctl *ctl, int32_t *status, cudaStream_t s) {
+  // (usually idle: one wave that returns when no row takes the dense path)
+  launch_k(to_f16_kernel, 4 * num_sms(), 256, 0, s, (const uint4 *)src[0], (uint4 *)dst[0],
+           (const uint4 *)src[1], (uint4 *)dst[1], (const uint4 *)src[2], (uint4 *)dst[2],
+           elems / 8, ctl, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s) {
   const int blocks = a.T < 2 * num_sms() ? a.T : 2 * num_sms();
   launch_k(bwd_prep_rows_kernel, blocks, 256, 0, s, a.ws.ctl, a.ws.rows, (const uint4 *)a.dy,
-           (const uint4 *)a.x, (uint4 *)a.ws.dyg, (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F);
+           (const uint4 *)a.x, (uint4 *)a.ws.dyg, (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F,
+           a.tw.status);
   return cudaGetLastError();
 }
 

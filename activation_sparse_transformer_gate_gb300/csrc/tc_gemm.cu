@@ -5,17 +5,27 @@
 //              also u and h = g*u) -> h rows (+ g_fb / u_fb rows of overflow
 //              rows); the plain FFN's dense rows                (dense rows)
 //   EPI_DOWN : y[tok] = h Wd, Wd read MN-major straight from [F][D]   (dense rows)
+//              (gated FFN: h and a copy of Wd in fp16, see below)
 //   EPI_U    : the gated FFN's dense rows: B = Wu only, g read back from the
 //              TwELL slots / wide tiles, h = g*u (+ u at the slots)   (dense rows)
-//   EPI_DH   : dh = dy Wd^T + lambda sign(h) -> dz, du, h rows (bf16 hi +
-//              lo parts) and column sums of dz                    (bwd rows)
+//   EPI_DH   : dh = dy Wd^T + lambda sign(h) -> dz, du, h rows (fp16) and
+//              column sums of dz                                  (bwd rows)
 //   EPI_DHS  : the same dh for the rows left to the gathers, read only at the
 //              TwELL slots (and the overflow rows' backup-row columns) ->
 //              fp32 dz, du, h where the gather SDDMM puts them   (bwd, sparse)
-//   EPI_DX   : dx[tok] = dz Wg + du Wu (K ranges over the hi and lo parts,
-//              B MN-major)                                        (bwd rows)
-//   EPI_DW   : dW = A^T B with A, B both MN-major (token axis = K, hi and lo
-//              parts of A), fp32 rows stored or added             (bwd rows)
+//   EPI_DX   : dx[tok] = dz Wg + du Wu (two K ranges, B MN-major) (bwd rows)
+//   EPI_DW   : dW = A^T B with A, B both MN-major (token axis = K), fp32
+//              rows stored or added                               (bwd rows)
+//
+// Precision of the dense-path rows.  Their activations h = g u and their
+// gradients dz, du, h are formed in fp32 and enter the tensor cores as MMA
+// operands.  One bf16 rounding of them would give output errors of 1-5% of
+// rms at the largest elements (where a few large activations dominate a
+// row), so these GEMMs take fp16 operands (kind::f16 with F16 A and B): 2^-11
+// relative rounding, about an eighth of that error, at the cost of one GEMM.
+// The other operand (W_down, W_gate, W_up, x, dy: bf16) is copied to fp16,
+// which is exact for values of magnitude within [2^-14, 65504]; larger ones
+// would not be representable (TWELL_ERR_RANGE).
 //   EPI_F32  : plain fp32 C = A B^T, A B or A^T B (test hook)
 //
 // "Sparser, Faster, Lighter Transformer Language Models", technical summary
@@ -39,6 +49,7 @@
 // returns.  The four epilogue warps take the outcome of each wait together,
 // so they leave their loop at the same tile.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -145,10 +156,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: D=f32, A=B=bf16, A and B each K- or
-// MN-major (bits 15 and 16), N>>3 at bit 17, M>>4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+// Instruction descriptor, kind::f16: D=f32 (bits 4-5), A and B both bf16
+// (bits 7-9 and 10-12 = 1) or both fp16 (= 0), A and B each K- or MN-major
+// (bits 15 and 16), N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -246,21 +259,22 @@ __device__ __forceinline__ unsigned short slot_val(const uint32_t (&vw)[16], int
   return (unsigned short)(vw[k >> 1] >> (16 * (k & 1)));
 }
 
-// 32 fp32 values as bf16 hi (RNE) and lo = bf16(v - hi) parts, 64 bytes each.
-__device__ __forceinline__ void store_hi_lo(bf16 *hi, bf16 *lo, const float (&v)[32]) {
-  uint32_t hw[16], lw[16];
+// 32 fp32 values as fp16 (round to nearest even), 64 bytes; a value beyond
+// the fp16 range records TWELL_ERR_RANGE.
+__device__ __forceinline__ void store_f16x32(__half *dst, const float (&v)[32], int32_t *status) {
+  uint32_t w[16];
+  bool big = false;
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
-    const uint32_t hp = pack_bf2(v[i], v[i + 1]);
-    hw[i / 2] = hp;
-    lw[i / 2] = pack_bf2(v[i] - bf_lo(hp), v[i + 1] - bf_hi(hp));
+    big |= fabsf(v[i]) > 65504.f || fabsf(v[i + 1]) > 65504.f;
+    __half2 h = __floats2half2_rn(v[i], v[i + 1]);
+    w[i / 2] = *reinterpret_cast<uint32_t *>(&h);
   }
-  uint4 *h4 = (uint4 *)hi, *l4 = (uint4 *)lo;
+  if (big) set_status(status, TWELL_ERR_RANGE);
+  uint4 *d4 = (uint4 *)dst;
 #pragma unroll
-  for (int v4 = 0; v4 < 4; ++v4) {
-    h4[v4] = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
-    l4[v4] = make_uint4(lw[4 * v4], lw[4 * v4 + 1], lw[4 * v4 + 2], lw[4 * v4 + 3]);
-  }
+  for (int v4 = 0; v4 < 4; ++v4)
+    d4[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
 }
 
 __device__ __forceinline__ void epi_bar() {  // named barrier of the 4 epilogue warps
@@ -299,7 +313,7 @@ struct TcParams {
   const Ctl *ctl;          // dense-path control (EPI_GU / EPI_DOWN), else null
   int N, Kdim;             // output columns, contraction length
   int Tn, F, D, C, Kslots, cap, gated, train;
-  int Tp;                  // rows of a hi part (the dense-path row buffers' rows)
+  int Tp;                  // rows of the dense-path row buffers
   long long l2_bytes;      // L2 size of the device (tile order)
   const float *bg, *rb;
   const int32_t *rows, *pos;
@@ -311,7 +325,7 @@ struct TcParams {
   bf16 *wide;
   float *out;              // EPI_F32, EPI_DW
   float lambda;            // EPI_DH: L1 coefficient
-  bf16 *dz2, *du2, *h2;    // EPI_DH outputs, [2 Tp][F]: hi rows, then lo rows
+  __half *dz2, *du2, *h2;  // EPI_DH outputs, [Tp][F] fp16
   float *dbg_r;            // EPI_DH: column sums of dz (zeroed before); EPI_DW: added to dbg_out
   float *dbg_out;          // EPI_DW: dbg (added from dbg_r with the W_gate problem)
   float *outq[3];          // EPI_DW: the fp32 output of each problem (dWg, [dWu,] dWd)
@@ -495,7 +509,7 @@ struct Cfg {
 
 }  // namespace
 
-template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false, bool F16 = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
   pdl_begin();
@@ -524,17 +538,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
   const int NQ = EPI == EPI_DW ? p.nq : 1;  // independent problems of one shape
   const int tiles_q = m_blocks * n_blocks;
   const int num_tiles = NQ * tiles_q;
-  // The backward GEMMs contract over several K ranges of KT1 k-blocks each:
-  // an operand rounded to bf16 is split into hi + lo parts (rows m and
-  // p.Tp + m of its buffer), each multiplied by the same other operand.
-  //   EPI_DX: dz_hi Wg, dz_lo Wg, du_hi Wu, du_lo Wu (plain FFN: the first two)
-  //   EPI_DW: A_hi B, A_lo B
+  // The dense-path dx GEMM contracts over two K ranges of KT1 k-blocks:
+  // dz with W_gate, then du with W_up (the plain FFN: the first only).
   const int Kd = p.k_dev ? *p.k_dev : p.Kdim;
   const int KT1 = (Kd + BK - 1) / BK;
-  //   EPI_DOWN (gated): h_hi Wd, h_lo Wd (h = g u formed in fp32; the plain
-  //   FFN's h = g is exact in bf16: one range)
-  const int NR = EPI == EPI_DX ? (p.gated ? 4 : 2)
-                               : (EPI == EPI_DW || (EPI == EPI_DOWN && p.gated) ? 2 : 1);
+  const int NR = (EPI == EPI_DX && p.gated) ? 2 : 1;
   const int KT = NR * KT1;
   // Tile order.  When B is larger than half of L2, groups of gm M-blocks,
   // and within a group all N-blocks with the M-blocks innermost: the CTAs in
@@ -603,20 +611,18 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           mbar_expect_tx(fb, CF::STAGE_BYTES);
           const int r = NR > 1 ? kt / KT1 : 0;   // K range
           const int kc = (kt - r * KT1) * BK;     // k within the range
-          const int lo = (r & 1) ? p.Tp : 0;      // row offset of a lo part
-          const bool second = EPI == EPI_DX && r >= 2;
+          const bool second = EPI == EPI_DX && r == 1;
           const CUtensorMap *amap = second ? &maps.a[1] : aq;
           if (A_MN) {
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(sbase + i * (64 * BK * 2), amap, mb * BM + 64 * i, kc + lo, fb);
+              tma_load_2d(sbase + i * (64 * BK * 2), amap, mb * BM + 64 * i, kc, fb);
           } else {
-            tma_load_2d(sbase, amap, kc, mb * BM + lo, fb);
+            tma_load_2d(sbase, amap, kc, mb * BM, fb);
           }
 #pragma unroll
           for (int op = 0; op < NB; ++op) {
-            const CUtensorMap *bm =
-                &maps.b[bq + ((op == 1 || second || (EPI == EPI_DW && dense_all)) ? 1 : 0)];
+            const CUtensorMap *bm = &maps.b[bq + ((op == 1 || second) ? 1 : 0)];
             const uint32_t bbase = sbase + CF::A_BYTES + op * CF::B_BYTES;
             if (B_MN) {
 #pragma unroll
@@ -648,7 +654,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN, F16);
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
@@ -957,13 +963,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
               uw[i / 2] = pack_bf2(zu[i], zu[i + 1]);
             }
           }
-          // h = g u in fp32 as bf16 hi + lo rows (rows m and Tp + m): the
-          // down GEMM contracts over both, so h enters it to ~2^-17
-          // relative, as on the gather path (one bf16 rounding of h alone
-          // gives output errors of several percent of rms where a row's
-          // output is dominated by a few large activations)
-          store_hi_lo(p.h + (size_t)m * p.F + n0 + c0, p.h + ((size_t)p.Tp + m) * p.F + n0 + c0,
-                      hv);
+          // h = g u (fp32) as the fp16 operand of the down GEMM
+          store_f16x32((__half *)p.h + (size_t)m * p.F + n0 + c0, hv, p.status);
           if (dense_all && p.train && ps < 0) {
             // all-dense training: u at this row's slots in the block (staged
             // in shared memory to be picked by slot column)
@@ -996,11 +997,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         // the forward saved: the dense backup rows of an overflow row, else
         // the TwELL slots (g) and u at the slots, loaded once per tile with
         // vector loads.  dz, du and h = g u are computed in fp32 and stored
-        // as bf16 hi + lo parts (v = hi + lo to about 2^-17 relative: the
-        // GEMMs that take them as operands then lose no more than the fp32
-        // gather path), hi at row m and lo at row Tp + m of p.dz2 / p.du2 /
-        // p.h2.  Rows past the last one (inside this tile) are written as
-        // zeros: the weight-gradient GEMMs contract over them.
+        // as fp16 rows (the operands of the dx and weight-gradient GEMMs) at
+        // row m of p.dz2 / p.du2 / p.h2.  Rows past the last one (inside this
+        // tile) are written as zeros: the weight-gradient GEMMs contract over
+        // them.
         const int tok = tok_u;
         const int ps = ps_u;
         const int K = p.Kslots;
@@ -1012,7 +1012,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           float v[32];
           tmem_ld32(tacc + c0, v);
           if (n0 + c0 >= p.N) continue;  // uniform (F is a multiple of 32)
-          const size_t o = (size_t)m * p.F + n0 + c0, ol = o + (size_t)p.Tp * p.F;
+          const size_t o = (size_t)m * p.F + n0 + c0;
           float dz[32], du[32], hv[32];
           if (row_ok) {
             uint32_t ga[16], ua[16];  // bf16 pairs of g and u (plain FFN: u = 1)
@@ -1081,9 +1081,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dz[i] = du[i] = hv[i] = 0.f;
           }
-          store_hi_lo(p.dz2 + o, p.dz2 + ol, dz);
-          if (p.gated) store_hi_lo(p.du2 + o, p.du2 + ol, du);
-          store_hi_lo(p.h2 + o, p.h2 + ol, hv);
+          store_f16x32(p.dz2 + o, dz, p.status);
+          if (p.gated) store_f16x32(p.du2 + o, du, p.status);
+          store_f16x32(p.h2 + o, hv, p.status);
           // dbg: column sums of this warp's 32 rows by recursive halving (lane
           // l ends with column l), one atomic per column and warp
 #pragma unroll
@@ -1307,10 +1307,10 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
          CUDA_SUCCESS;
 }
 
-template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false, bool F16 = false>
 cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cudaStream_t s) {
   using CF = Cfg<BN, NB, B_MN, EPI, A_MN>;
-  auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI, A_MN>;
+  auto kern = tc_gemm_kernel<BN, NB, B_MN, EPI, A_MN, F16>;
   // once per instantiation and process (concurrent first calls from several
   // host threads are safe)
   static cudaError_t attr_err = cudaSuccess;
@@ -1327,13 +1327,13 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int max_tiles, cuda
   return cudaGetLastError();
 }
 
-template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false>
+template <int BN, int NB, bool B_MN, int EPI, bool A_MN = false, bool F16 = false>
 cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a2, const CUtensorMap &b0,
                       const CUtensorMap &b1, const TcParams &p, int max_tiles, cudaStream_t s) {
   TcMaps maps;
   maps.a[0] = a; maps.a[1] = a2; maps.a[2] = a;
   maps.b[0] = b0; maps.b[1] = b1; maps.b[2] = b0; maps.b[3] = b1;
-  return launch_tc<BN, NB, B_MN, EPI, A_MN>(maps, p, max_tiles, s);
+  return launch_tc<BN, NB, B_MN, EPI, A_MN, F16>(maps, p, max_tiles, s);
 }
 
 TcParams base_params(const FwdArgs &a) {
@@ -1404,15 +1404,16 @@ cudaError_t launch_tc_dense_gu(const FwdArgs &a, cudaStream_t s) {
   return launch_tc<128, 1, false, EPI_GU>(mxg, mx, mg, mg, p, tiles, s);
 }
 
-// Down projection of the dense-path rows: A = h rows (dense-path order; the
-// gated FFN's h as hi rows then lo rows, contracted as two K ranges),
-// B = W_down read MN-major from its neuron-major [F][D] storage.
+// Down projection of the dense-path rows: A = h rows (dense-path order),
+// B = W_down read MN-major from its neuron-major [F][D] storage.  Gated FFN:
+// h (fp32 g u) and W_down in fp16 (its copy in the workspace); plain FFN:
+// h = g, exact in bf16, against W_down itself.
 cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   // 128 x 256 output tiles (as the gate GEMM): half the A re-reads of 128 x 128
   const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   CUtensorMap mh, md;
-  if (!make_map(&mh, a.ws.h, a.F, a.gated ? 2 * Tp : Tp, 64, BM) ||
-      !make_map(&md, a.Wd, a.D, a.F, 64, 64))
+  if (!make_map(&mh, a.ws.h, a.F, Tp, 64, BM) ||
+      !make_map(&md, a.gated ? a.ws.wd16 : a.Wd, a.D, a.F, 64, 64))
     return cudaErrorInvalidValue;
   TcParams p = base_params(a);
   p.m_dev = &a.ws.ctl->n_rows;
@@ -1420,6 +1421,7 @@ cudaError_t launch_tc_dense_down(const FwdArgs &a, cudaStream_t s) {
   p.N = a.D;
   p.Kdim = a.F;
   const int tiles = ((a.T + BM - 1) / BM) * ((a.D + 255) / 256);
+  if (a.gated) return launch_tc<256, 1, true, EPI_DOWN, false, true>(mh, mh, md, md, p, tiles, s);
   return launch_tc<256, 1, true, EPI_DOWN>(mh, mh, md, md, p, tiles, s);
 }
 
@@ -1439,7 +1441,7 @@ TcParams bwd_params(const BwdArgs &a) {
   p.gated = a.gated; p.train = 1; p.rows = a.ws.rows; p.pos = a.ws.pos; p.ctl = a.ws.ctl;
   p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = (bf16 *)a.tw.val; p.uval = (bf16 *)a.tw.u_val;
   p.g_fb = (bf16 *)a.tw.g_fb; p.u_fb = (bf16 *)a.tw.u_fb;
-  p.dz2 = (bf16 *)a.ws.dzr; p.du2 = (bf16 *)a.ws.dur; p.h2 = (bf16 *)a.ws.hr;
+  p.dz2 = (__half *)a.ws.dzr; p.du2 = (__half *)a.ws.dur; p.h2 = (__half *)a.ws.hr;
   p.Tp = a.ws.rp;
   p.y = (bf16 *)a.dx; p.lambda = a.lambda; p.dbg_r = a.ws.dbg_r; p.status = a.tw.status;
   return p;
@@ -1448,18 +1450,20 @@ TcParams bwd_params(const BwdArgs &a) {
 }  // namespace
 
 // dh = dy W_down^T over the dense-path rows, then the L1 term and dz / du / h.
+// fp16 operands: the dense-path dy rows (copied by the row-preparation
+// kernel in every mode) and the workspace's fp16 copy of W_down, both exact
+// copies of the bf16 values, so dh is the bf16 product's.
 cudaError_t launch_tc_bwd_dh(const BwdArgs &a, cudaStream_t s) {
   const int Tp = a.ws.rp;  // rows of the dense-path row buffers
-  CUtensorMap mdyg, mdy, mwd;
-  if (!make_map(&mdyg, a.ws.dyg, a.D, Tp, 64, BM) || !make_map(&mdy, a.dy, a.D, a.T, 64, BM) ||
-      !make_map(&mwd, a.Wd, a.D, a.F, 64, 256))
+  CUtensorMap mdyg, mwd;
+  if (!make_map(&mdyg, a.ws.dyg, a.D, Tp, 64, BM) || !make_map(&mwd, a.ws.wd16, a.D, a.F, 64, 256))
     return cudaErrorInvalidValue;
   TcParams p = bwd_params(a);
   p.m_dev = &a.ws.ctl->n_rows;
   p.N = a.F;
   p.Kdim = a.D;
-  return launch_tc<256, 1, false, EPI_DH>(mdyg, mdy, mwd, mwd, p, (Tp / BM) * ((a.F + 255) / 256),
-                                          s);
+  return launch_tc<256, 1, false, EPI_DH, false, true>(mdyg, mdyg, mwd, mwd, p,
+                                                       (Tp / BM) * ((a.F + 255) / 256), s);
 }
 
 // dh of the rows the gathers own as one GEMM over every row, dy W_down^T
@@ -1482,37 +1486,40 @@ cudaError_t launch_tc_bwd_dh_sampled(const BwdArgs &a, cudaStream_t s) {
 }
 
 // dx[tok] = dz W_gate + du W_up over the dense-path rows (one accumulator,
-// four K ranges: the hi and lo parts of dz and du; W read MN-major from
-// [F][D]).
+// two K ranges; fp16 dz, du and the workspace's fp16 copies of W_gate,
+// W_up, read MN-major from [F][D]).
 cudaError_t launch_tc_bwd_dx(const BwdArgs &a, cudaStream_t s) {
   const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   CUtensorMap mz, mu, mwg, mwu;
-  if (!make_map(&mz, a.ws.dzr, a.F, 2 * Tp, 64, BM) ||
-      !make_map(&mu, a.ws.dur, a.F, 2 * Tp, 64, BM) || !make_map(&mwg, a.Wg, a.D, a.F, 64, 64) ||
-      !make_map(&mwu, a.gated ? a.Wu : a.Wg, a.D, a.F, 64, 64))
+  if (!make_map(&mz, a.ws.dzr, a.F, Tp, 64, BM) || !make_map(&mu, a.ws.dur, a.F, Tp, 64, BM) ||
+      !make_map(&mwg, a.ws.wg16, a.D, a.F, 64, 64) ||
+      !make_map(&mwu, a.gated ? a.ws.wu16 : a.ws.wg16, a.D, a.F, 64, 64))
     return cudaErrorInvalidValue;
   TcParams p = bwd_params(a);
   p.m_dev = &a.ws.ctl->n_rows;
   p.N = a.D;
   p.Kdim = a.F;
-  return launch_tc<256, 1, true, EPI_DX>(mz, mu, mwg, mwu, p, (Tp / BM) * ((a.D + 255) / 256), s);
+  return launch_tc<256, 1, true, EPI_DX, false, true>(mz, mu, mwg, mwu, p,
+                                                      (Tp / BM) * ((a.D + 255) / 256), s);
 }
 
 // dWg = dz^T x (+ dbg), dWu = du^T x, dWd = h^T dy over the dense-path rows:
-// both operands MN-major, the token axis is the contraction (hi and lo parts
-// of dz / du / h as two K ranges).  Stored in all-dense mode, added to the
-// gather kernel's rows otherwise.
+// both operands MN-major, the token axis is the contraction; fp16 dz, du, h
+// and the dense-path x, dy rows in fp16 (copied by the row-preparation kernel
+// in every mode).  Stored in all-dense mode, added to the gather kernel's
+// rows otherwise.
 cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s) {
   const int Tp = a.ws.rp;  // rows of the dense-path row buffers
   // problems: dWg (A = dz, B = x), [dWu (du, x),] dWd (h, dy)
   TcMaps maps;
   const void *A[3] = {a.ws.dzr, a.gated ? (const void *)a.ws.dur : a.ws.hr, a.ws.hr};
   for (int q = 0; q < 3; ++q)
-    if (!make_map(&maps.a[q], A[q], a.F, 2 * Tp, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&maps.b[0], a.ws.xg, a.D, Tp, 64, 64) || !make_map(&maps.b[1], a.x, a.D, a.T, 64, 64) ||
-      !make_map(&maps.b[2], a.ws.dyg, a.D, Tp, 64, 64) ||
-      !make_map(&maps.b[3], a.dy, a.D, a.T, 64, 64))
+    if (!make_map(&maps.a[q], A[q], a.F, Tp, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&maps.b[0], a.ws.xg, a.D, Tp, 64, 64) ||
+      !make_map(&maps.b[2], a.ws.dyg, a.D, Tp, 64, 64))
     return cudaErrorInvalidValue;
+  maps.b[1] = maps.b[0];
+  maps.b[3] = maps.b[2];
   TcParams p = bwd_params(a);
   p.k_dev = &a.ws.ctl->n_rows;
   p.M_host = a.F;
@@ -1523,7 +1530,7 @@ cudaError_t launch_tc_bwd_dw(const BwdArgs &a, cudaStream_t s) {
   p.outq[2] = a.dWd;
   p.dbg_out = a.dbg;
   const int tiles = p.nq * ((a.F + BM - 1) / BM) * ((a.D + 255) / 256);
-  return launch_tc<256, 1, true, EPI_DW, true>(maps, p, tiles, s);
+  return launch_tc<256, 1, true, EPI_DW, true, true>(maps, p, tiles, s);
 }
 
 #ifdef TWELL_TEST_HOOKS

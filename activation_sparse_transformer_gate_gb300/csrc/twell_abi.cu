@@ -65,7 +65,7 @@ static const char *kKernelNames[KID_COUNT] = {
     "bwd_slots_sddmm",      "bwd_dx_spmm",      "twell_transpose",    "bwd_dw_gather",
     "bwd_dense_dh_gemm",    "fill_u_slots",     "assemble_fb_rows",   "bwd_dense_dx_gemm",
     "bwd_dense_dw_gemm",    "bwd_prep_rows",    "rowell_pack_dense",  "rowell_updown",
-    "bwd_dh_gemm_sampled"};
+    "bwd_dh_gemm_sampled", "weights_to_f16"};
 
 Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dtype, int train,
                           int rows_cap) {
@@ -88,12 +88,24 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
   const int cap = (rows_cap <= 0 || rows_cap >= T) ? T : rows_cap;
   const size_t Rp = ((size_t)cap + 127) / 128 * 128;
   w.rp = (int)Rp;
-  w.h = take(es * 2 * Rp * F);  // gated bf16 dense path: h hi rows, then lo rows
-  w.xg = take(es * Rp * D);
+  // Below one tile of rows (and T) no row can take the dense-path GEMMs (the
+  // dispatcher sends overflow rows there from OVF_GEMM_MIN rows on): their
+  // buffers are left out.
+  w.dense_bufs = cap >= T || cap >= OVF_GEMM_MIN;
+  auto take_dense = [&](size_t bytes) -> void * { return w.dense_bufs ? take(bytes) : nullptr; };
+  w.h = take_dense(es * Rp * F);
+  w.xg = take_dense(es * Rp * D);
   w.wide = take(es * Tp * F);   // indexed by token (written for overflowing tiles)
+  if (dtype == TWELL_BF16) {    // fp16 operand copies of the dense-path GEMMs
+    w.wd16 = take_dense(2 * (size_t)F * D);
+    if (train) {
+      w.wg16 = take_dense(2 * (size_t)F * D);
+      w.wu16 = take_dense(2 * (size_t)F * D);
+    }
+  }
   if (train) {
-    w.urows = take(es * Rp * F);
-    w.dyg = take(es * Rp * D);
+    w.urows = take_dense(es * Rp * F);
+    w.dyg = take_dense(es * Rp * D);
     w.dbg_r = (float *)take(4 * (size_t)F);
     w.slot_parts = (unsigned long long *)take(8 * (size_t)SLOT_PARTS_MAX);
     const size_t slots = nt * (size_t)T * (size_t)K;
@@ -104,8 +116,8 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_e = (float4 *)take(16 * slots);
     w.col_chunk = (int32_t *)take(4 * (size_t)F * (((size_t)T + 1023) / 1024));
-    // fp32 [rp][F] rows of the gather path's overflow rows, or bf16 hi + lo
-    // rows [2 rp][F] of the tensor-core backward (never both in one call)
+    // fp32 [rp][F] rows of the gather path's overflow rows, or fp16 [rp][F]
+    // rows of the tensor-core backward (never both in one call)
     w.dzr = (float *)take(4 * Rp * F);
     w.dur = (float *)take(4 * Rp * F);
     w.hr = (float *)take(4 * Rp * F);
@@ -171,15 +183,15 @@ float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_s
 // dense_density when > 0, none when < 0, else the default crossover of the
 // measured costs.  Per active (token, neuron) the forward gathers a W_up and
 // a W_down row (4·d_model bytes at ~14 TB/s when those matrices sit in L2)
-// where the dense path does ~6·d_model flops per (token, neuron) beyond the
-// shared gate GEMM (up, and down on h's bf16 hi and lo parts) at ~1.3
-// PFLOP/s: measured crossover ~1.3% at d_model 2048 / d_ff 8192.  When
-// the gathered matrices exceed L2 the gathers slow in about the proportion
-// of rows that miss it (d_model 4096 / d_ff 14336 bf16: 235 MB, ~9.5 TB/s
-// measured, crossover ~0.65%), so the default scales by L2 / their bytes.
-// The backward gathers five rows per pair where its dense path does 11 GEMM
-// units against the forward's 3 (dz, du, h enter as hi + lo parts): its
-// crossover is (11/3) / (5/2) = 1.47 times the forward's.
+// where the dense path does ~4·d_model flops per (token, neuron) beyond the
+// shared gate GEMM (the up and down GEMMs) at ~1.3 PFLOP/s: measured
+// crossover ~1.3% at d_model 2048 / d_ff 8192.  When the gathered matrices
+// exceed L2 the gathers slow in about the proportion of rows that miss it
+// (d_model 4096 / d_ff 14336 bf16: 235 MB, ~9.5 TB/s measured, crossover
+// ~0.65%), so the default scales by L2 / their bytes.  The backward gathers
+// five rows per pair where its dense path does 6 GEMM units against the
+// forward's 2 (dh, the two dx products, the three weight gradients): its
+// crossover is (6/2) / (5/2) = 1.2 times the forward's.
 float density_of(const twell_t *tw, int D, int gated, bool backward) {
   if (tw->dense_density > 0.f) return tw->dense_density;
   if (tw->dense_density < 0.f) return -1.f;
@@ -188,7 +200,7 @@ float density_of(const twell_t *tw, int D, int gated, bool backward) {
   const double l2 = (double)l2_size();
   double d = 0.013;
   if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
-  if (backward) d *= 1.47;
+  if (backward) d *= 1.2;
   return (float)d;
 }
 
@@ -227,8 +239,10 @@ cudaError_t run_gate_and_split(FwdArgs &a, cudaStream_t s) {
   return e;
 }
 
-// Step 4: dense gate+up (+ down when write_y) over the dense-path rows.
+// Step 4: dense gate+up (+ down when write_y) over the dense-path rows (none
+// when the workspace has no dense-path buffers).
 cudaError_t run_dense_rows(FwdArgs &a, bool write_y, cudaStream_t s) {
+  if (!a.ws.dense_bufs) return cudaSuccess;
   cudaError_t e;
   if (use_tc(a.dtype)) {
     e = launch_gather_rows(a.x, a.ws.xg, a.ws, a.T, a.D, a.dtype, s);
@@ -238,6 +252,13 @@ cudaError_t run_dense_rows(FwdArgs &a, bool write_y, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     prof_mark(KID_DENSE_GU, s);
     if (!write_y) return e;
+    if (a.gated) {  // the down GEMM's fp16 operand copy of W_down
+      const void *src[3] = {a.Wd, nullptr, nullptr};
+      void *const dst[3] = {a.ws.wd16, nullptr, nullptr};
+      e = launch_to_f16(src, dst, (size_t)a.F * (size_t)a.D, a.ws.ctl, a.tw.status, s);
+      if (e != cudaSuccess) return e;
+      prof_mark(KID_TO_F16, s);
+    }
     e = launch_tc_dense_down(a, s);
     prof_mark(KID_DENSE_DOWN, s);
     return e;
@@ -365,7 +386,7 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
   }
   // all-dense training: u at the slots of non-overflow rows (the tensor-core
   // up GEMM writes them in its epilogue)
-  if (e == cudaSuccess && a.train && a.gated && !use_tc(a.dtype)) {
+  if (e == cudaSuccess && a.train && a.gated && !use_tc(a.dtype) && a.ws.dense_bufs) {
     e = launch_fill_u_slots(a, s);
     prof_mark(KID_FILL_U, s);
   }

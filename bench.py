@@ -550,9 +550,9 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
     """Achieved rate of each kernel from its algorithmic work per launch:
     bytes for the gather kernels (rows gathered + rows streamed + TwELL),
     flops for the gate GEMM and for the dense-path GEMMs (rows_f / rows_b
-    rows of the forward / backward; the backward's dx and dW contractions
-    take dz, du, h as hi + lo parts, counted as executed).  See the design
-    notes for the per-unit figures."""
+    rows of the forward / backward; fp16 operands, one GEMM per product),
+    bytes for the fp16 weight copies of the dense path.  See the design notes
+    for the per-unit figures."""
     peaks = load_peaks()
     D, F, T, K = w.D, w.F, w.T, w.K
     es = 2 if w.dtype == "bf16" else 4
@@ -595,10 +595,15 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
     wrk = {k: v for k, v in wrk.items() if v[1] > 0}
     for k, rows, mult in (("dense_rows_gate_up", rows_f, 1), ("dense_rows_down", rows_f, 1),
                           ("bwd_dense_dh_gemm", rows_b, 1),
-                          ("bwd_dense_dx_gemm", rows_b, 4 if w.gated else 2),
-                          ("bwd_dense_dw_gemm", rows_b, 2 * ng)):
+                          ("bwd_dense_dx_gemm", rows_b, 2 if w.gated else 1),
+                          ("bwd_dense_dw_gemm", rows_b, ng)):
         if rows > 0:
             wrk[k] = ("tensor", 2.0 * mult * rows * D * F)
+    # fp16 copies of the weights the dense-path GEMMs take (read bf16, write
+    # fp16): W_down in the forward (gated), W_down, W_gate (, W_up) in the backward
+    n16 = (ng if train else (1 if w.gated else 0)) if (rows_f > 0 or rows_b > 0) else 0
+    if n16 and es == 2:
+        wrk["weights_to_f16"] = ("hbm", n16 * F * D * 4)
     out = {}
     for k, (bound, work) in wrk.items():
         if k not in kern:

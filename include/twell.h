@@ -79,7 +79,10 @@ typedef enum {
   TWELL_ERR_CUDA = -7,       /* a CUDA runtime/driver call failed            */
   TWELL_ERR_WORKSPACE = -8,  /* workspace NULL, misaligned or too small      */
   TWELL_ERR_UNSUPPORTED = -9,/* valid request this build does not implement  */
-  TWELL_ERR_STATIC_LIMIT = -10 /* size above a fixed static-scratch maximum   */
+  TWELL_ERR_STATIC_LIMIT = -10,/* size above a fixed static-scratch maximum   */
+  TWELL_ERR_RANGE = -11      /* device: a dense-path value beyond the fp16
+                                range (|v| > 65504) of the tensor-core
+                                operands of the dense-path rows            */
 } twell_status;
 
 typedef enum { TWELL_F32 = 0, TWELL_BF16 = 1 } twell_dtype;
@@ -108,7 +111,7 @@ typedef struct {
                              gathers cost more than dense GEMMs.  0 selects
                              the measured crossover: 0.013 when the gathered
                              weights (W_up + W_down) fit in L2, scaled by
-                             L2 / their bytes when they do not, and 1.47x
+                             L2 / their bytes when they do not, and 1.2x
                              that in the backward; < 0 disables this test.
                              The backward applies the same rules to the
                              saved TwELL.                                    */

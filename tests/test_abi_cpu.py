@@ -167,10 +167,25 @@ def test_workspace_size_with_a_dense_row_cap(lib):
     assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 4096) == full
     assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 9999) == full
     capped = tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 256)
-    # per dense row: h hi + lo (2 x 2F), u rows (2F), dz/du/h rows (3 x 4F) bytes, x and dy rows
-    per_row = 2 * 2 * 8192 + 2 * 8192 + 3 * 4 * 8192 + 2 * 2 * 2048
+    # per dense row: h (2F), u rows (2F), dz/du/h rows (3 x 4F) bytes, x and dy rows
+    per_row = 2 * 8192 + 2 * 8192 + 3 * 4 * 8192 + 2 * 2 * 2048
     assert full - capped == (4096 - 256) * per_row
     assert capped < full / 3
     # rounded up to whole 128-row tiles
     assert (tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 200) ==
             capped)
+
+
+def test_workspace_without_dense_path_rows(lib):
+    """A cap below one 128-row tile admits no dense-path row: the workspace
+    then holds no dense-path GEMM buffers or fp16 weight copies, only the
+    gather path's overflow-row arrays (128 rows)."""
+    T, D, F = 4096, 2048, 8192
+    small = tw.twell_workspace_size_rows(T, D, F, 128, 8, tw.TWELL_BF16, 1, 64)
+    tile = tw.twell_workspace_size_rows(T, D, F, 128, 8, tw.TWELL_BF16, 1, 128)
+    dense_row_bytes = 128 * (2 * F + 2 * F + 2 * D + 2 * D)  # h, u rows, x and dy rows
+    f16_copies = 3 * 2 * F * D
+    assert tile - small == dense_row_bytes + f16_copies
+    # T below one tile: every row may run densely, the buffers are kept
+    assert (tw.twell_workspace_size_rows(100, D, F, 128, 8, tw.TWELL_BF16, 1, 100) ==
+            tw.twell_workspace_size(100, D, F, 128, 8, tw.TWELL_BF16, 1))

@@ -1,13 +1,15 @@
 """GPU parity of whole training steps at the pages' larger workload sizes,
 through the C ABI, against the CPU oracle.
 
-* d_model 4096 / d_ff 14336, T = 8192 (the sparsity sweep's shapes) in each
-  regime the dispatcher chooses with its default thresholds:
-    - bias -2.58, K = 8 (~0.5% active): gathers forward and backward, dh from
-      the gather SDDMM;
-    - bias -2.33, K = 8 (~1% active): the forward runs every row densely on
-      the tensor cores, the backward gathers with dh from the tensor-core
-      GEMM read at the slots;
+* d_model 4096 / d_ff 14336, T = 8192 (the sparsity sweep's shapes) in the
+  dispatcher's regimes:
+    - bias -2.58, K = 8 (~0.5% active, default thresholds): gathers forward
+      and backward, dh from the gather SDDMM;
+    - bias -2.33, K = 8 (~1% active, default thresholds): every row dense,
+      forward and backward (the fp16 tensor-core path);
+    - the same with the backward's density test off: the forward runs every
+      row densely, the backward gathers with dh from the tensor-core GEMM
+      read at the slots;
     - bias -1.64, K = 16 (~5% active): every row dense, forward and backward.
 * T = 16384 with dense leading tokens (16 of every 1024 at ~20% active):
   the hot rows overflow into the dense backup on the forward and run on the
@@ -77,20 +79,23 @@ def check_y(a, w, g, rows):
 
 
 REGIMES = {
-    # name: (bias, K, forward all-dense, backward all-dense, dh GEMM, full dbg)
-    "0.5pct_gathers": (-2.58, 8, 0, 0, 0, False),
-    "1pct_dense_fwd_gather_bwd": (-2.33, 8, 1, 0, 1, True),
-    "5pct_all_dense": (-1.64, 16, 1, 1, 0, False),
+    # name: (bias, K, backward density threshold (None: the forward's),
+    #        forward all-dense, backward all-dense, dh GEMM, full dbg)
+    "0.5pct_gathers": (-2.58, 8, None, 0, 0, 0, False),
+    "1pct_all_dense": (-2.33, 8, None, 1, 1, 0, False),
+    "1pct_dense_fwd_gather_bwd": (-2.33, 8, -1.0, 1, 0, 1, True),
+    "5pct_all_dense": (-1.64, 16, None, 1, 1, 0, False),
 }
 
 
 @pytest.mark.parametrize("regime", sorted(REGIMES))
 def test_config4_training_step(regime):
-    bias, K, fwd_dense, bwd_dense, dh_gemm, full_dbg = REGIMES[regime]
+    bias, K, bwd_dd, fwd_dense, bwd_dense, dh_gemm, full_dbg = REGIMES[regime]
     w = synth.scaled(synth.config4(bias, K), lam=1e-4, train=True)
     a = synth.generate(w)
     out = {}
-    g = run_train(a, w, w.lam, dense_density=0.0, dh_density=0.0, out=out, keep_twell=True)
+    g = run_train(a, w, w.lam, dense_density=0.0, dh_density=0.0, out=out, keep_twell=True,
+                  bwd_dense_density=bwd_dd)
     assert g["code"] == 0
     assert ctl_fields(out["ctl"])[1] == fwd_dense
     assert ctl_fields(out["ctl_bwd"])[1] == bwd_dense

@@ -310,7 +310,7 @@ def shifted(t, elems):
 
 
 def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0, dh_density=-1.0,
-              keep_twell=False):
+              keep_twell=False, bwd_dense_density=None):
     """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
     the density test of the dispatcher off, so that moderately dense test
     workloads still run the gather kernels; dh_density < 0 keeps dh on the
@@ -318,7 +318,9 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0,
     density; 0: the dispatcher's default); out (dict) receives the
     workspace's control block after the forward ("ctl") and after the
     backward ("ctl_bwd").  keep_twell: also return the saved TwELL (idx, nnz,
-    the overflow rows and their dense backup rows) for activity checks."""
+    the overflow rows and their dense backup rows) for activity checks.
+    bwd_dense_density: the backward's own density threshold (the twell_t is
+    passed per call), else the forward's."""
     import torch
     import activation_sparse_transformer_gate_gb300 as tw
     T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
@@ -339,6 +341,8 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0,
     dWu = torch.full_like(dWg, float("nan")) if d["Wu"] is not None else None
     dWd = torch.full_like(dWg, float("nan"))
     dbg = torch.full((F,), float("nan"), dtype=torch.float32, device="cuda")
+    if bwd_dense_density is not None:
+        bufs.t.dense_density = float(bwd_dense_density)
     tw.twell_ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], bufs.t, d["dy"], lam, D, dx, dWg, dbg,
                           dWu, dWd, ws, nws)
     if out is not None:
