@@ -53,6 +53,7 @@ class twell_t(ctypes.Structure):
         ("status", ctypes.c_void_p), ("dense_switch", ctypes.c_float),
         ("dense_density", ctypes.c_float), ("dh_density", ctypes.c_float),
         ("dense_rows_cap", ctypes.c_int32),
+        ("gather_passes", ctypes.c_int32),
     ]
 
 
@@ -185,7 +186,8 @@ class TwellBuffers:
 
     def __init__(self, T: int, F: int, C: int, K: int, dtype: int, ovf_cap: Optional[int] = None,
                  train: bool = False, device="cuda", dense_switch: float = 0.0,
-                 dense_density: float = 0.0, dh_density: float = 0.0, dense_rows_cap: int = 0):
+                 dense_density: float = 0.0, dh_density: float = 0.0, dense_rows_cap: int = 0,
+                 gather_passes: int = 0):
         import torch
         tdt = torch.bfloat16 if dtype == TWELL_BF16 else torch.float32
         nt = F // C
@@ -205,7 +207,8 @@ class TwellBuffers:
                          ovf_cap=cap, g_fb=_ptr(self.g_fb), u_val=_ptr(self.u_val),
                          u_fb=_ptr(self.u_fb), status=_ptr(self.status),
                          dense_switch=float(dense_switch), dense_density=float(dense_density),
-                         dh_density=float(dh_density), dense_rows_cap=int(dense_rows_cap))
+                         dh_density=float(dh_density), dense_rows_cap=int(dense_rows_cap),
+                         gather_passes=int(gather_passes))
 
 
 class RowEllBuffers:

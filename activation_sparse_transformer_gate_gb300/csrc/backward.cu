@@ -50,6 +50,7 @@ struct BParams {
   void *dx;
   float *dWg, *dbg, *dWu, *dWd;
   int gemm_rows;             // 1: the dense-path rows go through the tensor-core GEMMs
+  int v0, nvp;               // dx / dW gathers: this pass's columns, in 16-byte vectors
   int32_t *status;
 };
 
@@ -335,7 +336,9 @@ __global__ void __launch_bounds__(DH_WARPS * 32, U >= 8 ? 2 : (U >= 4 ? 3 : 4))
 // ---------------------------------------------------------------------------
 // 2b. Per-token dx SpMM (dense x hybrid): dx_t = sum over active pairs of
 // dz W_gate[n] + du W_up[n].  No reductions, no barriers in the pair loop;
-// the working set is W_gate and W_up.
+// the working set is W_gate and W_up, or the column range [v0, v0 + nvp)
+// of both when the launch is split into column passes (each element of dx
+// sums the same products in the same order either way).
 template <class T, int VPT, int NB, int NTH>
 __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   pdl_begin();
@@ -350,7 +353,8 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
 
   const int t = blockIdx.x, tid = threadIdx.x;
   const int nt = p.F / p.C;
-  const int NV = p.D / EV;
+  const int NV = p.D / EV;             // row stride
+  const int v0 = p.v0, NP = p.nvp;     // this pass's vectors of each row
   const int ps = p.pos[t];
   if (ps >= p.cap || gemm_row(p, ps)) return;
   float2 dxg[VPT][EV / 2], dxu[VPT][EV / 2];  // two accumulator chains
@@ -358,7 +362,8 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
   for (int v = 0; v < VPT; ++v)
 #pragma unroll
     for (int e = 0; e < EV / 2; ++e) dxg[v][e] = dxu[v][e] = make_float2(0.f, 0.f);
-  const uint4 *Wg4 = (const uint4 *)p.Wg, *Wu4 = (const uint4 *)p.Wu;
+  const uint4 *Wg4 = (const uint4 *)p.Wg + v0;
+  const uint4 *Wu4 = p.gated ? (const uint4 *)p.Wu + v0 : nullptr;
   const PairSource<T> src = bwd_source<T>(p, t, ps);
   int group = LIST_CAP / (ps >= 0 ? p.C : p.K);
   if (group > (int)blockDim.x) group = blockDim.x;
@@ -380,11 +385,11 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
       const int nb = P - b0 < NB ? P - b0 : NB;
       uint4 wg[NB][VPT], wu[NB][VPT];
       if (NTH > 0 && nb == NB) {
-        gather8<T, VPT, NB, NTH>(Wg4, s_n, b0, nb, NV, wg);
-        if (p.gated) gather8<T, VPT, NB, NTH>(Wu4, s_n, b0, nb, NV, wu);
+        gather8<T, VPT, NB, NTH>(Wg4, s_n, b0, nb, NV, NP, wg);
+        if (p.gated) gather8<T, VPT, NB, NTH>(Wu4, s_n, b0, nb, NV, NP, wu);
       } else {
-        gather8<T, VPT, NB>(Wg4, s_n, b0, nb, NV, wg);
-        if (p.gated) gather8<T, VPT, NB>(Wu4, s_n, b0, nb, NV, wu);
+        gather8<T, VPT, NB>(Wg4, s_n, b0, nb, NV, NP, wg);
+        if (p.gated) gather8<T, VPT, NB>(Wu4, s_n, b0, nb, NV, NP, wu);
       }
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
     }
     __syncthreads();
   }
-  uint4 *dxrow = (uint4 *)p.dx + (size_t)t * NV;
+  uint4 *dxrow = (uint4 *)p.dx + (size_t)t * NV + v0;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(BParams p) {
       o[2 * e] = dxg[v][e].x + dxu[v][e].x;
       o[2 * e + 1] = dxg[v][e].y + dxu[v][e].y;
     }
-    if (vi < NV) stg_stream(dxrow + vi, Vec<T>::pack(o));
+    if (vi < NP) stg_stream(dxrow + vi, Vec<T>::pack(o));
   }
 }
 
@@ -507,7 +512,10 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
 // (ascending tokens), then the overflow rows (ascending).  Rows of neurons
 // that are never active are written as zeros.  The list is staged in shared
 // memory first (one coalesced load), so each batch of PB tokens costs one
-// round trip: its x and dy rows.
+// round trip: its x and dy rows.  Split into column passes, a CTA handles
+// the columns [v0, v0 + nvp) of the neuron's rows (the working set is that
+// range of x and dy; every element sums the same products in the same
+// order); dbg is written by the first pass.
 constexpr int DW_LIST = 512;
 
 template <class T, int VPT, int NB, int NTH>
@@ -517,8 +525,9 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
   __shared__ float4 s_e[DW_LIST];
   if (p.gemm_rows && p.ctl->dense) return;  // the GEMMs write every row
   const int n = blockIdx.x, tid = threadIdx.x;
-  const int NV = p.D / EV;
-  const uint4 *x4 = (const uint4 *)p.x, *dy4 = (const uint4 *)p.dy;
+  const int NV = p.D / EV;             // row stride
+  const int v0 = p.v0, NP = p.nvp;     // this pass's vectors of each row
+  const uint4 *x4 = (const uint4 *)p.x + v0, *dy4 = (const uint4 *)p.dy + v0;
   float2 ag[VPT][EV / 2], au[VPT][EV / 2], ad[VPT][EV / 2];
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
@@ -548,7 +557,7 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 #pragma unroll
           for (int v = 0; v < VPT; ++v) {
             const int vi = tid + v * blockDim.x;
-            const bool ok = b < nb && vi < NV;
+            const bool ok = b < nb && vi < NP;
             xv[b][v] = ok ? ldg_stream(xr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
             yv[b][v] = ok ? ldg_stream(yr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
           }
@@ -576,16 +585,17 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int vi = tid + v * blockDim.x;
-      if (vi >= NV) continue;
+      if (vi >= NP) continue;
       axpy3<T>(ag[v], au[v], ad[v], r, x4[(size_t)t * NV + vi], dy4[(size_t)t * NV + vi]);
     }
   }
-  float4 *og = (float4 *)(p.dWg + (size_t)n * p.D), *od = (float4 *)(p.dWd + (size_t)n * p.D);
-  float4 *ou = p.gated ? (float4 *)(p.dWu + (size_t)n * p.D) : nullptr;
+  const size_t o0 = (size_t)n * p.D + (size_t)v0 * EV;
+  float4 *og = (float4 *)(p.dWg + o0), *od = (float4 *)(p.dWd + o0);
+  float4 *ou = p.gated ? (float4 *)(p.dWu + o0) : nullptr;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int vi = tid + v * blockDim.x;
-    if (vi >= NV) continue;
+    if (vi >= NP) continue;
 #pragma unroll
     for (int q = 0; q < EV / 4; ++q) {
       stg_stream(og + vi * (EV / 4) + q, f4bits(ag[v][2 * q], ag[v][2 * q + 1]));
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
       if (ou) stg_stream(ou + vi * (EV / 4) + q, f4bits(au[v][2 * q], au[v][2 * q + 1]));
     }
   }
-  if (tid == 0) p.dbg[n] = sb;
+  if (tid == 0 && v0 == 0) p.dbg[n] = sb;
 }
 
 // ---------------------------------------------------------------------------
@@ -642,6 +652,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // the dense-path rows' tensor-core GEMMs (when the workspace has their buffers)
   const bool gemm = tc && a.ws.dense_bufs;
   p.gemm_rows = gemm ? 1 : 0;
+  p.v0 = 0;
+  p.nvp = a.D / (bf ? 8 : 4);
 
   // 1. hybrid split of the saved activations into this workspace, with the
   // forward's dispatcher rules when the dense-path rows have GEMMs
@@ -713,10 +725,6 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   }
   const int EV = bf ? 8 : 4;
   const int NV = a.D / EV;
-  // token / neuron CTAs: each thread owns two 16-byte vectors of a row (half
-  // the per-row overhead of one), batches of 3 rows per matrix in flight
-  const int vpt = NV <= 64 ? 1 : NV <= 512 ? 2 : 4;
-  const int threads = ((NV + vpt - 1) / vpt + 31) / 32 * 32;
   const int vl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 // (the constant-offset row loads that help the SpMM kernels made this one slower)
 #define TW_DH(TT, L) launch_k(bwd_dh_kernel<TT, L, 1>, a.T, 256, 0, s, p)
@@ -753,12 +761,27 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return join3(e);
   prof_mark(KID_BWD_SLOTS, s);
-#define TW_VPT(K, TT, G, SS)                                                                   \
+  // Token / neuron CTAs over the column passes of the dx and dW gathers: each
+  // thread owns two 16-byte vectors of a row (half the per-row overhead of
+  // one), batches of 3 rows per matrix in flight.
+  const size_t es = bf ? 2 : 4;
+  const int dx_passes = gather_passes(a.tw.gather_passes, (a.gated ? 2.0 : 1.0) * a.F * a.D * es, NV);
+  const int dw_passes = gather_passes(a.tw.gather_passes, 2.0 * a.T * a.D * es, NV);
+#define TW_VPT(K, TT, G, SS, NPASS)                                                            \
   do {                                                                                         \
-    if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, SS, p);                              \
-    else if (vpt == 2 && NV == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, SS, p);              \
-    else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, SS, p);                         \
-    else launch_k(K<TT, 4, 2, 0>, G, threads, 0, SS, p);                                       \
+    for (int i_ = 0; i_ < (NPASS); ++i_) {                                                     \
+      p.v0 = (int)((long)NV * i_ / (NPASS));                                                   \
+      p.nvp = (int)((long)NV * (i_ + 1) / (NPASS)) - p.v0;                                     \
+      const int np_ = p.nvp;                                                                   \
+      const int vpt = np_ <= 64 ? 1 : np_ <= 512 ? 2 : 4;                                      \
+      const int threads = ((np_ + vpt - 1) / vpt + 31) / 32 * 32;                              \
+      if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, SS, p);                            \
+      else if (vpt == 2 && np_ == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, SS, p);           \
+      else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, SS, p);                       \
+      else launch_k(K<TT, 4, 2, 0>, G, threads, 0, SS, p);                                     \
+    }                                                                                          \
+    p.v0 = 0;                                                                                  \
+    p.nvp = NV;                                                                                \
   } while (0)
   // Steps 3-4 on s2: forked here, after dh, and joined before returning.
   if (fork) {
@@ -777,10 +800,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     return r;
   };
   auto dx_spmm = [&]() {
-    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s);
-    else TW_VPT(bwd_dx_kernel, float, a.T, s);
+    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s, dx_passes);
+    else TW_VPT(bwd_dx_kernel, float, a.T, s, dx_passes);
     const cudaError_t r = cudaGetLastError();
-    prof_mark(KID_BWD_DX, s);
+    prof_mark(KID_BWD_DX, s, dx_passes);
     return r;
   };
   // the transpose first when forked: it is short and heads the longer chain
@@ -792,10 +815,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = transpose();
   }
   if (e == cudaSuccess) {  // 4. weight gradients
-    if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw);
-    else TW_VPT(bwd_dw_kernel, float, a.F, sw);
+    if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes);
+    else TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes);
     e = cudaGetLastError();
-    prof_mark(KID_BWD_DW, sw);
+    prof_mark(KID_BWD_DW, sw, dw_passes);
   }
 #undef TW_VPT
   // 5. weight gradients of the dense-path rows (added to those of step 4;

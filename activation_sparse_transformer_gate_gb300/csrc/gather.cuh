@@ -38,24 +38,27 @@ template <> struct Vec<float> {
 
 // Gather NB rows (neurons s_n[b0 .. b0+nb)) of a [F][D] matrix: this thread's
 // 16-byte vectors of each row, as 128-bit read-only loads that skip L1.
-// NTH == 0: any block size; vectors past the row end and rows b >= nb (nb may
-// be 0) are zero.  NTH > 0: a full batch (nb == NB) of exact rows, VPT * NTH
-// vectors each, in a block of NTH threads: constant offsets, no predicates.
+// Rows are `stride` vectors apart; `len` vectors are read from each row,
+// starting at `base` (a column range of the rows: base is offset by the
+// range's first vector, len its width).  NTH == 0: any block size; vectors
+// past len and rows b >= nb (nb may be 0) are zero.  NTH > 0: a full batch
+// (nb == NB) of exact rows, len = VPT * NTH vectors each, in a block of NTH
+// threads: constant offsets, no predicates.
 template <class T, int VPT, int NB = PB, int NTH = 0>
-__device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb, int NV,
-                                        uint4 (&r)[NB][VPT]) {
+__device__ __forceinline__ void gather8(const uint4 *base, const int *s_n, int b0, int nb,
+                                        int stride, int len, uint4 (&r)[NB][VPT]) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     if (NTH > 0) {
-      const uint4 *row = base + (size_t)s_n[b0 + b] * NV + threadIdx.x;
+      const uint4 *row = base + (size_t)s_n[b0 + b] * stride + threadIdx.x;
 #pragma unroll
       for (int v = 0; v < VPT; ++v) r[b][v] = ldg_stream(row + v * NTH);
     } else {
-      const uint4 *row = base + (size_t)s_n[b < nb ? b0 + b : 0] * NV + threadIdx.x;  // b0 may lie past the list
+      const uint4 *row = base + (size_t)s_n[b < nb ? b0 + b : 0] * stride + threadIdx.x;  // b0 may lie past the list
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         const int vi = threadIdx.x + v * blockDim.x;
-        r[b][v] = (b < nb && vi < NV) ? ldg_stream(row + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+        r[b][v] = (b < nb && vi < len) ? ldg_stream(row + v * blockDim.x) : make_uint4(0, 0, 0, 0);
       }
     }
   }

@@ -27,12 +27,12 @@ struct Workspace {
   void *dyg;          // [rp][D] (training, tensor-core path): dense-path dy rows, fp16
   void *wd16, *wg16, *wu16;  // [F][D] fp16 copies of W_down (and, training, W_gate,
                       // W_up): operands of the dense-path GEMMs (bf16 only)
-  float *dbg_r;       // [F] fp32 (training): dbg of the dense-path rows
+  float *dbg_r;       // [Rp/32][F] fp32 (training): dbg of the dense-path rows per 32-row group
   unsigned long long *slot_parts;  // [SLOT_PARTS_MAX] per-block slot counts (backward)
   // backward scratch
   float *dz;          // [F/C][T][K] fp32: dz at the slots
   float *du;          // [F/C][T][K] fp32: du at the slots
-  float *hs;          // [F/C][T][K] fp32: h at the slots
+  float *hs;          // [F/C][T][K] fp32: h at the slots (backward; the forward's two passes)
   int32_t *col_ptr;   // [F+1] neuron-major (transposed) pointers
   int32_t *col_cnt;   // [F]   per-neuron counts / cursors
   float4 *col_e;      // [T*(F/C)*K] transposed entries {token (int bits), dz, du, h}
@@ -84,6 +84,22 @@ constexpr int TR_CHUNK = 1024;
 // Streaming multiprocessors and L2 bytes of the current device (queried once).
 int num_sms();
 long long l2_size();
+// Passes over a gather kernel's d_model columns (or, for the forward's
+// up/down, over its two matrices) so that each pass's gathered working set
+// stays in L2.  requested > 0: that many (at most nv, the row's 16-byte
+// vectors); 0: the fewest powers of two up to GATHER_MAX_PASSES whose share
+// of set_bytes fits in GATHER_L2_SHARE of L2.  Measured on GB300 (random
+// rows, 575k gathers): 18.3 TB/s from one 34 MB matrix, 15.7 TB/s from one
+// 117 MB matrix, 11.0 TB/s from two 117 MB matrices read together.  At
+// d_model 4096 / d_ff 14336 (W_gate + W_up 235 MB, x + dy 134 MB at 8192
+// tokens) two passes beat one (dx SpMM 1.03 -> 0.68 ms, dW 1.02 -> 0.74 ms,
+// although x + dy is just below the 135.5 MB L2: the kernels also stream
+// other data through it) and four (1.03, 0.84 ms: the per-pass list
+// building and the narrower CTAs cost more than the smaller working set
+// saves).
+constexpr double GATHER_L2_SHARE = 0.9;
+constexpr int GATHER_MAX_PASSES = 4;
+int gather_passes(int requested, double set_bytes, int nv);
 
 cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // Hybrid split.  With a workspace: reads the overflow-row bitmap (which must
@@ -122,8 +138,8 @@ cudaError_t launch_copy_fb_rows(const void *H, const twell_t &tw, cudaStream_t s
 // of 128 (dst holds T rounded up to 128 rows).
 cudaError_t launch_gather_rows(const void *src, void *dst, const Workspace &ws, int T, int D,
                                int dtype, cudaStream_t s);
-// Backward, dense-path rows (bf16): zeroes ws.dbg_r and copies the dy and x
-// rows of the dense-path rows (every row in all-dense mode) into ws.dyg /
+// Backward, dense-path rows (bf16): copies the dy and x rows of the
+// dense-path rows (every row in all-dense mode) into ws.dyg /
 // ws.xg as fp16.
 cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s);
 // fp16 copies of up to three bf16 [F][D] matrices (src[i] -> dst[i], null
@@ -191,7 +207,7 @@ cudaError_t launch_rowell_updown(const void *x, const void *Wu, const void *Wd, 
                                  const int32_t *nnz, void *y, cudaStream_t s);
 
 // updown.cu
-cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s, int *launches = nullptr);
 
 // backward.cu
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s);

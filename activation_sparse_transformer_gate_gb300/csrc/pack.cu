@@ -469,20 +469,16 @@ __device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 &v, bool &big) {
 }
 
 // Backward, dense-path rows (all rows in all-dense mode, else the overflow
-// rows when they take the GEMMs): zero the dbg partial sums, and copy the
-// rows' dy and x as fp16 (the operands of the fp16 tensor-core GEMMs; in
+// rows when they take the GEMMs): copy the rows' dy and x as fp16 (the operands of the fp16 tensor-core GEMMs; in
 // all-dense mode row m is token m), zero rows up to the next multiple of 128.
 // One launch, idle when there are no such rows.
 __global__ void bwd_prep_rows_kernel(const Ctl *__restrict__ ctl, const int32_t *__restrict__ rows,
                                      const uint4 *__restrict__ dy, const uint4 *__restrict__ x,
                                      uint4 *__restrict__ dyg, uint4 *__restrict__ xg,
-                                     float *__restrict__ dbg_r, int row_vecs, int F,
-                                     int32_t *status) {
+                                     int row_vecs, int32_t *status) {
   pdl_begin();
   const int n = ctl->n_rows;
   if (n == 0) return;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < F; i += gridDim.x * blockDim.x)
-    dbg_r[i] = 0.f;
   const bool dense = ctl->dense != 0;
   const int npad = (n + 127) / 128 * 128;
   bool big = false;
@@ -532,8 +528,7 @@ cudaError_t launch_to_f16(const void *const src[3], void *const dst[3], size_t e
 cudaError_t launch_bwd_prep_rows(const BwdArgs &a, cudaStream_t s) {
   const int blocks = a.T < 2 * num_sms() ? a.T : 2 * num_sms();
   launch_k(bwd_prep_rows_kernel, blocks, 256, 0, s, a.ws.ctl, a.ws.rows, (const uint4 *)a.dy,
-           (const uint4 *)a.x, (uint4 *)a.ws.dyg, (uint4 *)a.ws.xg, a.ws.dbg_r, a.D * 2 / 16, a.F,
-           a.tw.status);
+           (const uint4 *)a.x, (uint4 *)a.ws.dyg, (uint4 *)a.ws.xg, a.D * 2 / 16, a.tw.status);
   return cudaGetLastError();
 }
 

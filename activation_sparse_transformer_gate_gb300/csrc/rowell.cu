@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(RE_THREADS) rowell_updown_kernel(REParams p) {
     for (int b0 = 0; b0 < m; b0 += PB) {
       const int nb = m - b0 < PB ? m - b0 : PB;
       uint4 r[PB][VPT];
-      gather8<T, VPT, PB>(Wd4, s_n, b0, nb, NV, r);
+      gather8<T, VPT, PB>(Wd4, s_n, b0, nb, NV, NV, r);
 #pragma unroll
       for (int b = 0; b < PB; ++b) {
         if (b >= nb) break;

@@ -326,7 +326,8 @@ struct TcParams {
   float *out;              // EPI_F32, EPI_DW
   float lambda;            // EPI_DH: L1 coefficient
   __half *dz2, *du2, *h2;  // EPI_DH outputs, [Tp][F] fp16
-  float *dbg_r;            // EPI_DH: column sums of dz (zeroed before); EPI_DW: added to dbg_out
+  float *dbg_r;            // EPI_DH: column sums of dz per 32-row group [group][F]; EPI_DW:
+                           // summed over the groups in order and added to dbg_out
   float *dbg_out;          // EPI_DW: dbg (added from dbg_r with the W_gate problem)
   float *outq[3];          // EPI_DW: the fp32 output of each problem (dWg, [dWu,] dWd)
   int nq;                  // EPI_DW: problems in the launch
@@ -1085,7 +1086,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
           if (p.gated) store_f16x32(p.du2 + o, du, p.status);
           store_f16x32(p.h2 + o, hv, p.status);
           // dbg: column sums of this warp's 32 rows by recursive halving (lane
-          // l ends with column l), one atomic per column and warp
+          // l ends with column l), stored per 32-row group (m / 32) and
+          // summed in group order by the weight-gradient GEMM: no atomics,
+          // so the sum is the same on every run
 #pragma unroll
           for (int w = 16; w >= 1; w >>= 1) {
             const bool up = (lane & w) != 0;
@@ -1096,7 +1099,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
               dz[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
             }
           }
-          atomicAdd(p.dbg_r + n0 + c0 + lane, dz[0]);
+          p.dbg_r[(size_t)(m >> 5) * p.F + n0 + c0 + lane] = dz[0];
         }
       } else if (EPI == EPI_DHS) {
         // dh of the rows the gathers own (not the dense-path rows), from the
@@ -1199,8 +1202,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             o4[v4] = r;
           }
         }
-        if (q == 0 && nb == 0 && row_ok)
-          p.dbg_out[m] = (dense_all ? 0.f : p.dbg_out[m]) + p.dbg_r[m];
+        if (q == 0 && nb == 0 && row_ok) {  // dbg: the dense-path rows' group sums, in order
+          const int groups = (*p.k_dev + 127) / 128 * 4;
+          float sb = 0.f;
+          for (int g = 0; g < groups; ++g) sb += p.dbg_r[(size_t)g * p.F + m];
+          p.dbg_out[m] = (dense_all ? 0.f : p.dbg_out[m]) + sb;
+        }
       } else if (EPI == EPI_DOWN || EPI == EPI_DX) {
         const int tok = row_ok ? (dense_all ? m : p.rows[m]) : 0;
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -1256,6 +1263,17 @@ long long l2_size() {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) n = v;
   });
   return n;
+}
+
+int gather_passes(int requested, double set_bytes, int nv) {
+  int n = requested;
+  if (n <= 0) {  // automatic: passes whose working sets fit in GATHER_L2_SHARE of L2
+    const double budget = GATHER_L2_SHARE * (double)l2_size();
+    n = 1;
+    while (budget > 0.0 && set_bytes / n > budget && n < GATHER_MAX_PASSES) n *= 2;
+  }
+  if (n > nv) n = nv;
+  return n < 1 ? 1 : n;
 }
 
 int num_sms() {

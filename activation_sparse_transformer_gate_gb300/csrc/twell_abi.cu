@@ -103,15 +103,16 @@ Workspace carve_workspace(void *base, int T, int D, int F, int C, int K, int dty
       w.wu16 = take_dense(2 * (size_t)F * D);
     }
   }
+  const size_t slots = nt * (size_t)T * (size_t)K;
+  if (!train) w.hs = (float *)take(4 * slots);  // h at the slots between the up and down passes
   if (train) {
     w.urows = take_dense(es * Rp * F);
     w.dyg = take_dense(es * Rp * D);
-    w.dbg_r = (float *)take(4 * (size_t)F);
+    w.dbg_r = (float *)take_dense(4 * (Rp / 32) * (size_t)F);
     w.slot_parts = (unsigned long long *)take(8 * (size_t)SLOT_PARTS_MAX);
-    const size_t slots = nt * (size_t)T * (size_t)K;
     w.dz = (float *)take(4 * slots);
     w.du = (float *)take(4 * slots);
-    w.hs = (float *)take(4 * slots);
+    w.hs = (float *)take(4 * slots);  // also the forward's h between its two passes
     w.col_ptr = (int32_t *)take(4 * ((size_t)F + 1));
     w.col_cnt = (int32_t *)take(4 * (size_t)F);
     w.col_e = (float4 *)take(16 * slots);
@@ -154,7 +155,7 @@ twell_status check_tw(const twell_t *tw, int train) {
   twell_status s = check_shape(tw->T, 16, tw->F, tw->C, tw->K, tw->dtype);
   if (s != TWELL_OK) return s;
   if (!tw->idx || !tw->val || !tw->nnz || !tw->n_ovf || !tw->status) return TWELL_ERR_ARG;
-  if (tw->ovf_cap < 0 || tw->dense_rows_cap < 0) return TWELL_ERR_ARG;
+  if (tw->ovf_cap < 0 || tw->dense_rows_cap < 0 || tw->gather_passes < 0) return TWELL_ERR_ARG;
   if (tw->ovf_cap > 0 && (!tw->ovf_rows || !tw->g_fb)) return TWELL_ERR_ARG;
   if (!aligned16(tw->idx) || !aligned16(tw->val) || !aligned16(tw->nnz)) return TWELL_ERR_ALIGN;
   if (tw->ovf_cap > 0 && !aligned16(tw->g_fb)) return TWELL_ERR_ALIGN;
@@ -186,21 +187,24 @@ float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_s
 // where the dense path does ~4·d_model flops per (token, neuron) beyond the
 // shared gate GEMM (the up and down GEMMs) at ~1.3 PFLOP/s: measured
 // crossover ~1.3% at d_model 2048 / d_ff 8192.  When the gathered matrices
-// exceed L2 the gathers slow in about the proportion of rows that miss it
-// (d_model 4096 / d_ff 14336 bf16: 235 MB, ~9.5 TB/s measured, crossover
-// ~0.65%), so the default scales by L2 / their bytes.  The backward gathers
-// five rows per pair where its dense path does 6 GEMM units against the
-// forward's 2 (dh, the two dx products, the three weight gradients): its
-// crossover is (6/2) / (5/2) = 1.2 times the forward's.
+// exceed L2 the forward's gathers slow down even in two passes (d_model
+// 4096 / d_ff 14336 bf16: 235 MB, ~10 TB/s, crossover ~0.65%), so its
+// default scales by L2 / their bytes.  The backward gathers five rows per
+// pair where its dense path does 6 GEMM units against the forward's 2 (dh,
+// the two dx products, the three weight gradients): its crossover is
+// (6/2) / (5/2) = 1.2 times the forward's unscaled one, with no L2 scaling:
+// its dx and dW gathers run in passes whose working sets fit in L2 at close
+// to the rates of the smaller shape (d_model 4096 / d_ff 14336 at 0.99%
+// active: gather backward ~2.9 ms against 3.9 ms for the six GEMMs).
 float density_of(const twell_t *tw, int D, int gated, bool backward) {
   if (tw->dense_density > 0.f) return tw->dense_density;
   if (tw->dense_density < 0.f) return -1.f;
+  if (backward) return 0.013f * 1.2f;
   const size_t es = tw->dtype == TWELL_BF16 ? 2 : 4;
   const double wbytes = (double)(gated ? 2 : 1) * (double)tw->F * (double)D * (double)es;
   const double l2 = (double)l2_size();
   double d = 0.013;
   if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
-  if (backward) d *= 1.2;
   return (float)d;
 }
 
@@ -374,8 +378,9 @@ twell_status twell_ffn_forward(const void *x, const void *Wg, const float *bg,
     e = run_dense_rows(a, true, aux->s2);
   }
   if (e == cudaSuccess) {
-    e = launch_updown_fused(a, s);
-    prof_mark(KID_UPDOWN, s);
+    int n = 1;
+    e = launch_updown_fused(a, s, &n);
+    prof_mark(KID_UPDOWN, s, n);
   }
   if (fork) {  // join (also after an error, so the caller's stream stays ordered)
     const cudaError_t j1 = cudaEventRecord(aux->join, aux->s2);

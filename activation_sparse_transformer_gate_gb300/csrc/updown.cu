@@ -18,6 +18,16 @@
 // the phases.  All-dense mode (and overflow rows when there are many) is left
 // to the tensor-core dense-row GEMMs; a few overflow rows are handled here
 // from the wide-tile buffer.
+//
+// Two passes when W_up and W_down together do not fit in L2: with both in
+// one pass every token's CTA reads rows of both, the working set is both
+// matrices, and rows miss L2 (d_model 4096 / d_ff 14336 bf16, 235 MB: 47% L2
+// hits, 5.4 GB of DRAM reads for 9.4 GB gathered; random-row gathers of the
+// two matrices in that order run at 11.0 TB/s on GB300, one matrix at a time
+// at 15.7 TB/s).  The up pass then computes h = g u of every slot into an
+// fp32 slot array (the same values the fused kernel keeps in shared memory),
+// and the down pass reads them back: each pass's working set is one matrix.
+// Overflow rows handled here run both phases in the up pass.
 #include "common.cuh"
 #include "gather.cuh"
 #include "kernels.h"
@@ -34,7 +44,9 @@ struct UDParams {
   const void *val, *wide;
   void *u_val, *y, *g_fb, *u_fb;
   const int32_t *pos;
+  float *hsl;   // [F/C][T][K] h at the slots between the two passes
   int Tn, D, F, C, K, gated, train, cap;
+  int phase;    // 0: up and down in one pass; 1: up pass; 2: down pass
   const Ctl *ctl;
   int32_t *status;
 };
@@ -65,6 +77,9 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   const int ps = p.pos[t];
   const bool ovf = ps >= 0;
   if (ovf && p.ctl->ovf_gemm) return;
+  if (ovf && p.phase == 2) return;               // done in the up pass
+  const bool up_only = p.phase == 1 && !ovf;     // h to the slot array, no y
+  const bool down_only = p.phase == 2;           // h from the slot array
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
   const int nt = p.F / p.C;
   const int NV = p.D / EV;
@@ -78,7 +93,7 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
       if (u4) u4[v] = make_uint4(0, 0, 0, 0);
     }
   }
-  if (p.gated)  // x_t to shared memory (visible after the barriers of build_pairs)
+  if (p.gated && !down_only)  // x_t to shared memory (visible after the barriers of build_pairs)
     for (int v = tid; v < NV; v += blockDim.x)  // x_t is read once here: evict-first
       s_x[v] = ldg_stream<L2_FIRST>((const uint4 *)p.x + (size_t)t * NV + v);
   float2 yr[VPT][EV / 2];
@@ -103,7 +118,7 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
       for (int i = tid; i < P; i += blockDim.x)
         if (s_slot[i] != PAD_SLOT) ((T *)p.g_fb)[(size_t)ps * p.F + s_n[i]] = from_f<T>(s_g[i]);
     // ---- phase 1: u and h of every pair, one warp per pair ------------------
-    if (p.gated) {
+    if (p.gated && !down_only) {
       for (int i0 = w; i0 < P; i0 += nw * PIF) {
         uint4 wr[PIF][VPL];
 #pragma unroll
@@ -133,13 +148,20 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
         }
       }
     }
+    if (down_only)  // h of the up pass (slots of a non-overflow row are >= 0)
+      for (int i = tid; i < P; i += blockDim.x) s_g[i] = p.hsl[s_slot[i]];
     __syncthreads();
+    if (up_only) {
+      for (int i = tid; i < P; i += blockDim.x) p.hsl[s_slot[i]] = s_g[i];
+      __syncthreads();  // the list is rewritten by the next group
+      continue;
+    }
     // ---- phase 2: y += h * W_down[n], thread-owned slices -------------------
     for (int b0 = 0; b0 < P; b0 += PB2) {
       const int nb = P - b0 < PB2 ? P - b0 : PB2;
       uint4 wd[PB2][VPT];
-      if (EXACT && nb == PB2) gather8<T, VPT, PB2, UD_THREADS>(Wd4, s_n, b0, nb, NV, wd);
-      else gather8<T, VPT, PB2>(Wd4, s_n, b0, nb, NV, wd);
+      if (EXACT && nb == PB2) gather8<T, VPT, PB2, UD_THREADS>(Wd4, s_n, b0, nb, NV, NV, wd);
+      else gather8<T, VPT, PB2>(Wd4, s_n, b0, nb, NV, NV, wd);
 #pragma unroll
       for (int b = 0; b < PB2; ++b) {
         if (b >= nb) break;
@@ -151,6 +173,7 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
     __syncthreads();  // the list is rewritten by the next group
   }
 
+  if (up_only) return;
   uint4 *yrow = (uint4 *)p.y + (size_t)t * NV;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
@@ -159,24 +182,33 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
   }
 }
 
-cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s) {
+cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s, int *launches) {
   UDParams p;
   p.x = a.x; p.Wu = a.Wu; p.Wd = a.Wd; p.idx = a.tw.idx; p.nnz = a.tw.nnz; p.val = a.tw.val;
   p.wide = a.ws.wide; p.u_val = a.tw.u_val; p.y = a.y; p.g_fb = a.tw.g_fb; p.u_fb = a.tw.u_fb;
   p.pos = a.ws.pos; p.Tn = a.T; p.D = a.D; p.F = a.F; p.C = a.C; p.K = a.K; p.gated = a.gated;
   p.train = a.train && a.gated; p.cap = a.tw.ovf_cap; p.ctl = a.ws.ctl; p.status = a.tw.status;
+  p.hsl = a.ws.hs;
+  // one pass, or the up pass then the down pass (gated FFN whose two
+  // gathered matrices do not fit in L2 together)
+  const size_t es = a.dtype == TWELL_BF16 ? 2 : 4;
+  const bool two = a.gated && gather_passes(a.tw.gather_passes, 2.0 * a.F * a.D * es, a.D * es / 16) > 1;
+  if (launches) *launches = two ? 2 : 1;
   const int EV = a.dtype == TWELL_BF16 ? 8 : 4;
   const int NV = a.D / EV;  // <= 1024 (checked by the caller)
   const int vpl = NV <= 32 ? 1 : NV <= 64 ? 2 : NV <= 128 ? 4 : NV <= 256 ? 8 : NV <= 512 ? 16 : 32;
 #define TW_UD(TT, L)                                                                           \
   do {                                                                                         \
     constexpr int VPT_ = (L + 3) / 4;                                                          \
-    if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                             \
-      launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>, a.T,        \
-               UD_THREADS, 0, s, p);                                                           \
-    else                                                                                       \
-      launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>, a.T,       \
-               UD_THREADS, 0, s, p);                                                           \
+    for (int ph = two ? 1 : 0; ph <= (two ? 2 : 0); ++ph) {                                    \
+      p.phase = ph;                                                                            \
+      if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                           \
+        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>, a.T,      \
+                 UD_THREADS, 0, s, p);                                                         \
+      else                                                                                     \
+        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>, a.T,     \
+                 UD_THREADS, 0, s, p);                                                         \
+    }                                                                                          \
   } while (0)
 #define TW_UD_T(TT)                                                                            \
   do {                                                                                         \

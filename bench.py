@@ -73,6 +73,9 @@ def parse_args():
                     help="backward: slot density above which dh comes from the tensor-core "
                          "GEMM read at the slots (0: the library default; < 0: always the "
                          "gather SDDMM; a tiny value: always the GEMM)")
+    ap.add_argument("--gather-passes", type=int, default=0,
+                    help="passes of the gather kernels over their matrices / d_model columns "
+                         "(0: the library's choice from L2 size; 1: one pass)")
     return ap.parse_args()
 
 
@@ -169,7 +172,8 @@ class Bench:
         T, D, F = w.T, w.D, w.F
         self.bufs = tw.TwellBuffers(T, F, w.C, w.K, self.dtype, train=train, device=dev,
                                     dense_density=args.dense_density,
-                                    dh_density=args.dh_density)
+                                    dh_density=args.dh_density,
+                                    gather_passes=args.gather_passes)
         self.ws, self.nws = tw.workspace(T, D, F, w.C, w.K, self.dtype, train, device=dev)
         self.y = torch.empty((T, D), dtype=tdt, device=dev)
         self.dx = self.dWg = self.dWu = self.dWd = self.dbg = None
@@ -547,12 +551,14 @@ def gather_ceiling(torch, dev, W, w, pairs, timed, sh):
 
 
 def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
-    """Achieved rate of each kernel from its algorithmic work per launch:
+    """Achieved rate of each kernel from its algorithmic work per step:
     bytes for the gather kernels (rows gathered + rows streamed + TwELL),
     flops for the gate GEMM and for the dense-path GEMMs (rows_f / rows_b
     rows of the forward / backward; fp16 operands, one GEMM per product),
-    bytes for the fp16 weight copies of the dense path.  See the design notes
-    for the per-unit figures."""
+    bytes for the fp16 weight copies of the dense path; divided by the
+    kernel's device time per step (a gather kernel split into passes over
+    its matrices or columns launches once per pass, each with its share of
+    the work).  See the design notes for the per-unit figures."""
     peaks = load_peaks()
     D, F, T, K = w.D, w.F, w.T, w.K
     es = 2 if w.dtype == "bf16" else 4
@@ -601,14 +607,14 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
             wrk[k] = ("tensor", 2.0 * mult * rows * D * F)
     # fp16 copies of the weights the dense-path GEMMs take (read bf16, write
     # fp16): W_down in the forward (gated), W_down, W_gate (, W_up) in the backward
-    n16 = (ng if train else (1 if w.gated else 0)) if (rows_f > 0 or rows_b > 0) else 0
+    n16 = ((1 if w.gated and rows_f > 0 else 0) + (ng if train and rows_b > 0 else 0))
     if n16 and es == 2:
         wrk["weights_to_f16"] = ("hbm", n16 * F * D * 4)
     out = {}
     for k, (bound, work) in wrk.items():
         if k not in kern:
             continue
-        sec = kern[k]["avg_ms"] / 1e3
+        sec = kern[k]["ms_per_step"] / 1e3
         src = peaks["source"]
         if bound == "hbm":
             ach, peak, unit = work / sec / 1e9, peaks["hbm_gbs"], "GB/s"

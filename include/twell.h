@@ -109,10 +109,11 @@ typedef struct {
                              at most K per row and tile) exceed
                              dense_density * T * F: at such densities the
                              gathers cost more than dense GEMMs.  0 selects
-                             the measured crossover: 0.013 when the gathered
-                             weights (W_up + W_down) fit in L2, scaled by
-                             L2 / their bytes when they do not, and 1.2x
-                             that in the backward; < 0 disables this test.
+                             the measured crossover: in the forward 0.013
+                             when the gathered weights (W_up + W_down) fit
+                             in L2, scaled by L2 / their bytes when they do
+                             not; in the backward 0.0156 (its gathers run in
+                             L2-sized passes); < 0 disables this test.
                              The backward applies the same rules to the
                              saved TwELL.                                    */
   float dh_density;       /* backward, bf16 on the tensor-core path: when the
@@ -134,6 +135,18 @@ typedef struct {
                              overflow rows (more: TWELL_ERR_CAPACITY).  The
                              same value must be used for the workspace size
                              and every call.                                 */
+  int32_t gather_passes;  /* passes of the row-gather kernels over their
+                             gathered matrices, so that each pass's working
+                             set stays in L2: the forward's up and down
+                             projections run as one pass or as an up pass
+                             then a down pass (gated FFN, >= 2); the
+                             backward's dx and weight-gradient gathers split
+                             d_model into this many column ranges.  Results
+                             are bit-identical for every value.  0 selects
+                             it from the working set (W_up + W_down; W_gate +
+                             W_up; x + dy) against the L2 size; >= 1 forces it
+                             (the column split at most d_model / 8 (bf16) or
+                             d_model / 4 (fp32) passes).                     */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward

@@ -167,8 +167,9 @@ def test_workspace_size_with_a_dense_row_cap(lib):
     assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 4096) == full
     assert tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 9999) == full
     capped = tw.twell_workspace_size_rows(4096, 2048, 8192, 128, 8, tw.TWELL_BF16, 1, 256)
-    # per dense row: h (2F), u rows (2F), dz/du/h rows (3 x 4F) bytes, x and dy rows
-    per_row = 2 * 8192 + 2 * 8192 + 3 * 4 * 8192 + 2 * 2 * 2048
+    # per dense row: h (2F), u rows (2F), dz/du/h rows (3 x 4F) bytes, x and dy
+    # rows, and the dbg column sums (4F per 32 rows)
+    per_row = 2 * 8192 + 2 * 8192 + 3 * 4 * 8192 + 2 * 2 * 2048 + 4 * 8192 // 32
     assert full - capped == (4096 - 256) * per_row
     assert capped < full / 3
     # rounded up to whole 128-row tiles
@@ -185,7 +186,8 @@ def test_workspace_without_dense_path_rows(lib):
     tile = tw.twell_workspace_size_rows(T, D, F, 128, 8, tw.TWELL_BF16, 1, 128)
     dense_row_bytes = 128 * (2 * F + 2 * F + 2 * D + 2 * D)  # h, u rows, x and dy rows
     f16_copies = 3 * 2 * F * D
-    assert tile - small == dense_row_bytes + f16_copies
+    dbg_groups = 4 * (128 // 32) * F                          # dbg column sums per 32 rows
+    assert tile - small == dense_row_bytes + f16_copies + dbg_groups
     # T below one tile: every row may run densely, the buffers are kept
     assert (tw.twell_workspace_size_rows(100, D, F, 128, 8, tw.TWELL_BF16, 1, 100) ==
             tw.twell_workspace_size(100, D, F, 128, 8, tw.TWELL_BF16, 1))

@@ -82,8 +82,8 @@ REGIMES = {
     # name: (bias, K, backward density threshold (None: the forward's),
     #        forward all-dense, backward all-dense, dh GEMM, full dbg)
     "0.5pct_gathers": (-2.58, 8, None, 0, 0, 0, False),
-    "1pct_all_dense": (-2.33, 8, None, 1, 1, 0, False),
-    "1pct_dense_fwd_gather_bwd": (-2.33, 8, -1.0, 1, 0, 1, True),
+    "1pct_all_dense": (-2.33, 8, 1e-9, 1, 1, 0, False),
+    "1pct_dense_fwd_gather_bwd": (-2.33, 8, None, 1, 0, 1, True),
     "5pct_all_dense": (-1.64, 16, None, 1, 1, 0, False),
 }
 

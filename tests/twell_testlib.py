@@ -310,7 +310,7 @@ def shifted(t, elems):
 
 
 def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0, dh_density=-1.0,
-              keep_twell=False, bwd_dense_density=None):
+              keep_twell=False, bwd_dense_density=None, gather_passes=0):
     """Forward (train) + backward through the C ABI.  dense_density < 0 keeps
     the density test of the dispatcher off, so that moderately dense test
     workloads still run the gather kernels; dh_density < 0 keeps dh on the
@@ -320,7 +320,8 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0,
     backward ("ctl_bwd").  keep_twell: also return the saved TwELL (idx, nnz,
     the overflow rows and their dense backup rows) for activity checks.
     bwd_dense_density: the backward's own density threshold (the twell_t is
-    passed per call), else the forward's."""
+    passed per call), else the forward's.  gather_passes: the twell_t's
+    passes of the gather kernels (0: the library's choice)."""
     import torch
     import activation_sparse_transformer_gate_gb300 as tw
     T, D, F, C, K = a["x"].shape[0], a["x"].shape[1], a["Wg"].shape[0], w.C, w.K
@@ -330,7 +331,7 @@ def run_train(a, w, lam, ovf_cap=None, dense_density=-1.0, out=None, wd_shift=0,
     if wd_shift:
         d["Wd"] = shifted(d["Wd"], wd_shift)
     bufs = tw.TwellBuffers(T, F, C, K, dtype, ovf_cap, train=True, dense_density=dense_density,
-                           dh_density=dh_density)
+                           dh_density=dh_density, gather_passes=gather_passes)
     ws, nws = tw.workspace(T, D, F, C, K, dtype, True)
     y = torch.empty((T, D), dtype=tdt, device="cuda")
     tw.twell_ffn_forward(d["x"], d["Wg"], d["bg"], d["rb"], d["Wu"], d["Wd"], D, 1, bufs.t, y, ws, nws)
