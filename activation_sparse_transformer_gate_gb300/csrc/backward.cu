@@ -765,8 +765,9 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   // thread owns two 16-byte vectors of a row (half the per-row overhead of
   // one), batches of 3 rows per matrix in flight.
   const size_t es = bf ? 2 : 4;
-  const int dx_passes = gather_passes(a.tw.gather_passes, (a.gated ? 2.0 : 1.0) * a.F * a.D * es, NV);
-  const int dw_passes = gather_passes(a.tw.gather_passes, 2.0 * a.T * a.D * es, NV);
+  const int dx_passes = gather_passes(a.tw.gather_passes, (a.gated ? 2.0 : 1.0) * a.F * a.D * es, NV,
+                                      GATHER_MIN_WIDTH);
+  const int dw_passes = gather_passes(a.tw.gather_passes, 2.0 * a.T * a.D * es, NV, GATHER_MIN_WIDTH);
 #define TW_VPT(K, TT, G, SS, NPASS)                                                            \
   do {                                                                                         \
     for (int i_ = 0; i_ < (NPASS); ++i_) {                                                     \

@@ -88,7 +88,8 @@ long long l2_size();
 // up/down, over its two matrices) so that each pass's gathered working set
 // stays in L2.  requested > 0: that many (at most nv, the row's 16-byte
 // vectors); 0: the fewest powers of two up to GATHER_MAX_PASSES whose share
-// of set_bytes fits in GATHER_L2_SHARE of L2.  Measured on GB300 (random
+// of set_bytes fits in GATHER_L2_SHARE of L2, keeping at least min_width
+// vectors per pass.  Measured on GB300 (random
 // rows, 575k gathers): 18.3 TB/s from one 34 MB matrix, 15.7 TB/s from one
 // 117 MB matrix, 11.0 TB/s from two 117 MB matrices read together.  At
 // d_model 4096 / d_ff 14336 (W_gate + W_up 235 MB, x + dy 134 MB at 8192
@@ -96,10 +97,13 @@ long long l2_size();
 // although x + dy is just below the 135.5 MB L2: the kernels also stream
 // other data through it) and four (1.03, 0.84 ms: the per-pass list
 // building and the narrower CTAs cost more than the smaller working set
-// saves).
+// saves).  Column passes narrower than 256 vectors (4 KB of a bf16 row) lost
+// everywhere they were measured (also d_model 2048 / 16384 tokens: dW 0.73 ->
+// 0.87 ms in two passes), hence GATHER_MIN_WIDTH for the column splits.
 constexpr double GATHER_L2_SHARE = 0.9;
 constexpr int GATHER_MAX_PASSES = 4;
-int gather_passes(int requested, double set_bytes, int nv);
+constexpr int GATHER_MIN_WIDTH = 256;
+int gather_passes(int requested, double set_bytes, int nv, int min_width);
 
 cudaError_t launch_pack_dense(const void *H, const twell_t &tw, cudaStream_t s);
 // Hybrid split.  With a workspace: reads the overflow-row bitmap (which must

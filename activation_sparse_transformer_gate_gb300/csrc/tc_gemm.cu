@@ -1265,12 +1265,14 @@ long long l2_size() {
   return n;
 }
 
-int gather_passes(int requested, double set_bytes, int nv) {
+int gather_passes(int requested, double set_bytes, int nv, int min_width) {
   int n = requested;
   if (n <= 0) {  // automatic: passes whose working sets fit in GATHER_L2_SHARE of L2
     const double budget = GATHER_L2_SHARE * (double)l2_size();
     n = 1;
-    while (budget > 0.0 && set_bytes / n > budget && n < GATHER_MAX_PASSES) n *= 2;
+    while (budget > 0.0 && set_bytes / n > budget && n < GATHER_MAX_PASSES &&
+           nv / (2 * n) >= min_width)
+      n *= 2;
   }
   if (n > nv) n = nv;
   return n < 1 ? 1 : n;

@@ -192,7 +192,7 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s, int *launches)
   // one pass, or the up pass then the down pass (gated FFN whose two
   // gathered matrices do not fit in L2 together)
   const size_t es = a.dtype == TWELL_BF16 ? 2 : 4;
-  const bool two = a.gated && gather_passes(a.tw.gather_passes, 2.0 * a.F * a.D * es, a.D * es / 16) > 1;
+  const bool two = a.gated && gather_passes(a.tw.gather_passes, 2.0 * a.F * a.D * es, a.D * es / 16, 1) > 1;
   if (launches) *launches = two ? 2 : 1;
   const int EV = a.dtype == TWELL_BF16 ? 8 : 4;
   const int NV = a.D / EV;  // <= 1024 (checked by the caller)

@@ -447,11 +447,15 @@ def run_ours(args, rank, world, local_rank):
         mem, energy = memory_and_energy(torch, dev, local_rank, d, w, train, b.step, bufs, nws,
                                         int(row_ovf_count(bufs, w)))
         if w.dtype == "bf16":
-            cm = capped_memory(torch, tw, b, timed)
-            mem["capped_step"] = cm
-            mem["capped_vs_dense_peak"] = round(
-                cm["measured_peak_extra_bytes"] /
-                max(mem["dense_step_peak_beyond_outputs_bytes"], 1), 4)
+            # 256 rows: the dense path still takes up to two row tiles; 64:
+            # below one 128-row tile, no dense-path buffers at all (every row
+            # on the gathers, as at this sparsity anyway)
+            for key, cap in (("capped_step", 256), ("capped_step_no_dense_path", 64)):
+                cm = capped_memory(torch, tw, b, timed, cap)
+                mem[key] = cm
+                mem[key.replace("capped_step", "capped_vs_dense_peak")] = round(
+                    cm["measured_peak_extra_bytes"] /
+                    max(mem["dense_step_peak_beyond_outputs_bytes"], 1), 4)
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(b.a, w, train, args.cpu_seconds)
     del b, d, bufs, ws, y
     torch.cuda.empty_cache()
