@@ -1035,18 +1035,32 @@ def end_to_end(torch, d, step, y, dx, w, train, timed, args, stream, flush_buf):
         torch.cuda.synchronize(stream.device)
         return t0.elapsed_time(t1) / K
 
+    def flush_only(K):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(K):
+            flush_buf.fill_(1)
+        t1.record(stream)
+        torch.cuda.synchronize(stream.device)
+        return t0.elapsed_time(t1) / K
+
     for _ in range(3):
         serial_step()
     steps = max(10, min(args.steps, 200))
     ms_serial = timed(serial_step, steps) / steps
     pipelined(3)
     ms = pipelined(steps)
+    ms_flush = flush_only(steps)
     h2d_bytes = hx.numel() * 2 + (hdy.numel() * 2 if train else 0)
     d2h_bytes = hy[0].numel() * 2 + (hdx[0].numel() * 2 if train else 0)
     return {"value": round(w.T / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
             "ms_per_step": round(ms, 5), "steps": steps,
             "copies": "double-buffered on a second stream, overlapping the neighbouring steps",
+            "l2_flush_ms_per_step": round(ms_flush, 5),
+            "note_flush": "the timed region also holds the write of a 2 x L2 buffer before every "
+                          "step (cold L2, as for value); l2_flush_ms_per_step is that write's "
+                          "own time, not subtracted",
             "serial_ms_per_step": round(ms_serial, 5),
             "serial_tokens_per_s": round(w.T / (ms_serial / 1e3), 1),
             "outputs_copied": "y" + (" and dx; the fp32 weight gradients (dW_gate, dW_up, "
