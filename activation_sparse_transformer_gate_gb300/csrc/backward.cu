@@ -100,6 +100,21 @@ __device__ __forceinline__ void axpy3(float2 *ag, float2 *au, float2 *ad, const 
   }
 }
 
+// ag += dz x, au += du x for one 16-byte vector of x (r = {token, dz, du, h}).
+template <class T>
+__device__ __forceinline__ void axpy2(float2 *ag, float2 *au, const float4 &r, const uint4 &xv) {
+  constexpr int EV = Vec<T>::EV;
+  float fx[EV];
+  Vec<T>::unpack(xv, fx);
+  const float2 zz = make_float2(r.y, r.y), uu = make_float2(r.z, r.z);
+#pragma unroll
+  for (int q = 0; q < EV / 2; ++q) {
+    const float2 xf = make_float2(fx[2 * q], fx[2 * q + 1]);
+    ag[q] = __ffma2_rn(zz, xf, ag[q]);
+    au[q] = __ffma2_rn(uu, xf, au[q]);
+  }
+}
+
 }  // namespace
 
 // Pair list of one token for the backward: slots for a non-overflow row, the
@@ -518,10 +533,20 @@ __global__ void __launch_bounds__(TR_CHUNK) twell_transpose_kernel(BParams p) {
 // order); dbg is written by the first pass.
 constexpr int DW_LIST = 512;
 
-template <class T, int VPT, int NB, int NTH>
+// PART 0: all three gradients; 1: dW_gate, dW_up and dbg (x rows only); 2:
+// dW_down (dy rows only).  Split in two, each launch gathers one matrix's
+// rows (half the working set) and holds fewer accumulators, so it needs
+// fewer registers per thread and more CTAs fit on an SM (86 and 63 against
+// 128 registers at d_model 2048).  Measured: x + dy of 134 MB (d_model 2048
+// at 16384 tokens; d_model 4096 at 8192) 0.735 -> 0.686 ms and 0.739 ->
+// 0.706 ms; at 34 MB (d_model 2048, 4096 tokens) it loses, 0.211 -> 0.222
+// ms (each part repeats the per-neuron list staging and row stores), so
+// the split is taken only when x + dy exceed half of L2.
+template <class T, int VPT, int NB, int NTH, int PART>
 __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
   pdl_begin();
   constexpr int EV = Vec<T>::EV;
+  constexpr bool DX = PART != 2, DY = PART != 1;  // x rows (dW_gate, dW_up) / dy rows (dW_down)
   __shared__ float4 s_e[DW_LIST];
   if (p.gemm_rows && p.ctl->dense) return;  // the GEMMs write every row
   const int n = blockIdx.x, tid = threadIdx.x;
@@ -550,16 +575,16 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
         if (NTH > 0 && nb == NB) {  // full batch of exact rows: constant offsets
 #pragma unroll
           for (int v = 0; v < VPT; ++v) {
-            xv[b][v] = ldg_stream(xr + v * NTH);
-            yv[b][v] = ldg_stream(yr + v * NTH);
+            if (DX) xv[b][v] = ldg_stream(xr + v * NTH);
+            if (DY) yv[b][v] = ldg_stream(yr + v * NTH);
           }
         } else {
 #pragma unroll
           for (int v = 0; v < VPT; ++v) {
             const int vi = tid + v * blockDim.x;
             const bool ok = b < nb && vi < NP;
-            xv[b][v] = ok ? ldg_stream(xr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
-            yv[b][v] = ok ? ldg_stream(yr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+            if (DX) xv[b][v] = ok ? ldg_stream(xr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
+            if (DY) yv[b][v] = ok ? ldg_stream(yr + v * blockDim.x) : make_uint4(0, 0, 0, 0);
           }
         }
       }
@@ -569,7 +594,11 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
         const float4 r = s_e[e0 + b];
         sb += r.y;
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) axpy3<T>(ag[v], au[v], ad[v], r, xv[b][v], yv[b][v]);
+        for (int v = 0; v < VPT; ++v) {
+          if (DX && DY) axpy3<T>(ag[v], au[v], ad[v], r, xv[b][v], yv[b][v]);
+          else if (DX) axpy2<T>(ag[v], au[v], r, xv[b][v]);
+          else axpy_vec<T>(ad[v], r.w, yv[b][v]);
+        }
       }
     }
   }
@@ -586,7 +615,9 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
     for (int v = 0; v < VPT; ++v) {
       const int vi = tid + v * blockDim.x;
       if (vi >= NP) continue;
-      axpy3<T>(ag[v], au[v], ad[v], r, x4[(size_t)t * NV + vi], dy4[(size_t)t * NV + vi]);
+      if (DX && DY) axpy3<T>(ag[v], au[v], ad[v], r, x4[(size_t)t * NV + vi], dy4[(size_t)t * NV + vi]);
+      else if (DX) axpy2<T>(ag[v], au[v], r, x4[(size_t)t * NV + vi]);
+      else axpy_vec<T>(ad[v], r.w, dy4[(size_t)t * NV + vi]);
     }
   }
   const size_t o0 = (size_t)n * p.D + (size_t)v0 * EV;
@@ -598,12 +629,12 @@ __global__ void __launch_bounds__(256) bwd_dw_kernel(BParams p) {
     if (vi >= NP) continue;
 #pragma unroll
     for (int q = 0; q < EV / 4; ++q) {
-      stg_stream(og + vi * (EV / 4) + q, f4bits(ag[v][2 * q], ag[v][2 * q + 1]));
-      stg_stream(od + vi * (EV / 4) + q, f4bits(ad[v][2 * q], ad[v][2 * q + 1]));
-      if (ou) stg_stream(ou + vi * (EV / 4) + q, f4bits(au[v][2 * q], au[v][2 * q + 1]));
+      if (DX) stg_stream(og + vi * (EV / 4) + q, f4bits(ag[v][2 * q], ag[v][2 * q + 1]));
+      if (DY) stg_stream(od + vi * (EV / 4) + q, f4bits(ad[v][2 * q], ad[v][2 * q + 1]));
+      if (DX && ou) stg_stream(ou + vi * (EV / 4) + q, f4bits(au[v][2 * q], au[v][2 * q + 1]));
     }
   }
-  if (tid == 0 && v0 == 0) p.dbg[n] = sb;
+  if (DX && tid == 0 && v0 == 0) p.dbg[n] = sb;
 }
 
 // ---------------------------------------------------------------------------
@@ -767,8 +798,15 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const size_t es = bf ? 2 : 4;
   const int dx_passes = gather_passes(a.tw.gather_passes, (a.gated ? 2.0 : 1.0) * a.F * a.D * es, NV,
                                       GATHER_MIN_WIDTH);
-  const int dw_passes = gather_passes(a.tw.gather_passes, 2.0 * a.T * a.D * es, NV, GATHER_MIN_WIDTH);
-#define TW_VPT(K, TT, G, SS, NPASS)                                                            \
+  // dW: x rows and dy rows in separate launches when together they exceed
+  // half of L2 (any forced pass count > 1 splits too), and column passes
+  // chosen on x + dy together (d_model 4096 at 8192 tokens: split and two
+  // column passes 0.71 ms, split alone 0.82, two column passes alone 0.74)
+  const double dw_set = 2.0 * a.T * a.D * es;
+  const bool dw_split = a.tw.gather_passes > 0 ? a.tw.gather_passes > 1
+                                               : dw_set > 0.5 * (double)l2_size();
+  const int dw_passes = gather_passes(a.tw.gather_passes, dw_set, NV, GATHER_MIN_WIDTH);
+#define TW_VPT(K, TT, G, SS, NPASS, EXTRA)                                                     \
   do {                                                                                         \
     for (int i_ = 0; i_ < (NPASS); ++i_) {                                                     \
       p.v0 = (int)((long)NV * i_ / (NPASS));                                                   \
@@ -776,10 +814,10 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
       const int np_ = p.nvp;                                                                   \
       const int vpt = np_ <= 64 ? 1 : np_ <= 512 ? 2 : 4;                                      \
       const int threads = ((np_ + vpt - 1) / vpt + 31) / 32 * 32;                              \
-      if (vpt == 1) launch_k(K<TT, 1, 8, 0>, G, threads, 0, SS, p);                            \
-      else if (vpt == 2 && np_ == 256) launch_k(K<TT, 2, 4, 128>, G, 128, 0, SS, p);           \
-      else if (vpt == 2) launch_k(K<TT, 2, 3, 0>, G, threads, 0, SS, p);                       \
-      else launch_k(K<TT, 4, 2, 0>, G, threads, 0, SS, p);                                     \
+      if (vpt == 1) launch_k(K<TT, 1, 8, 0 EXTRA>, G, threads, 0, SS, p);                      \
+      else if (vpt == 2 && np_ == 256) launch_k(K<TT, 2, 4, 128 EXTRA>, G, 128, 0, SS, p);     \
+      else if (vpt == 2) launch_k(K<TT, 2, 3, 0 EXTRA>, G, threads, 0, SS, p);                 \
+      else launch_k(K<TT, 4, 2, 0 EXTRA>, G, threads, 0, SS, p);                               \
     }                                                                                          \
     p.v0 = 0;                                                                                  \
     p.nvp = NV;                                                                                \
@@ -801,8 +839,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     return r;
   };
   auto dx_spmm = [&]() {
-    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s, dx_passes);
-    else TW_VPT(bwd_dx_kernel, float, a.T, s, dx_passes);
+    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s, dx_passes, );
+    else TW_VPT(bwd_dx_kernel, float, a.T, s, dx_passes, );
     const cudaError_t r = cudaGetLastError();
     prof_mark(KID_BWD_DX, s, dx_passes);
     return r;
@@ -816,10 +854,26 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = transpose();
   }
   if (e == cudaSuccess) {  // 4. weight gradients
-    if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes);
-    else TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes);
+#define TW_PART0 , 0
+#define TW_PART1 , 1
+#define TW_PART2 , 2
+    if (dw_split) {  // x rows (dW_gate, dW_up, dbg), then dy rows (dW_down)
+      if (bf) {
+        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART1);
+        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART2);
+      } else {
+        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART1);
+        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART2);
+      }
+    } else {
+      if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART0);
+      else TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART0);
+    }
+#undef TW_PART0
+#undef TW_PART1
+#undef TW_PART2
     e = cudaGetLastError();
-    prof_mark(KID_BWD_DW, sw, dw_passes);
+    prof_mark(KID_BWD_DW, sw, dw_passes * (dw_split ? 2 : 1));
   }
 #undef TW_VPT
   // 5. weight gradients of the dense-path rows (added to those of step 4;

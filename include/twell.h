@@ -141,12 +141,15 @@ typedef struct {
                              projections run as one pass or as an up pass
                              then a down pass (gated FFN, >= 2); the
                              backward's dx and weight-gradient gathers split
-                             d_model into this many column ranges.  Results
-                             are bit-identical for every value.  0 selects
-                             it from the working set (W_up + W_down; W_gate +
-                             W_up; x + dy) against the L2 size; >= 1 forces it
-                             (the column split at most d_model / 8 (bf16) or
-                             d_model / 4 (fp32) passes).                     */
+                             d_model into this many column ranges, and the
+                             weight gradients also gather x rows (dW_gate,
+                             dW_up, dbg) and dy rows (dW_down) in separate
+                             launches (>= 2).  Results are bit-identical for
+                             every value.  0 selects it from the working set
+                             (W_up + W_down; W_gate + W_up; x + dy) against
+                             the L2 size; >= 1 forces it (the column split
+                             at most d_model / 8 (bf16) or d_model / 4
+                             (fp32) passes).                                 */
 } twell_t;
 
 /* Bytes of scratch that twell_pack / twell_ffn_forward / twell_ffn_backward
