@@ -37,6 +37,18 @@ namespace twell {
 namespace {
 
 constexpr int UD_THREADS = 128;  // 4 warps per token CTA
+// Rows of W_down in flight per batch of the down phase, exact row shapes:
+// 24 / VPT vectors per thread (12 rows at d_model 2048 bf16), but 4 rows
+// at VPT 4 and 2 at VPT 8, where more spill registers: at d_model 4096 the
+// 6-row batch spilled and 4 rows took the kernel from 0.93 to 0.74 ms
+// (config 4, 0.49% active).  At d_model 2048, 8 or 6 rows with five CTAs
+// per SM were slower than 12 with four (0.194 -> 0.211 / 0.222 ms).
+template <int VPT>
+constexpr int exact_rows() { return VPT == 4 ? 4 : VPT == 8 ? 2 : 24 / VPT; }
+// Rows in flight for the other shapes (predicated loads): 16 / VPT, one at
+// VPT 8 (d_model 8192 bf16), where two spill.
+template <int VPT>
+constexpr int generic_rows() { return VPT == 8 ? 1 : 16 / VPT; }
 
 struct UDParams {
   const void *x, *Wu, *Wd;
@@ -62,7 +74,7 @@ struct UDParams {
 // shuffles only); one barrier; phase 2 -- every thread accumulates its slice
 // of y += h * W_down[n] over all pairs, 8 rows in flight, no barrier.
 template <class T, int VPT, int VPL, int PIF, int PB2, bool EXACT>
-__global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
+__global__ void __launch_bounds__(UD_THREADS, 4) updown_fused_kernel(UDParams p) {
   pdl_begin();
   constexpr int EV = Vec<T>::EV;
   __shared__ int s_n[LIST_CAP];
@@ -127,16 +139,24 @@ __global__ void __launch_bounds__(256, 2) updown_fused_kernel(UDParams p) {
           // exact rows: load the (valid, clamped) row unconditionally, discard its dot
           warp_row<VPL, L2_NORMAL, EXACT>(Wu4 + (size_t)s_n[i < P ? i : i0] * NV, NV, EXACT || i < P, wr[q]);
         }
-        uint4 xw[VPL];
+        // x_t: with one row in flight per warp it is read from shared memory
+        // vector by vector inside the dot (no registers held for it across
+        // the row loads); with two, once into registers for both rows
+        constexpr bool XS = PIF == 1;
+        uint4 xw[XS ? 1 : VPL];
+        if (!XS) {
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-          const int vi = lane + 32 * k;
-          xw[k] = (EXACT || vi < NV) ? s_x[vi] : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < VPL; ++k) {
+            const int vi = lane + 32 * k;
+            xw[k] = (EXACT || vi < NV) ? s_x[vi] : make_uint4(0, 0, 0, 0);
+          }
         }
 #pragma unroll
         for (int q = 0; q < PIF; ++q) {
           const int i = i0 + q * nw;
-          const float u = warp_dot<T, VPL>(xw, wr[q]);
+          float u;
+          if constexpr (XS) u = warp_dot_smem<T, VPL>(s_x, NV, wr[q]);
+          else u = warp_dot<T, VPL>(reinterpret_cast<const uint4(&)[VPL]>(xw), wr[q]);
           if (lane == 0 && i < P) {
             s_g[i] *= u;  // h = g * u, in place
             if (p.train) {
@@ -203,10 +223,10 @@ cudaError_t launch_updown_fused(const FwdArgs &a, cudaStream_t s, int *launches)
     for (int ph = two ? 1 : 0; ph <= (two ? 2 : 0); ++ph) {                                    \
       p.phase = ph;                                                                            \
       if (NV == 32 * (L) && NV == VPT_ * UD_THREADS)                                           \
-        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 24 / VPT_, true>, a.T,      \
+        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), exact_rows<VPT_>(), true>, a.T,  \
                  UD_THREADS, 0, s, p);                                                         \
       else                                                                                     \
-        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), 16 / VPT_, false>, a.T,     \
+        launch_k(updown_fused_kernel<TT, VPT_, L, (L <= 8 ? 2 : 1), generic_rows<VPT_>(), false>, a.T, \
                  UD_THREADS, 0, s, p);                                                         \
     }                                                                                          \
   } while (0)
