@@ -188,8 +188,9 @@ float switch_of(const twell_t *tw) { return tw->dense_switch > 0.f ? tw->dense_s
 // shared gate GEMM (the up and down GEMMs) at ~1.3 PFLOP/s: measured
 // crossover ~1.3% at d_model 2048 / d_ff 8192.  When the gathered matrices
 // exceed L2 the forward's gathers slow down even in two passes (d_model
-// 4096 / d_ff 14336 bf16: 235 MB, ~10 TB/s, crossover ~0.65%), so its
-// default scales by L2 / their bytes.  The backward gathers five rows per
+// 4096 / d_ff 14336 bf16: 235 MB, ~13 TB/s; measured crossover ~0.9%: at
+// 0.49% active 1.26 ms against 1.71 for the dense path, at 0.99% 1.76
+// against 1.71), so its default is then 0.7 of the in-L2 one.  The backward gathers five rows per
 // pair where its dense path does 6 GEMM units against the forward's 2 (dh,
 // the two dx products, the three weight gradients): its crossover is
 // (6/2) / (5/2) = 1.2 times the forward's unscaled one, with no L2 scaling:
@@ -204,7 +205,7 @@ float density_of(const twell_t *tw, int D, int gated, bool backward) {
   const double wbytes = (double)(gated ? 2 : 1) * (double)tw->F * (double)D * (double)es;
   const double l2 = (double)l2_size();
   double d = 0.013;
-  if (l2 > 0.0 && wbytes > l2) d *= l2 / wbytes;
+  if (l2 > 0.0 && wbytes > l2) d *= 0.7;
   return (float)d;
 }
 

@@ -111,9 +111,9 @@ typedef struct {
                              gathers cost more than dense GEMMs.  0 selects
                              the measured crossover: in the forward 0.013
                              when the gathered weights (W_up + W_down) fit
-                             in L2, scaled by L2 / their bytes when they do
-                             not; in the backward 0.0156 (its gathers run in
-                             L2-sized passes); < 0 disables this test.
+                             in L2, 0.0091 when they do not; in the backward
+                             0.0156 (its gathers run in L2-sized passes);
+                             < 0 disables this test.
                              The backward applies the same rules to the
                              saved TwELL.                                    */
   float dh_density;       /* backward, bf16 on the tensor-core path: when the
