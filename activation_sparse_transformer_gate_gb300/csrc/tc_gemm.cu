@@ -359,6 +359,51 @@ __device__ __forceinline__ void fetch_slots(const TcParams &p, int col, int tok,
   load_slots(p.idx + jt * p.Kslots, p.val + jt * p.Kslots, p.Kslots, iw, vw);
 }
 
+// EPI_DHS with two 128-column TwELL tiles per output tile and K <= 8: what
+// one row needs of both tiles (its dense-backup position, and per tile the
+// count, the slot indices, g and u at the slots), in compact registers.
+struct DhsSlots {
+  int ps, nz0, nz1;
+  uint32_t i0[2], v0[4], q0[4], i1[2], v1[4], q1[4];
+};
+
+__device__ __forceinline__ void dhs_fetch(const TcParams &p, int tok, bool row_ok, int n0,
+                                          DhsSlots &S) {
+  S.ps = row_ok ? p.pos[tok] : -1;
+  S.nz0 = S.nz1 = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) S.i0[i] = S.i1[i] = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S.v0[i] = S.q0[i] = S.v1[i] = S.q1[i] = 0u;
+  if (!row_ok || S.ps >= 0) return;
+  uint32_t iw[8], vw[16];
+  const size_t j0 = (size_t)(n0 / 128) * p.Tn + tok;
+  S.nz0 = p.nnz[j0];
+  load_idx(p.idx + j0 * p.Kslots, p.Kslots, iw);
+  S.i0[0] = iw[0]; S.i0[1] = iw[1];
+  load_vals(p.val + j0 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S.v0[i] = vw[i];
+  if (p.gated) {
+    load_vals(p.uval + j0 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S.q0[i] = vw[i];
+  }
+  if (n0 + 128 >= p.N) return;
+  const size_t j1 = j0 + p.Tn;
+  S.nz1 = p.nnz[j1];
+  load_idx(p.idx + j1 * p.Kslots, p.Kslots, iw);
+  S.i1[0] = iw[0]; S.i1[1] = iw[1];
+  load_vals(p.val + j1 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S.v1[i] = vw[i];
+  if (p.gated) {
+    load_vals(p.uval + j1 * p.Kslots, p.Kslots, vw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S.q1[i] = vw[i];
+  }
+}
+
 // EPI_DHS: the gradients of one TwELL tile's slots (tile j, row tok) from dh
 // at the slots, as the gather SDDMM finishes an entry: h = g u, dh += lambda
 // sign(h), dz = [g > 0] dh u, du = [g > 0] dh g (plain FFN: u = 1), stored
@@ -709,6 +754,19 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // accumulator row of this thread
     const int et = threadIdx.x - 64;        // 0..127 among epilogue threads
+    // EPI_DHS with two 128-column TwELL tiles per output tile and K <= 8:
+    // each row's slot data is fetched one output tile ahead (while the
+    // previous tile is processed), so its latency is hidden even when the
+    // epilogue, not the MMAs, sets the pace
+    const bool pf2 = EPI == EPI_DHS && BN == 256 && p.C == 128 && p.Kslots <= 8;
+    DhsSlots dcur, dnxt;
+    auto dhs_fetch_tile = [&](int t_, DhsSlots &S) {
+      int mb_, nb_;
+      tile_mn(t_ - (t_ / tiles_q) * tiles_q, m_blocks, n_blocks, gm, mb_, nb_);
+      const int m_ = mb_ * BM + row;
+      dhs_fetch(p, m_, m_ < M, nb_ * BN, S);
+    };
+    if (pf2 && (int)blockIdx.x < num_tiles) dhs_fetch_tile(blockIdx.x, dcur);
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
       const int q = tile / tiles_q;
@@ -731,34 +789,14 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
       // row (ps >= 0) read that instead
       constexpr bool SLOTS = EPI == EPI_U || EPI == EPI_DH || EPI == EPI_DHS;
       const int tok_u = (SLOTS && row_ok) ? ((dense_all || EPI == EPI_DHS) ? m : p.rows[m]) : 0;
-      const int ps_u = ((EPI == EPI_DH || EPI == EPI_DHS) && row_ok) ? p.pos[tok_u] : -1;
+      const int ps_u = ((EPI == EPI_DH || (EPI == EPI_DHS && !pf2)) && row_ok) ? p.pos[tok_u] : -1;
       int pf_nz = 0;
       uint32_t pf_iw[8], pf_vw[16], pf_qw[16] = {};  // (pf_qw: plain FFN leaves it zero)
-      if (SLOTS && row_ok && ps_u < 0) {
+      if (pf2 && tile + (int)gridDim.x < num_tiles) dhs_fetch_tile(tile + gridDim.x, dnxt);
+      if (SLOTS && row_ok && ps_u < 0 && !pf2) {
         fetch_slots(p, n0, tok_u, pf_nz, pf_iw, pf_vw);
         if ((EPI == EPI_DH || EPI == EPI_DHS) && p.gated)
           load_vals(p.uval + ((size_t)(n0 / p.C) * p.Tn + tok_u) * p.Kslots, p.Kslots, pf_qw);
-      }
-      // EPI_DHS with two 128-column TwELL tiles per output tile and K <= 8:
-      // the second tile's slots are fetched here as well, into a compact set
-      // (two full sets would not fit the register budget)
-      const bool pf2 = EPI == EPI_DHS && BN == 256 && p.C == 128 && p.Kslots <= 8;
-      int pf2_nz = 0;
-      uint32_t pf2_i[2] = {0u, 0u}, pf2_v[4] = {0u, 0u, 0u, 0u}, pf2_q[4] = {0u, 0u, 0u, 0u};
-      if (pf2 && row_ok && ps_u < 0 && n0 + 128 < p.N) {
-        const size_t jt2 = (size_t)((n0 + 128) / 128) * p.Tn + tok_u;
-        uint32_t iw[8], vw[16];
-        pf2_nz = p.nnz[jt2];
-        load_idx(p.idx + jt2 * p.Kslots, p.Kslots, iw);
-        pf2_i[0] = iw[0]; pf2_i[1] = iw[1];
-        load_vals(p.val + jt2 * p.Kslots, p.Kslots, vw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pf2_v[i] = vw[i];
-        if (p.gated) {
-          load_vals(p.uval + jt2 * p.Kslots, p.Kslots, vw);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) pf2_q[i] = vw[i];
-        }
       }
       // Each epilogue thread waits (bounded) for the accumulator; the AND of
       // the outcomes is taken at a barrier, so if any thread gave up (or
@@ -1117,19 +1155,16 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
         // 11 us although the epilogue overlaps the next tile's MMAs, so only
         // live slots are stored: 102.6 -> 99.0 us.)
         const int tok = m;
-        const int ps = ps_u;
+        const int ps = pf2 ? dcur.ps : ps_u;
         const bool skip = !row_ok || ps >= p.cap || (ps >= 0 && p.ctl->ovf_gemm);
         const int K = p.Kslots;
         float *st = (float *)s_slots + row * DHS_STRIDE;
         const int nch = (p.Tn + TR_CHUNK - 1) / TR_CHUNK;
         if (pf2) {
           const bool two = n0 + 128 < p.N;  // uniform: the second TwELL tile exists
-          const uint32_t i0[2] = {pf_iw[0], pf_iw[1]};
-          const uint32_t v0[4] = {pf_vw[0], pf_vw[1], pf_vw[2], pf_vw[3]};
-          const uint32_t q0[4] = {pf_qw[0], pf_qw[1], pf_qw[2], pf_qw[3]};
-          const int nz0 = min(pf_nz, K), nz1 = min(pf2_nz, K);
+          const int nz0 = min(dcur.nz0, K), nz1 = min(dcur.nz1, K);
           const uint32_t blk =
-              dhs_blocks<8>(i0, K, nz0, 128) | (dhs_blocks<8>(pf2_i, K, nz1, 128) << 4);
+              dhs_blocks<8>(dcur.i0, K, nz0, 128) | (dhs_blocks<8>(dcur.i1, K, nz1, 128) << 4);
           float d0[8], d1[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) d0[k] = d1[k] = 0.f;
@@ -1141,18 +1176,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcParams p) {
             if (skip) continue;
             if (ps >= 0) dhs_store_row_block(p, ps, n0 + cb, v);
             else if ((blk >> (cb >> 5)) & 1u) {
-              if (cb < 128) dhs_pick<8>(st, v, cb, K, nz0, i0, d0);
-              else dhs_pick<8>(st, v, cb - 128, K, nz1, pf2_i, d1);
+              if (cb < 128) dhs_pick<8>(st, v, cb, K, nz0, dcur.i0, d0);
+              else dhs_pick<8>(st, v, cb - 128, K, nz1, dcur.i1, d1);
             }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
           if (!skip && ps < 0) {
-            dhs_store_slots<8>(p, n0 / 128, tok, K, nz0, i0, v0, q0, d0, nch);
-            if (two) dhs_store_slots<8>(p, n0 / 128 + 1, tok, K, nz1, pf2_i, pf2_v, pf2_q, d1, nch);
+            dhs_store_slots<8>(p, n0 / 128, tok, K, nz0, dcur.i0, dcur.v0, dcur.q0, d0, nch);
+            if (two)
+              dhs_store_slots<8>(p, n0 / 128 + 1, tok, K, nz1, dcur.i1, dcur.v1, dcur.q1, d1, nch);
           }
-          continue;  // the buffer is released
+          dcur = dnxt;  // the next tile's slots (fetched before this tile's wait)
+          continue;     // the buffer is released
         }
         for (int jt = 0; jt < BN / p.C; ++jt) {
           const int n1 = n0 + jt * p.C;
