@@ -806,7 +806,13 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
   const bool dw_split = a.tw.gather_passes > 0 ? a.tw.gather_passes > 1
                                                : dw_set > 0.5 * (double)l2_size();
   const int dw_passes = gather_passes(a.tw.gather_passes, dw_set, NV, GATHER_MIN_WIDTH);
-#define TW_VPT(K, TT, G, SS, NPASS, EXTRA)                                                     \
+// NB2: batches of two rows (instead of four) in the exact 128-thread shape:
+// fewer registers, five CTAs per SM instead of four.  Measured better where
+// the rows come partly from DRAM (passes over a working set beyond L2: dx
+// at d_model 4096, 0.678 -> 0.659 ms) and for the split dW launches (0.707
+// -> 0.672 ms at d_model 4096, 0.689 -> 0.665 at d_model 2048 / 16384
+// tokens); worse at d_model 2048 / 4096 tokens (dx 0.186 -> 0.194 ms).
+#define TW_VPT(K, TT, G, SS, NPASS, EXTRA, NB2)                                                \
   do {                                                                                         \
     for (int i_ = 0; i_ < (NPASS); ++i_) {                                                     \
       p.v0 = (int)((long)NV * i_ / (NPASS));                                                   \
@@ -815,6 +821,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
       const int vpt = np_ <= 64 ? 1 : np_ <= 512 ? 2 : 4;                                      \
       const int threads = ((np_ + vpt - 1) / vpt + 31) / 32 * 32;                              \
       if (vpt == 1) launch_k(K<TT, 1, 8, 0 EXTRA>, G, threads, 0, SS, p);                      \
+      else if (vpt == 2 && np_ == 256 && (NB2)) launch_k(K<TT, 2, 2, 128 EXTRA>, G, 128, 0, SS, p); \
       else if (vpt == 2 && np_ == 256) launch_k(K<TT, 2, 4, 128 EXTRA>, G, 128, 0, SS, p);     \
       else if (vpt == 2) launch_k(K<TT, 2, 3, 0 EXTRA>, G, threads, 0, SS, p);                 \
       else launch_k(K<TT, 4, 2, 0 EXTRA>, G, threads, 0, SS, p);                               \
@@ -839,8 +846,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
     return r;
   };
   auto dx_spmm = [&]() {
-    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s, dx_passes, );
-    else TW_VPT(bwd_dx_kernel, float, a.T, s, dx_passes, );
+    if (bf) TW_VPT(bwd_dx_kernel, bf16, a.T, s, dx_passes, , dx_passes > 1);
+    else TW_VPT(bwd_dx_kernel, float, a.T, s, dx_passes, , dx_passes > 1);
     const cudaError_t r = cudaGetLastError();
     prof_mark(KID_BWD_DX, s, dx_passes);
     return r;
@@ -859,15 +866,15 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t s) {
 #define TW_PART2 , 2
     if (dw_split) {  // x rows (dW_gate, dW_up, dbg), then dy rows (dW_down)
       if (bf) {
-        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART1);
-        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART2);
+        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART1, true);
+        TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART2, true);
       } else {
-        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART1);
-        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART2);
+        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART1, true);
+        TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART2, true);
       }
     } else {
-      if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART0);
-      else TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART0);
+      if (bf) TW_VPT(bwd_dw_kernel, bf16, a.F, sw, dw_passes, TW_PART0, false);
+      else TW_VPT(bwd_dw_kernel, float, a.F, sw, dw_passes, TW_PART0, false);
     }
 #undef TW_PART0
 #undef TW_PART1
