@@ -170,6 +170,32 @@ __device__ __forceinline__ float warp_dot_smem(const uint4 *s_a, int NV, const u
   return s;
 }
 
+// warp_dot_smem without the final reduction: adds the products of vectors
+// lane + 32 k (k < VPL) of s_a (zero past NV) and b into the lane's two
+// partial sums, so a long row can be taken in parts with the same order of
+// additions as in one piece.
+template <class T, int VPL>
+__device__ __forceinline__ void warp_dot_smem_acc(const uint4 *s_a, int NV, const uint4 (&b)[VPL],
+                                                  float &s0, float &s1) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) {
+    const int vi = lane + 32 * k;
+    const uint4 a = vi < NV ? s_a[vi] : make_uint4(0, 0, 0, 0);
+    if constexpr (Vec<T>::EV == 8) {
+      s0 = dot2_bf16(a.x, b[k].x, s0);
+      s1 = dot2_bf16(a.y, b[k].y, s1);
+      s0 = dot2_bf16(a.z, b[k].z, s0);
+      s1 = dot2_bf16(a.w, b[k].w, s1);
+    } else {
+      s0 = fmaf(__uint_as_float(a.x), __uint_as_float(b[k].x), s0);
+      s1 = fmaf(__uint_as_float(a.y), __uint_as_float(b[k].y), s1);
+      s0 = fmaf(__uint_as_float(a.z), __uint_as_float(b[k].z), s0);
+      s1 = fmaf(__uint_as_float(a.w), __uint_as_float(b[k].w), s1);
+    }
+  }
+}
+
 // Where the active pairs of one (row, tile) come from.  Rows whose tiles all
 // fit their K slots read the TwELL slots; an overflow row reads a dense vector
 // of C ReLU values for each tile (the wide-tile buffer in the forward, the

@@ -39,12 +39,12 @@ namespace {
 constexpr int UD_THREADS = 128;  // 4 warps per token CTA
 // Rows of W_down in flight per batch of the down phase, exact row shapes:
 // 24 / VPT vectors per thread (12 rows at d_model 2048 bf16), but 4 rows
-// at VPT 4 and 2 at VPT 8, where more spill registers: at d_model 4096 the
+// at VPT 4 and 1 at VPT 8, where more spill registers: at d_model 4096 the
 // 6-row batch spilled and 4 rows took the kernel from 0.93 to 0.74 ms
 // (config 4, 0.49% active).  At d_model 2048, 8 or 6 rows with five CTAs
 // per SM were slower than 12 with four (0.194 -> 0.211 / 0.222 ms).
 template <int VPT>
-constexpr int exact_rows() { return VPT == 4 ? 4 : VPT == 8 ? 2 : 24 / VPT; }
+constexpr int exact_rows() { return VPT == 4 ? 4 : VPT == 8 ? 1 : 24 / VPT; }
 // Rows in flight for the other shapes (predicated loads): 16 / VPT, one at
 // VPT 8 (d_model 8192 bf16), where two spill.
 template <int VPT>
@@ -130,7 +130,32 @@ __global__ void __launch_bounds__(UD_THREADS, 4) updown_fused_kernel(UDParams p)
       for (int i = tid; i < P; i += blockDim.x)
         if (s_slot[i] != PAD_SLOT) ((T *)p.g_fb)[(size_t)ps * p.F + s_n[i]] = from_f<T>(s_g[i]);
     // ---- phase 1: u and h of every pair, one warp per pair ------------------
-    if (p.gated && !down_only) {
+    if (p.gated && !down_only && VPL > 16) {
+      // rows of more than 16 vectors per lane (d_model 8192 bf16): one row
+      // per warp, loaded and dotted 16 vectors per lane at a time (the whole
+      // row in registers would spill); the partial sums run in one order
+      for (int i = w; i < P; i += nw) {
+        const uint4 *row = Wu4 + (size_t)s_n[i] * NV;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+        for (int h = 0; h < VPL; h += 16) {
+          uint4 wr[16];
+          warp_row<16, L2_NORMAL, EXACT>(row + 32 * h, NV - 32 * h, true, wr);
+          warp_dot_smem_acc<T, 16>(s_x + 32 * h, NV - 32 * h, wr, s0, s1);
+        }
+        float u = s0 + s1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+        if (lane == 0) {
+          s_g[i] *= u;  // h = g * u, in place
+          if (p.train) {
+            const int sl = s_slot[i];
+            if (sl >= 0) ((T *)p.u_val)[sl] = from_f<T>(u);
+            else if (fb && sl != PAD_SLOT) ((T *)p.u_fb)[(size_t)ps * p.F + (-1 - sl)] = from_f<T>(u);
+          }
+        }
+      }
+    } else if (p.gated && !down_only) {
       for (int i0 = w; i0 < P; i0 += nw * PIF) {
         uint4 wr[PIF][VPL];
 #pragma unroll
