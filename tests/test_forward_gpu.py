@@ -310,6 +310,20 @@ def test_config2_full_size_sampled():
     assert abs(frac - 0.0099) < 0.001, frac
 
 
+def test_config2_full_size_every_row():
+    """Config 2 at full size, every token compared: the TwELL slots, counts
+    and overflow list of all 4096 rows, and y over the whole tensor, so every
+    tile of the persistent gate GEMM's grid and every token CTA of the
+    gathers is checked, not a sample."""
+    w = synth.config2()
+    a = synth.generate(w)
+    g = run_forward(a, w)
+    assert g["code"] == 0
+    # activity decisions whose exact z lies within fp32 rounding of 0 may go
+    # either way: expected a few among the 33.5 M entries
+    check_forward(a, w, g, max_ambiguous=64)
+
+
 def test_config3_full_size_hot_rows():
     w = synth.config3()
     a = synth.generate(w)
