@@ -343,20 +343,23 @@ def measure(torch, lib, b, timed, per_step, flush_buf, args, steps, w_key, full=
 
 
 SWEEP = ("c2", "c3", "c4:-1.28:8", "c4:-1.64:8", "c4:-2.33:8", "c4:-2.58:8", "c1")
+# training steps of the larger workloads beside the headline one
+SWEEP_TRAIN = ("c3", "c4:-2.58:8", "c4:-2.33:8")
 
 
 def sweep(torch, tw, lib, dev, args, timed, per_step, flush_buf):
     """Compact records of the inference forward of the other workloads (the
-    pages' shapes), each with its own dominant-kernel roofline and the two
-    dense cuBLAS arms on the same inputs."""
+    pages' shapes) and of the training step of the larger ones, each with
+    its own dominant-kernel roofline and the two dense cuBLAS arms on the
+    same inputs."""
     out = {}
-    for key in SWEEP:
-        w = workload_of(key, False)
-        b = Bench(torch, tw, w, False, dev, args)
-        rec, _, _, _, _ = measure(torch, lib, b, timed, per_step, flush_buf, args, 30, key,
-                                  full=False)
-        rec = {"workload": describe(w, False), "dtype": w.dtype, **rec}
-        out[f"{key}:fwd"] = rec
+    for key, train in [(k, False) for k in SWEEP] + [(k, True) for k in SWEEP_TRAIN]:
+        w = workload_of(key, train)
+        b = Bench(torch, tw, w, train, dev, args)
+        rec, _, _, _, _ = measure(torch, lib, b, timed, per_step, flush_buf, args,
+                                  20 if train else 30, key, full=False)
+        rec = {"workload": describe(w, train), "dtype": w.dtype, **rec}
+        out[f"{key}:{'train' if train else 'fwd'}"] = rec
         del b
         torch.cuda.empty_cache()
     return out
