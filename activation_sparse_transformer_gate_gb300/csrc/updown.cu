@@ -41,8 +41,9 @@ constexpr int UD_THREADS = 128;  // 4 warps per token CTA
 // 24 / VPT vectors per thread (12 rows at d_model 2048 bf16), but 4 rows
 // at VPT 4 and 1 at VPT 8, where more spill registers: at d_model 4096 the
 // 6-row batch spilled and 4 rows took the kernel from 0.93 to 0.74 ms
-// (config 4, 0.49% active).  At d_model 2048, 8 or 6 rows with five CTAs
-// per SM were slower than 12 with four (0.194 -> 0.211 / 0.222 ms).
+// (8192 tokens, d_ff 14336, 0.49% active).  At d_model 2048, 8 or 6 rows
+// with five CTAs per SM were slower than 12 with four (0.194 -> 0.211 /
+// 0.222 ms at 4096 tokens, d_ff 8192).
 template <int VPT>
 constexpr int exact_rows() { return VPT == 4 ? 4 : VPT == 8 ? 1 : 24 / VPT; }
 // Rows in flight for the other shapes (predicated loads): 16 / VPT, one at
