@@ -646,10 +646,17 @@ def kernel_rooflines(kern, w, nnz, train, rows_f=0, rows_b=0, dh_gemm=False):
 
 
 def kernel_source_hash() -> str:
+    """Hash of the library's sources with comments and blank space removed,
+    so that a capture stays matched to its kernels across comment edits."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "activation_sparse_transformer_gate_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"\s+", " ", text)
+        h.update(f.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 
