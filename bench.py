@@ -282,6 +282,10 @@ def dominant_roofline(kern, rl, workload, train, gceil):
         return None
     r = rl[dominant]
     traffic = traffic_for(dominant, workload, train)
+    src = "random-row gather probe on the same matrix and pair count"
+    if isinstance(gceil, dict):  # per kernel: the rows it gathers (weight or token rows)
+        src = gceil.get("_source", {}).get(dominant, src)
+        gceil = gceil.get(dominant)
     if r["bound"] != "hbm" or not gceil:
         return {"kernel": dominant, "bound": r["bound"], "achieved": round(r["achieved"], 2),
                 "peak": r["peak"], "unit": r["unit"], "frac": round(r["frac"], 4),
@@ -293,8 +297,8 @@ def dominant_roofline(kern, rl, workload, train, gceil):
     return {"kernel": dominant, "bound": "l2", "achieved": round(r["achieved"], 2),
             "peak": round(gceil, 1), "unit": "GB/s", "frac": round(r["achieved"] / gceil, 4),
             "traffic": traffic,
-            "peak_source": "measured in this run: random-row gather probe on the same matrix "
-                           "and pair count (the memory level that serves these gathers)",
+            "peak_source": f"measured in this run: {src} (the memory level that serves these "
+                           "gathers)",
             "hbm": hbm}
 
 
@@ -316,24 +320,34 @@ def measure(torch, lib, b, timed, per_step, flush_buf, args, steps, w_key, full=
     nnz = b.bufs.nnz.cpu().numpy().astype(np.int64)
     rows_f, rows_b, dh_gemm = b.dispatch()
     rl = kernel_rooflines(kern, w, nnz, train, rows_f, rows_b, dh_gemm)
-    gceil = None
+    gceil = gceil_x = None
     if any(r.get("bound") == "hbm" for k, r in rl.items() if not k.startswith("_")):
+        # weight rows (up/down, dh, dx) and, for the weight-gradient gather,
+        # token rows of x (the rows it gathers: x and dy, T x d_model each)
         gceil = gather_ceiling(torch, b.dev, b.d["Wu"] if w.gated else b.d["Wd"], w,
                                rl["_counts"]["pairs_all"], timed, b.sh)
-        if gceil:
-            for k, r in rl.items():
-                if r.get("bound") == "hbm":
-                    r["frac_of_l2_gather"] = r["achieved"] / gceil
+        if "bwd_dw_gather" in rl:
+            gceil_x = gather_ceiling(torch, b.dev, b.d["x"], w, rl["_counts"]["pairs_all"], timed,
+                                     b.sh, n_rows=w.T)
+        for k, r in rl.items():
+            c = gceil_x if k == "bwd_dw_gather" else gceil
+            if r.get("bound") == "hbm" and c:
+                r["frac_of_l2_gather"] = r["achieved"] / c
+    ceilings = dict({k: gceil for k in rl if not k.startswith("_")},
+                    bwd_dw_gather=gceil_x,
+                    _source={"bwd_dw_gather": "random-row gather probe on x (token rows, as this "
+                                              "kernel gathers x and dy rows), same pair count"})
     dense = None if args.no_dense else dense_arms(torch, b.d, w, train, timed, args, steps)
     row_ovf = (nnz > w.K).any(axis=0)
     rec = {"ms_per_step": round(ms, 5), "median_ms": round(med, 5),
            "tokens_per_s": round(w.T / (ms / 1e3), 1),
-           "roofline": dominant_roofline(kern, rl, w_key, train, gceil),
+           "roofline": dominant_roofline(kern, rl, w_key, train, ceilings),
            "path": {"forward_all_dense": bool(rows_f >= w.T), "forward_dense_rows": rows_f,
                     "backward_dense_rows": rows_b if train else None,
                     "backward_dh_gemm": dh_gemm if train else None},
            "sparsity": {"active_frac": float(nnz.sum() / (w.T * w.F)), "n_ovf": int(row_ovf.sum())},
-           "l2_gather_gbs": round(gceil, 1) if gceil else None}
+           "l2_gather_gbs": round(gceil, 1) if gceil else None,
+           "l2_gather_token_rows_gbs": round(gceil_x, 1) if gceil_x else None}
     if dense:
         rec["dense_cublas"] = dense["eager"]
         rec["dense_gemm_only"] = dense["gemm_only"]
@@ -489,6 +503,7 @@ def run_ours(args, rank, world, local_rank):
         "sparsity": rec["sparsity"],
         "path": rec["path"],
         "l2_gather_gbs": rec["l2_gather_gbs"],
+        "l2_gather_token_rows_gbs": rec["l2_gather_token_rows_gbs"],
         "memory": mem,
         "energy": energy,
     }
@@ -528,15 +543,17 @@ def fp32_alu_tflops() -> float:
     return 152 * 128 * 2 * 2.07e9 / 1e12
 
 
-def gather_ceiling(torch, dev, W, w, pairs, timed, sh):
-    """GB/s at which the GPU gathers `pairs` rows of W (F x d_model, bf16) in
-    a uniform random order with plain 16-byte loads: the measured ceiling
-    for the sparse kernels' row gathers (L2-served when W fits in L2), timed
-    like the step (events on the stream, L2 flushed before every run)."""
+def gather_ceiling(torch, dev, W, w, pairs, timed, sh, n_rows=None):
+    """GB/s at which the GPU gathers `pairs` rows of W (n_rows x d_model,
+    default F rows) in a uniform random order with plain 16-byte loads: the
+    measured ceiling for the sparse kernels' row gathers (L2-served when W
+    fits in L2), timed like the step (events on the stream, L2 flushed
+    before every run)."""
     if pairs < 1:
         return None
     rng = np.random.default_rng(7)
-    rows = torch.from_numpy(rng.integers(0, w.F, size=pairs).astype(np.int32)).to(dev)
+    n_rows = w.F if n_rows is None else n_rows
+    rows = torch.from_numpy(rng.integers(0, n_rows, size=pairs).astype(np.int32)).to(dev)
     blocks = 6 * torch.cuda.get_device_properties(dev).multi_processor_count
     out = torch.empty((blocks * 8,), dtype=torch.int32, device=dev)
     hooks = tw_hooks()

@@ -80,3 +80,18 @@ def test_fp32_gate_gemm_is_rated_on_the_alu_peak():
     twell = (w.F // w.C) * w.T * (5 * w.K + 1)
     want = pairs * w.D * 4 + w.T * w.D * 4 + twell
     assert rl["twell_updown_fused"]["algorithmic"] == want
+
+
+def test_dw_gather_is_read_against_its_own_rows_probe():
+    """Per-kernel ceilings: the weight-gradient gather (token rows of x and
+    dy) is rated on the token-row probe, the others on the weight-row one."""
+    w, nnz = small_case()
+    kern = kern_times(["bwd_dw_gather", "bwd_dx_spmm"], 0.01)
+    kern["bwd_dw_gather"]["ms_per_step"] = 0.2
+    rl = bench.kernel_rooflines(kern, w, nnz, True, 0, 0)
+    alg = rl["bwd_dw_gather"]["achieved"]
+    ceil = {"bwd_dw_gather": 4 * alg, "bwd_dx_spmm": 2 * alg,
+            "_source": {"bwd_dw_gather": "token rows"}}
+    r = bench.dominant_roofline(kern, rl, "c2", True, ceil)
+    assert r["kernel"] == "bwd_dw_gather" and abs(r["frac"] - 0.25) < 1e-3
+    assert "token rows" in r["peak_source"]
