@@ -191,7 +191,28 @@ def test_malformed_index_is_reported(_lib, path):
     assert backward() == -5                            # TWELL_ERR_INDEX
     bufs.idx[j, t, k] = old                            # repaired: same results as before
     assert backward() == 0
-    for a, b in zip(ref[:3], (dx, dW[0], dW[2])):
+    for a, b in zip(ref, (dx, dW[0], dW[2], dbg)):
         assert torch.equal(a, b)
-    # (the dense-row path sums dbg's per-warp partials with atomics: order only)
-    assert torch.allclose(ref[3], dbg, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("scale, want", [(16.0, -11), (1.0, 0)])
+def test_fp16_range_is_reported(_lib, scale, want):
+    """The dense-path GEMMs take fp16 operands: h = g u beyond 65504 (x = 16,
+    unit weights, d_model 64: g = u = 1024) is refused with TWELL_ERR_RANGE;
+    the same call with x = 1 (h = 4096) runs clean."""
+    T, D, F, C, K = 128, 64, 256, 64, 8
+    bf = torch.bfloat16
+    x = torch.full((T, D), scale, dtype=bf, device="cuda")
+    Wg = torch.ones((F, D), dtype=bf, device="cuda")
+    Wu = torch.ones((F, D), dtype=bf, device="cuda")
+    Wd = torch.full((F, D), 1.0 / 256, dtype=bf, device="cuda")
+    bg = torch.zeros((F,), dtype=torch.float32, device="cuda")
+    bufs = tw.TwellBuffers(T, F, C, K, tw.TWELL_BF16, dense_density=1e-9)
+    ws, nws = tw.workspace(T, D, F, C, K, tw.TWELL_BF16, False)
+    y = torch.empty((T, D), dtype=bf, device="cuda")
+    tw.twell_ffn_forward(x, Wg, bg, None, Wu, Wd, D, 0, bufs.t, y, ws, nws)
+    code, n_ovf = tw.twell_get_status(bufs.t)
+    assert n_ovf == T            # every tile holds 64 > K active columns
+    assert code == want
+    if want == 0:                # h = 4096 at every entry: y = 4096 * 256 / 256
+        assert torch.equal(y, torch.full_like(y, 4096.0))
